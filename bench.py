@@ -1,0 +1,407 @@
+"""Benchmark: DeepSelect row-wise top-k on GB300, effective input HBM bandwidth.
+
+Workload (the DSA-indexer shape): 64 rows x 131,072 bf16 scores, i.i.d. N(0,1), row
+stride 131,072 elements (256 KiB, a multiple of 1024 bytes), k=512, B=B2=4096.  One step
+is one ds_topk call over the whole batch (every step of the method runs in the CUDA
+kernels).  value = rows*N*2 bytes per step / device time per step, in decimal GB/s,
+summed over ranks (each rank runs its own copy: rows are independent, weak scaling).
+
+Timing: W warm-up steps, then exactly K steps captured in CUDA graphs and replayed on one
+stream, bracketed by a barrier and torch.cuda.synchronize(), timed with CUDA events on
+that stream.  Inputs rotate over R device copies whose total exceeds 4x the L2, so each
+step reads its input from HBM.  SM clocks are sampled with nvidia-smi during the timed
+region.
+
+e2e: the same metric through the public API with host buffers: every step copies the
+step's input from pinned host memory, runs ds_topk, and reads the results back.
+
+--impl reference: the oracle (the CPU transcription of the method, oracle/) timed on
+this host's cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective input HBM GB/s (rows·N·bytes/time) at k=512; % of GB300 HBM peak"
+ROWS, N, K_TOP, B, B2 = 64, 131072, 512, 4096, 4096
+SEED = 0x5EED
+WORKLOAD = f"indexer_bf16: {ROWS} rows x {N} bf16 N(0,1), stride {N}, k={K_TOP}, B={B}, B2={B2}"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ds_scan_kernel_indexer_bf16.md")
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "top_selection_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_from_profile():
+    """dram bytes per launch recorded by the last ncu capture of this kernel, if the
+    kernel sources have not changed since."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            text = f.read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line and line.split(":", 1)[0].strip() in ("traffic_bytes_per_launch", "source_digest"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("source_digest") != _source_digest():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def _cpu_oracle(seconds: float, threads: int | None = None):
+    """The oracle's DeepSelect transcription over the workload's rows on this host's
+    cores, repeated for about `seconds`."""
+    import oracle
+    import synth
+    w = synth.indexer_bf16()
+    th = threads or oracle.max_threads()
+    oracle.deepselect(w.x[:4], w.dtype, K_TOP, B, B2, SEED, threads=th)   # build / warm
+    t0 = time.perf_counter()
+    runs = 0
+    while True:
+        oracle.deepselect(w.x, w.dtype, K_TOP, B, B2, SEED + runs, threads=th)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = runs * w.input_bytes / el / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": th, "kind": "oracle",
+            "sample": f"oracle DeepSelect transcription (C, OpenMP over rows) on the full {ROWS}x{N} bf16 "
+                      f"batch, {runs} runs in {el:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step runs the oracle's DeepSelect
+    transcription on a sample of the workload (a prefix of its rows, or of one row),
+    sized so that the whole run stays within about two minutes of CPU time."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import oracle
+    import synth
+    w = synth.indexer_bf16()
+    th = oracle.max_threads()
+    steps = max(1, args.steps)
+    t0 = time.perf_counter()
+    oracle.deepselect(w.x, w.dtype, K_TOP, B, B2, SEED, threads=th)
+    t_full = time.perf_counter() - t0
+    budget = 120.0
+    rows_ps, n_ps = ROWS, N
+    if steps * t_full > budget:
+        rows_ps = max(1, int(ROWS * budget / (steps * t_full)))
+        if rows_ps == 1:
+            t_row = t_full * th / ROWS
+            n_ps = int(min(N, max(2 * B, N * budget / (steps * max(t_row, 1e-9)))))
+    sample = np.ascontiguousarray(w.x[:rows_ps, :n_ps])
+    use_th = min(th, rows_ps)
+    for i in range(args.warmup):
+        oracle.deepselect(sample, w.dtype, K_TOP, B, B2, SEED + i, threads=use_th)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        oracle.deepselect(sample, w.dtype, K_TOP, B, B2, SEED + i, threads=use_th)
+    el = time.perf_counter() - t0
+    gbs = steps * rows_ps * n_ps * 2 / el / 1e9
+    desc = f"{rows_ps} row(s) x {n_ps} of the {ROWS}x{N} bf16 batch per step, oracle DeepSelect transcription"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_per_step": desc},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": use_th, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    import synth
+    import top_selection_gb300 as ds
+    from top_selection_gb300 import build as tbuild
+
+    ws, rank, local = _dist()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0 or ws == 1:
+        tbuild.build()
+    if dist:
+        dist.barrier()
+    ds.load()
+
+    w = synth.indexer_bf16()
+    host = torch.from_numpy(w.x.view(np.int16))
+    x0 = host.to(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 132 * 1024 * 1024) or 132 * 1024 * 1024
+    step_bytes = ROWS * N * 2
+    R = max(8, -(-4 * l2 // step_bytes))
+    xs = [x0.clone() for _ in range(R)]
+    outs = [(torch.empty((ROWS, K_TOP), dtype=torch.int16, device=dev),
+             torch.empty((ROWS, K_TOP), dtype=torch.int32, device=dev)) for _ in range(R)]
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    plan = ds.ds_get_plan(ds.DS_BF16, ROWS, N, K_TOP, B, B2)
+    launches_per_step = 2 if plan["merge_launch"] else 1
+
+    def call(i):
+        x = xs[i % R]
+        v, ix = outs[i % R]
+        st = ds.ds_topk(x.data_ptr(), ds.DS_BF16, ROWS, N, N, K_TOP, B, B2, SEED, v.data_ptr(), ix.data_ptr(),
+                        sptr)
+        if st != 0:
+            raise ds.DSError(st)
+
+    # first calls outside capture (attributes, any workspace)
+    with torch.cuda.stream(stream):
+        for i in range(R):
+            call(i)
+    stream.synchronize()
+    if ds.ds_get_device_status(sptr) != 0:
+        raise RuntimeError("device status after first calls")
+
+    G = min(args.graph_len, max(1, args.steps))
+
+    def make_graph(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    call(i)
+        return g
+
+    g_full = make_graph(G)
+    rem = args.steps % G
+    g_rem = make_graph(rem) if rem else None
+    g_warm = make_graph(max(3, args.warmup))
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local if ws > 1 else (dev.index or 0))
+    sampler.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps // G):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    status = ds.ds_get_device_status(sptr)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    t_max = ms
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    ms_per_step = t_max / args.steps
+    value = ws * step_bytes * args.steps / (t_max * 1e-3) / 1e9
+
+    # roofline of the scan kernel: algorithmic bytes per launch / average launch time
+    alg_bytes = step_bytes + ROWS * K_TOP * (2 + 4)
+    peak, peak_kind = _peak()
+    achieved = alg_bytes / (ms / args.steps * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
+                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
+                "kernel": "ds_scan_kernel<uint16_t>"}
+
+    # e2e through the public API with host buffers
+    pinned = host.pin_memory()
+    xe = torch.empty_like(x0)
+    ve = torch.empty((ROWS, K_TOP), dtype=torch.int16, device=dev)
+    ie = torch.empty((ROWS, K_TOP), dtype=torch.int32, device=dev)
+    hv = torch.empty((ROWS, K_TOP), dtype=torch.int16).pin_memory()
+    hi = torch.empty((ROWS, K_TOP), dtype=torch.int32).pin_memory()
+    e_steps = args.e2e_steps
+
+    def e2e_step():
+        xe.copy_(pinned, non_blocking=True)
+        ds.topk(xe, K_TOP, B, B2, seed=SEED, out=(ve, ie), stream=sptr)
+        hv.copy_(ve, non_blocking=True)
+        hi.copy_(ie, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": round(ws * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": ROWS * K_TOP * (2 + 4),
+           "steps": e_steps}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    cpu = _cpu_oracle(args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch_rows": ROWS * ws, "parallelism": f"rows replicated x{ws}",
+                   "l2": f"inputs rotated over {R} device copies ({R * step_bytes / 1e6:.0f} MB > 4x L2 "
+                         f"{l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {G} calls, CUDA events on the launching stream",
+                   "plan": plan},
+        "hbm_frac_of_peak": round(value / ws / peak, 4),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": args.steps * launches_per_step,
+        "device": torch.cuda.get_device_name(dev),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--graph-len", type=int, default=2000)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

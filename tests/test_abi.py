@@ -1,0 +1,96 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and loads, exports
+every function include/ds_topk.h declares, and rejects bad arguments before it touches
+the device."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ds_topk.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_selection_gb300 import build
+    build.build()
+    import top_selection_gb300 as ds
+    return ds.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(ds_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ["ds_topk", "ds_topk_ex", "ds_get_plan", "ds_workspace_bytes",
+                 "ds_get_device_status", "ds_status_string", "ds_version", "ds_block_order",
+                 "ds_wait_probe"]:
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\b[TW]\s+(ds_\w+)$", out, flags=re.M))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_header_compiles_as_c():
+    src = '#include "ds_topk.h"\nint main(void){ ds_status s = DS_OK; (void)s; return 0; }\n'
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-I" + os.path.join(ROOT, "include"),
+                    "-x", "c", "-"], input=src, text=True, check=True)
+
+
+def test_version_and_status_strings(lib):
+    import top_selection_gb300 as ds
+    assert "sm_103a" in ds.ds_version()
+    for code in range(8):
+        assert ds.ds_status_string(code)
+
+
+# Pointers below are never dereferenced: argument checks run before any CUDA call.
+P = 1 << 20   # a 16-byte aligned fake device address
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(dtype=2), 1),                         # unknown dtype
+    (dict(k=0), 1),
+    (dict(k=1001), 1),                          # k > N
+    (dict(B=0), 1),
+    (dict(B2=0), 1),
+    (dict(N=0), 1),
+    (dict(rows=-1), 1),
+    (dict(row_stride=999), 1),                  # stride < N
+    (dict(x=0), 1),                             # null input
+    (dict(out_idx=0), 1),
+    (dict(x=P + 8), 2),                         # misaligned input
+    (dict(out_vals=P + 4), 2),
+    (dict(row_stride=1004), 2),                 # 1004 * 2 bytes is not a multiple of 16
+    (dict(N=5000, row_stride=5000, k=4097), 3), # k above 4096
+    (dict(B=1001), 3),                          # B * 2 bytes not a multiple of 16
+    (dict(rows=0), 0),                          # nothing to do
+])
+def test_host_validation(lib, args, want):
+    import top_selection_gb300 as ds
+    a = dict(x=P, dtype=0, rows=2, N=1000, row_stride=1024, k=8, B=64, B2=64, seed=1,
+             out_vals=P, out_idx=P)
+    a.update(args)
+    st = ds.ds_topk(a["x"], a["dtype"], a["rows"], a["N"], a["row_stride"], a["k"], a["B"], a["B2"],
+                    a["seed"], a["out_vals"], a["out_idx"], 0)
+    assert st == want
+
+
+def test_fp32_alignment_rules(lib):
+    import top_selection_gb300 as ds
+    # fp32: B*4 must be a multiple of 16 -> B % 4 == 0; stride*4 % 16 -> stride % 4 == 0
+    assert ds.ds_topk(P, 1, 2, 100, 102, 4, 8, 8, 0, P, P, 0) == 2
+    assert ds.ds_topk(P, 1, 1, 100, 100, 4, 10, 8, 0, P, P, 0) == 3
+    assert ds.ds_topk(P, 1, 0, 100, 100, 4, 8, 8, 0, P, P, 0) == 0

@@ -1,0 +1,244 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Literal single-CTA rows must reproduce the oracle transcription's schedule exactly
+(A, R, W, max|C| for the same block order); every result must pass check_topk (value
+multiset bit-exact, indices distinct and pointing at their values, all columns above the
+k-th key present)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import bits_of, check_topk, check_topk_by_counts, pad_rows, run_gpu, to_device
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# ---------------------------------------------------------------- block order ------
+
+@pytest.mark.parametrize("seed,row,b0,n", [(0, 0, 0, 1), (0x5EED, 0, 0, 64), (123, 7, 40, 300),
+                                           (2**63 + 5, 2**31 + 3, 1000, 1024), (9, 1, 0, 17)])
+def test_block_order_matches_oracle(seed, row, b0, n):
+    import top_selection_gb300 as ds
+    out = torch.zeros(n, dtype=torch.int32, device="cuda")
+    assert ds.ds_block_order(seed, row, b0, n, out.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+    got = out.cpu().numpy().tolist()
+    draws = {b: oracle.block_draw(seed, row, b) for b in range(b0, b0 + n)}
+    want = sorted(draws, key=lambda b: (draws[b], b))
+    assert got == want
+    if b0 == 0:
+        assert got == oracle.block_permutation(seed, row, n).tolist()
+
+
+# ---------------------------------------------------------------- literal schedule -
+
+def _literal_case(x, dtype, k, B, B2, seed):
+    xp, n = pad_rows(x, dtype)
+    v, i, st = run_gpu(xp, dtype, k, B, B2, seed, N=n, parts=1, stats=True)
+    ov, oi, ost = oracle.deepselect(x, dtype, k, B, B2, seed, threads=8)
+    assert (ost[:, oracle.STAT_FLAGS] == 0).all()
+    for col in (oracle.STAT_A, oracle.STAT_R, oracle.STAT_W, oracle.STAT_MAXC, oracle.STAT_M):
+        assert np.array_equal(st[:, col], ost[:, col]), f"stat {col}: gpu {st[:, col]} oracle {ost[:, col]}"
+    check_topk(x, dtype, k, v, i)
+
+
+def test_literal_single_row_f32():
+    w = synth.row65536_f32()
+    _literal_case(w.x, w.dtype, 512, 1024, 1024, 0x5EED)
+
+
+@pytest.mark.parametrize("order", ["ascending", "descending", "staircase"])
+def test_literal_block_ordered(order):
+    N, k, B, B2 = 262144, 512, 1024, 1024
+    x = synth.block_ordered(N, B, order).reshape(1, -1)
+    for seed in (0, 1, 77):
+        _literal_case(x, synth.FP32, k, B, B2, seed)
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_literal_random_shapes(dtype):
+    rng = np.random.default_rng(10 + dtype)
+    for trial in range(12):
+        rows = int(rng.integers(1, 6))
+        N = int(rng.integers(1, 40000))
+        k = int(rng.integers(1, min(N, 4096) + 1))
+        B = int(rng.integers(1, 600)) * 8
+        B = max(B, -(-N // 1024 // 8) * 8 + 8)          # one CTA visits at most 1024 blocks
+        B2 = int(rng.integers(1, 3000))
+        x = rng.standard_normal((rows, N)).astype(np.float32)
+        if trial % 3 == 1:
+            x = np.round(x * 4) / 4                     # ties
+        if dtype == synth.BF16:
+            x = synth.f32_to_bf16_bits(x)
+        try:
+            _literal_case(x, dtype, k, B, B2, int(rng.integers(0, 2**63)))
+        except Exception as e:
+            raise AssertionError(f"trial {trial}: rows={rows} N={N} k={k} B={B} B2={B2}") from e
+
+
+# ---------------------------------------------------------------- edge cases -------
+
+def test_edge_values():
+    """Signed zeros, NaNs of both signs, infinities and denormals, in both dtypes."""
+    specials32 = np.array([0x00000000, 0x80000000, 0x7FC00000, 0xFFC00000, 0x7F800000, 0xFF800000,
+                           0x00000001, 0x80000001, 0x7F7FFFFF, 0xFF7FFFFF, 0x3F800000, 0xBF800000],
+                          dtype=np.uint32)
+    rng = np.random.default_rng(3)
+    row = specials32[rng.integers(0, len(specials32), size=5000)].reshape(1, -1)
+    for k in (1, 7, 100, 2000, 4096, 5000):
+        if k > 4096:
+            continue
+        v, i, _ = run_gpu(row.view(np.float32), synth.FP32, k, 256, 256, 4)
+        check_topk(row.view(np.float32), synth.FP32, k, v, i)
+    specials16 = np.array([0x0000, 0x8000, 0x7FC0, 0xFFC0, 0x7F80, 0xFF80, 0x0001, 0x8001, 0x3F80, 0xBF80],
+                          dtype=np.uint16)
+    row16 = specials16[rng.integers(0, len(specials16), size=3001)].reshape(1, -1)
+    for k in (1, 3, 500, 3001):
+        v, i, _ = run_gpu(row16, synth.BF16, k, 64, 64, 5)
+        check_topk(row16, synth.BF16, k, v, i)
+
+
+@pytest.mark.parametrize("N", [1, 2, 7, 8, 9, 15, 16, 17, 1023, 1025, 4097])
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_ragged_lengths(N, dtype):
+    rng = np.random.default_rng(N)
+    x = rng.standard_normal((3, N)).astype(np.float32)
+    if dtype == synth.BF16:
+        x = synth.f32_to_bf16_bits(x)
+    xp, n = pad_rows(x, dtype)
+    for k in sorted({1, max(1, N // 2), min(N, 4096)}):
+        v, i, _ = run_gpu(xp, dtype, k, 8, 8, 11, N=n)
+        check_topk(x, dtype, k, v, i)
+        v, i, _ = run_gpu(xp, dtype, k, 8, 8, 11, N=n, parts=1)
+        check_topk(x, dtype, k, v, i)
+
+
+def test_padded_stride():
+    w = synth.indexer_bf16(rows=5, N=131000, stride=131072)
+    v, i, _ = run_gpu(w.x, w.dtype, 512, 4096, 4096, 3, N=w.N)
+    check_topk(w.x, w.dtype, 512, v, i, N=w.N)
+
+
+def test_k_equals_n_and_k_max():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((2, 4096)).astype(np.float32)
+    v, i, _ = run_gpu(x, synth.FP32, 4096, 1024, 1024, 1)
+    check_topk(x, synth.FP32, 4096, v, i)
+    w = synth.sampler_f32(rows=3, N=129280)
+    v, i, _ = run_gpu(w.x, w.dtype, 4096, 8192, 4096, 2)
+    check_topk(w.x, w.dtype, 4096, v, i)
+
+
+# ---------------------------------------------------------------- split rows -------
+
+@pytest.mark.parametrize("parts,cluster", [(2, 2), (4, 4), (8, 8), (4, 1), (8, 2), (16, 4), (16, 16)])
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_split_rows(parts, cluster, dtype):
+    rng = np.random.default_rng(parts * 10 + cluster)
+    rows, N = 3, 200000
+    x = rng.standard_normal((rows, N)).astype(np.float32)
+    if dtype == synth.BF16:
+        x = synth.f32_to_bf16_bits(x)
+    for k in (1, 64, 512, 2048):
+        v, i, _ = run_gpu(x, dtype, k, 2048, 2048, 99, parts=parts, cluster=cluster)
+        check_topk(x, dtype, k, v, i)
+
+
+def test_split_rows_tie_heavy():
+    w = synth.longctx_bf16("levels", rows=2, N=300000)
+    for parts, cluster in [(4, 4), (8, 1), (16, 8)]:
+        v, i, _ = run_gpu(w.x, w.dtype, 2048, 4096, 4096, 5, parts=parts, cluster=cluster)
+        check_topk(w.x, w.dtype, 2048, v, i)
+
+
+def test_caller_workspace():
+    import top_selection_gb300 as ds
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((2, 300000)).astype(np.float32)
+    nb = ds.ds_workspace_bytes(synth.FP32, 2, 300000, 512, 4096, 4096, parts=8, cluster=2)
+    assert nb > 0
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        v, i, _ = run_gpu(x, synth.FP32, 512, 4096, 4096, 7, parts=8, cluster=2, workspace=ws)
+        check_topk(x, synth.FP32, 512, v, i)
+
+
+# ---------------------------------------------------------------- workloads --------
+
+def _auto(w, k):
+    v, i, _ = run_gpu(w.x, w.dtype, k, w.B, w.B2, 0x5EED, N=w.N)
+    check_topk(w.x, w.dtype, k, v, i, N=w.N, threads=16)
+
+
+def test_workload_row65536_f32():
+    _auto(synth.row65536_f32(), 512)
+
+
+def test_workload_indexer_bf16():
+    _auto(synth.indexer_bf16(), 512)
+
+
+@pytest.mark.parametrize("k", [1, 64, 512, 4096])
+def test_workload_sampler_f32(k):
+    _auto(synth.sampler_f32(), k)
+
+
+@pytest.mark.parametrize("kind", ["iid", "ascending", "levels"])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_workload_longctx_bf16(kind, k):
+    _auto(synth.longctx_bf16(kind), k)
+
+
+@pytest.mark.parametrize("k", [32, 4096])
+def test_workload_huge_f32(k):
+    w = synth.huge_f32()
+    v, i, _ = run_gpu(w.x, w.dtype, k, w.B, w.B2, 0x5EED)
+    check_topk_by_counts(w.x[0], k, v[0].view(np.float32), i[0].astype(np.int64))
+    # the oracle on a sampled slice of the same row, through the same launch shape
+    sl = np.ascontiguousarray(w.x[:, : 1 << 22])
+    v2, i2, _ = run_gpu(sl, w.dtype, k, w.B, w.B2, 0x5EED)
+    check_topk(sl, w.dtype, k, v2, i2)
+
+
+# ---------------------------------------------------------------- failure path -----
+
+def test_wait_timeout_is_reported_and_context_survives():
+    import top_selection_gb300 as ds
+    s = torch.cuda.current_stream().cuda_stream
+    assert ds.ds_get_device_status(s) == 0
+    assert ds.ds_wait_probe(2_000_000, s) == 0
+    assert ds.ds_get_device_status(s) == 5          # DS_ERR_TIMEOUT
+    assert ds.ds_get_device_status(s) == 0          # cleared
+    w = synth.row65536_f32(rows=2)
+    v, i, _ = run_gpu(w.x, w.dtype, 512, 1024, 1024, 1)
+    check_topk(w.x, w.dtype, 512, v, i)
+
+
+def test_graph_capture_replay():
+    import top_selection_gb300 as ds
+    w = synth.indexer_bf16(rows=8, N=131072)
+    xt = to_device(w.x, w.dtype)
+    vals = torch.empty((8, 512), dtype=xt.dtype, device="cuda")
+    idx = torch.empty((8, 512), dtype=torch.int32, device="cuda")
+    ds.topk(xt, 512, 4096, 4096, seed=1, out=(vals, idx))     # first call outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            ds.topk(xt, 512, 4096, 4096, seed=1, out=(vals, idx))
+    vals.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    v = vals.cpu().numpy().view(np.uint16)
+    check_topk(w.x, w.dtype, 512, v, idx.cpu().numpy())

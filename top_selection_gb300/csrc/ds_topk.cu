@@ -1,0 +1,947 @@
+// ds_topk.cu -- GB300 (sm_103a) DeepSelect row-wise top-k: kernels and the C ABI.
+//
+// DeepSelectTopk (DeepSelect-deep-dive.md, "Algorithm") per row: T = -inf; visit blocks
+// of B elements in a random order independent of x; append every element with key > T
+// to the candidate buffer; after a block, if the buffer holds >= k + B2 entries, run
+// RadixSelectTopK back to k and set T to the smallest kept key; finish with a final
+// RadixSelectTopK.
+//
+// GB300 mapping
+//   * One CTA scans one part of a row (a contiguous range of blocks; a part is the whole
+//     row when the row is not split).  A producer warp streams the part's blocks, in
+//     the part's Philox order, into a ring of shared-memory stages with 1-D bulk copies
+//     (cp.async.bulk, completion on mbarriers); the input is read from HBM exactly once,
+//     with an L2 evict-first hint.
+//   * Consumer warps filter each staged chunk against T with integer compares on the raw
+//     bits (16-byte vector loads from shared memory, one warp vote per vector) and append
+//     survivors with a warp prefix sum and one shared atomic per warp.
+//   * After each block the consumers agree on |C| (per-warp counts, one named barrier)
+//     and, at >= k + B2, run RadixSelectTopK in shared memory (ds_select.cuh).
+//   * Split rows ("Implementation" section of the deep-dive: one sequence over several
+//     SMs, CTA results merged): the CTAs of a row form a thread-block cluster.  They
+//     share the best threshold through distributed shared memory, and the final
+//     selection runs over the union of their candidate buffers (cluster-wide histograms),
+//     each CTA writing its own survivors straight to the output.  Rows split over more
+//     than one cluster also share T through a global per-row word, write per-cluster
+//     results to a workspace, and a small merge kernel finishes the row.
+//   * No tensor cores: nothing on this path is a dense contraction.
+//
+// Every wait on an mbarrier is bounded (about one second of SM clock); on expiry the
+// CTA records DS_ERR_TIMEOUT in the device status word, stops waiting, keeps its barrier
+// sequence so that no other thread is left waiting, and drains its own copies in flight
+// before exiting.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "ds_common.cuh"
+#include "ds_select.cuh"
+#include "ds_topk.h"
+
+namespace dsk {
+
+constexpr int kNCW = 8;                 // consumer warps per CTA
+constexpr int kScanThreads = (kNCW + 1) * 32;
+constexpr int kMergeThreads = kNCW * 32;
+constexpr int kChunkBytesMax = 16384;   // one bulk copy
+constexpr int kMergeTile = 2048;        // entries per merge block
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct ScanLayout {
+    size_t ring, ckey, cidx, hist, ghist, perm, ctrl, total;
+};
+
+__host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages, int cap, int G, int perm_cap) {
+    ScanLayout L;
+    size_t off = 0;
+    L.ring = off;
+    off += align_up(static_cast<size_t>(stages) * chunk * es, 128);
+    L.ckey = off;
+    off += align_up(static_cast<size_t>(cap) * es, 16);
+    L.cidx = off;
+    off += align_up(static_cast<size_t>(cap) * 4, 16);
+    L.hist = off;
+    off += kBins * 4;
+    L.ghist = off;
+    if (G > 1) off += kBins * 4;
+    L.perm = off;
+    off += align_up(static_cast<size_t>(perm_cap) * 4, 16);
+    L.ctrl = off;
+    off += align_up(sizeof(Ctrl), 16);
+    L.total = off;
+    return L;
+}
+
+struct MergeLayout {
+    size_t ckey, cidx, hist, ctrl, total;
+};
+
+__host__ __device__ inline MergeLayout merge_layout(int es, int cap) {
+    MergeLayout L;
+    size_t off = 0;
+    L.ckey = off;
+    off += align_up(static_cast<size_t>(cap) * es, 16);
+    L.cidx = off;
+    off += align_up(static_cast<size_t>(cap) * 4, 16);
+    L.hist = off;
+    off += kBins * 4;
+    L.ctrl = off;
+    off += align_up(sizeof(Ctrl), 16);
+    L.total = off;
+    return L;
+}
+
+struct ScanParams {
+    const char* x;
+    int64_t rows, N, stride_bytes, m;
+    int32_t k, B, B2;
+    uint64_t seed;
+    void* out_vals;
+    int32_t* out_idx;
+    long long* stats;
+    int32_t parts, G, C;          // CTAs per row, CTAs per cluster, clusters per row
+    int32_t chunk, stages, cap, perm_cap;
+    uint32_t epoch;
+    unsigned long long* gT;       // per-row shared threshold (C > 1)
+    uint32_t* ws_key;             // per (row, cluster) partial results (C > 1)
+    int32_t* ws_idx;
+    int32_t* ws_cnt;
+};
+
+struct MergeParams {
+    const uint32_t* ws_key;
+    const int32_t* ws_idx;
+    const int32_t* ws_cnt;
+    int32_t C, k, B2, cap;
+    uint32_t epoch;
+    const unsigned long long* gT;
+    void* out_vals;
+    int32_t* out_idx;
+};
+
+// ---------------------------------------------------------------- filter ----------
+// MODE 0: T = -inf, every element passes.  MODE 1: T >= +0, pass iff (int)bits > thr.
+// MODE 2: T <= -0, pass iff (unsigned)bits < thr.  For bf16 each 32-bit word holds two
+// values; the low one is shifted up, and thr is the threshold's bits << 16 (| 0xFFFF in
+// MODE 1), so one 32-bit compare decides each value.
+template <int MODE>
+__device__ __forceinline__ uint32_t pass_bits(uint32_t a, uint32_t thr) {
+    if (MODE == 1) return static_cast<int32_t>(a) > static_cast<int32_t>(thr) ? 1u : 0u;
+    return a < thr ? 1u : 0u;
+}
+
+template <typename KeyT, int MODE>
+__device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uint32_t col0, uint32_t thr, KeyT* ckey,
+                                                 uint32_t* cidx, Ctrl* ctrl, int cap, int warp, int lane) {
+    constexpr int NC = kNCW * 32;
+    constexpr int ES = sizeof(KeyT);
+    constexpr int VEC = 16 / ES;
+    uint32_t appended = 0;
+    for (int base = warp * 32; base < nvec; base += NC) {
+        const int vi = base + lane;
+        const bool valid = vi < nvec;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) v = src[vi];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t mask;
+        if (MODE == 0) {
+            mask = valid ? ((1u << VEC) - 1u) : 0u;
+        } else {
+            mask = 0u;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (ES == 4) {
+                    mask |= pass_bits<MODE>(w[q], thr) << q;
+                } else {
+                    mask |= pass_bits<MODE>(w[q] << 16, thr) << (2 * q);
+                    mask |= pass_bits<MODE>(w[q], thr) << (2 * q + 1);
+                }
+            }
+            if (!valid) mask = 0u;
+        }
+        if (!__any_sync(0xFFFFFFFFu, mask != 0u)) continue;
+        uint32_t keys[VEC];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (ES == 4) {
+                keys[q] = key_f32(w[q]);
+            } else {
+                keys[2 * q] = key_bf16(w[q] & 0xFFFFu);
+                keys[2 * q + 1] = key_bf16(w[q] >> 16);
+            }
+        }
+        appended += warp_append<KeyT, VEC>(mask, keys, col0 + static_cast<uint32_t>(vi) * VEC, ckey, cidx, ctrl, cap,
+                                           lane);
+    }
+    return appended;
+}
+
+// Elements of the row's last < 16 bytes, read straight from global memory (one per lane).
+template <typename KeyT>
+__device__ __forceinline__ uint32_t filter_tail(const char* xrow, int64_t c_first, int count, bool have, uint32_t tk,
+                                                KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int cap, int lane) {
+    constexpr int ES = sizeof(KeyT);
+    const bool valid = lane < count;
+    uint32_t key = 0u;
+    if (valid) {
+        if (ES == 2) key = key_bf16(reinterpret_cast<const uint16_t*>(xrow)[c_first + lane]);
+        else key = key_f32(reinterpret_cast<const uint32_t*>(xrow)[c_first + lane]);
+    }
+    const bool hit = valid && (!have || key > tk);
+    const uint32_t keys[1] = {key};
+    return warp_append<KeyT, 1>(hit ? 1u : 0u, keys, static_cast<uint32_t>(c_first + lane), ckey, cidx, ctrl, cap,
+                                lane);
+}
+
+__device__ __forceinline__ void threshold_mode(int es, bool have, uint32_t tk, int& mode, uint32_t& thr) {
+    if (!have) {
+        mode = 0;
+        thr = 0u;
+        return;
+    }
+    if (es == 4) {
+        const uint32_t raw = unkey_f32(tk);
+        mode = (raw & 0x80000000u) ? 2 : 1;
+        thr = raw;
+    } else {
+        const uint32_t raw = unkey_bf16(tk);
+        mode = (raw & 0x8000u) ? 2 : 1;
+        thr = (mode == 1) ? ((raw << 16) | 0xFFFFu) : (raw << 16);
+    }
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kSpinLimit) {
+            set_status(kErrTimeout);
+            return;
+        }
+    }
+}
+
+// Visiting order of blocks b0 .. b0+mp-1 of `row`: draw u_b = Philox(seed; b, row) for
+// each block, and place each block at its rank in (u_b, b) order.  `draws` is scratch of
+// mp words.  Ends with a CTA barrier.
+template <int NT>
+__device__ void block_order(uint64_t seed, int64_t row, int64_t b0, int mp, uint32_t* draws, int32_t* perm, int tid) {
+    for (int j = tid; j < mp; j += NT) draws[j] = block_draw(seed, row, b0 + j);
+    __syncthreads();
+    for (int j = tid; j < mp; j += NT) {
+        const uint32_t u = draws[j];
+        int r = 0;
+        for (int j2 = 0; j2 < mp; ++j2) {
+            const uint32_t v = draws[j2];
+            r += (v < u || (v == u && j2 < j)) ? 1 : 0;
+        }
+        perm[r] = static_cast<int32_t>(b0 + j);
+    }
+    __syncthreads();
+}
+
+// Exposes block_order for parity checks: one CTA, mp <= kPermMax.
+__global__ void __launch_bounds__(256) ds_block_order_kernel(uint64_t seed, int64_t row, int64_t b0, int mp,
+                                                              int32_t* out) {
+    __shared__ uint32_t draws[kPermMax];
+    __shared__ int32_t perm[kPermMax];
+    block_order<256>(seed, row, b0, mp, draws, perm, threadIdx.x);
+    for (int j = threadIdx.x; j < mp; j += 256) out[j] = perm[j];
+}
+
+// Waits on an mbarrier phase that never completes, with the given cycle limit: the same
+// bounded wait as the scan kernel, used to check that a wait that runs out is reported
+// through the status word and leaves the context usable.
+__global__ void ds_wait_probe_kernel(long long limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        const long long t0 = clock64();
+        while (!mbar_try_wait(&bar, 0)) {
+            if (clock64() - t0 > limit) {
+                set_status(kErrTimeout);
+                break;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- scan kernel -----
+template <typename KeyT>
+__global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanParams p) {
+    constexpr int NC = kNCW * 32;
+    constexpr int NT = kScanThreads;
+    constexpr int ES = sizeof(KeyT);
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const ScanLayout L = scan_layout(ES, p.chunk, p.stages, p.cap, p.G, p.perm_cap);
+    uint8_t* ring = smem + L.ring;
+    KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
+    uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    uint32_t* ghist = p.G > 1 ? reinterpret_cast<uint32_t*>(smem + L.ghist) : hist;
+    int32_t* perm = reinterpret_cast<int32_t*>(smem + L.perm);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t cta = blockIdx.x;
+    const int64_t row = cta / p.parts;
+    const int part = static_cast<int>(cta % p.parts);
+    const int cl = part / p.G;
+    const uint32_t crank = p.G > 1 ? cluster_ctarank() : 0u;
+    const int64_t b0 = static_cast<int64_t>(part) * p.m / p.parts;
+    const int64_t b1 = static_cast<int64_t>(part + 1) * p.m / p.parts;
+    const int mp = static_cast<int>(b1 - b0);
+    const char* xrow = p.x + row * p.stride_bytes;
+    const int chunk_bytes = p.chunk * ES;
+    const bool shared_T = p.G > 1 || p.C > 1;
+
+    if (tid == 0) {
+        int* z = reinterpret_cast<int*>(ctrl);
+        for (size_t i = 0; i < sizeof(Ctrl) / sizeof(int); ++i) z[i] = 0;
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&ctrl->full[s], 1);
+            mbar_init(&ctrl->empty[s], kNCW);
+        }
+        fence_mbar_init();
+    }
+    block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
+    if (p.G > 1) cluster_sync_all();  // every CTA's control block is initialised
+    const uint32_t a_shT = p.G > 1 ? map_rank(&ctrl->sharedT, 0) : 0u;
+
+    if (warp == kNCW) {
+        // ------------------------------ producer: bulk copies in block order ------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int seq = 0;
+            bool stop = false;
+            for (int i = 0; i < mp && !stop; ++i) {
+                const int64_t lo = static_cast<int64_t>(perm[i]) * p.B;
+                const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
+                for (int64_t c0 = lo; c0 < hi; c0 += p.chunk) {
+                    const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
+                    const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+                    const int s = seq % p.stages, use = seq / p.stages;
+                    if (use > 0 && !wait_bounded(&ctrl->empty[s], (use - 1) & 1, ctrl)) {
+                        stop = true;
+                        break;
+                    }
+                    if (bytes) {
+                        mbar_arrive_expect_tx(&ctrl->full[s], bytes);
+                        bulk_g2s(ring + static_cast<size_t>(s) * chunk_bytes, xrow + c0 * ES, bytes, &ctrl->full[s],
+                                 pol);
+                    } else {
+                        mbar_arrive(&ctrl->full[s]);
+                    }
+                    ctrl->issued[s] = use + 1;
+                    ++seq;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ consumers: filter, append, compact ---------
+        int seq = 0;
+        int n = 0;
+        bool hasT = false;
+        uint32_t T = 0u;
+        uint32_t wcnt = 0u;
+        long long sA = 0, sR = 0, sW = 0, sMax = 0;
+        for (int i = 0; i < mp; ++i) {
+            const int64_t lo = static_cast<int64_t>(perm[i]) * p.B;
+            const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
+            bool have = hasT;
+            uint32_t tk = T;
+            if (shared_T) {
+                uint32_t sh = 0u;
+                if (lane == 0) {
+                    if (p.G > 1) sh = ld_cluster_u32(a_shT);
+                    if (p.C > 1) {
+                        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+                        if (static_cast<uint32_t>(g >> 32) == p.epoch) sh = max(sh, static_cast<uint32_t>(g));
+                    }
+                }
+                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
+                if (sh != 0u && (!have || sh > tk)) {
+                    tk = sh;
+                    have = true;
+                }
+            }
+            int mode;
+            uint32_t thr;
+            threshold_mode(ES, have, tk, mode, thr);
+            for (int64_t c0 = lo; c0 < hi; c0 += p.chunk) {
+                const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
+                const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+                const int s = seq % p.stages, use = seq / p.stages;
+                if (wait_bounded(&ctrl->full[s], use & 1, ctrl)) {
+                    if (tid == 0) ctrl->observed[s] = use + 1;
+                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
+                    const int nvec = static_cast<int>(bytes / 16);
+                    const uint32_t col0 = static_cast<uint32_t>(c0);
+                    if (mode == 0) wcnt += filter_chunk<KeyT, 0>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
+                    else if (mode == 1) wcnt += filter_chunk<KeyT, 1>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
+                    else wcnt += filter_chunk<KeyT, 2>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
+                    const int tail = static_cast<int>(ce - bytes / ES);
+                    if (tail > 0 && warp == 0)
+                        wcnt += filter_tail<KeyT>(xrow, c0 + bytes / ES, tail, have, tk, ckey, cidx, ctrl, p.cap, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->empty[s]);
+                ++seq;
+            }
+            // end of block: agree on |C| and compact at >= k + B2
+            if (lane == 0) ctrl->block_cnt[i & 1][warp] = wcnt;
+            wcnt = 0u;
+            named_bar_sync(1, NC);
+            uint32_t add = 0u;
+#pragma unroll
+            for (int w = 0; w < kNCW; ++w) add += ctrl->block_cnt[i & 1][w];
+            n += static_cast<int>(add);
+            if (tid == 0) {
+                sA += add;
+                sMax = n > sMax ? n : sMax;
+            }
+            if (n >= p.k + p.B2) {
+                const uint32_t lo_k = hasT ? T : 0u;
+                const uint32_t hi_k = ctrl->maxkey;
+                if (tid == 0) {
+                    sW += n;
+                    sR += 1;
+                }
+                T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, lo_k, hi_k, tid);
+                hasT = true;
+                n = p.k;
+                if (tid == 0 && shared_T) {
+                    if (p.G > 1) red_cluster_max_u32(a_shT, T);
+                    if (p.C > 1)
+                        atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
+                }
+            }
+        }
+        if (tid == 0) {
+            ctrl->fin_n = n;
+            ctrl->fin_hasT = hasT ? 1 : 0;
+            ctrl->fin_T = T;
+            if (p.stats && p.parts == 1) {
+                long long* st = p.stats + row * DS_NSTAT;
+                st[0] = sA;
+                st[1] = sR;
+                st[2] = sW + n;
+                st[3] = sMax;
+                st[4] = mp;
+                st[5] = 0;
+                st[6] = sR;
+                st[7] = 0;
+            }
+        }
+    }
+    __syncthreads();
+    if (ctrl->abort && tid == 0) {
+        for (int s = 0; s < p.stages; ++s)
+            if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
+    }
+    const int n = ctrl->fin_n;
+    const bool hasT = ctrl->fin_hasT != 0;
+    const uint32_t T = ctrl->fin_T;
+
+    // ------------------------------ final selection over the cluster --------------
+    uint32_t lo_own = hasT ? T : 0u;
+    if (p.C > 1) {
+        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_own = max(lo_own, static_cast<uint32_t>(g));
+    }
+    uint32_t lo0, hi0;
+    if (p.G > 1) {
+        if (tid == 0) {
+            red_cluster_max_u32(map_rank(&ctrl->gmax, 0), ctrl->maxkey);
+            red_cluster_max_u32(a_shT, lo_own);
+        }
+        cluster_sync_all();
+        lo0 = ld_cluster_u32(a_shT);
+        hi0 = ld_cluster_u32(map_rank(&ctrl->gmax, 0));
+    } else {
+        lo0 = lo_own;
+        hi0 = ctrl->maxkey;
+    }
+    OutTarget out;
+    if (p.C > 1) {
+        out.vals = p.ws_key;
+        out.idx = p.ws_idx;
+        out.base = (row * p.C + cl) * static_cast<int64_t>(p.k);
+        out.to_keys = true;
+    } else {
+        out.vals = p.out_vals;
+        out.idx = p.out_idx;
+        out.base = row * static_cast<int64_t>(p.k);
+        out.to_keys = false;
+    }
+    out.esize = ES;
+    const bool write_ok = !ctrl->abort;
+    uint32_t kept;
+    if (p.G > 1)
+        kept = final_select<KeyT, NT, true>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, p.G, out, write_ok, tid);
+    else
+        kept = final_select<KeyT, NT, false>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, 1, out, write_ok, tid);
+    if (p.C > 1 && crank == 0 && tid == 0) p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(kept);
+}
+
+// ---------------------------------------------------------------- merge kernel ----
+// Finishes rows split over C clusters: DeepSelect over the C partial results of the row
+// (each at most k (key, column) pairs), filtered against the row's shared threshold,
+// which every kept partial entry meets or exceeds.
+template <typename KeyT>
+__global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeParams p) {
+    constexpr int NT = kMergeThreads;
+    constexpr int ES = sizeof(KeyT);
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const MergeLayout L = merge_layout(ES, p.cap);
+    KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
+    uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = blockIdx.x;
+    if (tid == 0) {
+        int* z = reinterpret_cast<int*>(ctrl);
+        for (size_t i = 0; i < sizeof(Ctrl) / sizeof(int); ++i) z[i] = 0;
+    }
+    uint32_t lo_g = 0u;
+    {
+        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_g = static_cast<uint32_t>(g);
+    }
+    __syncthreads();
+    int n = 0, blk = 0;
+    bool hasT = false;
+    uint32_t T = 0u, wcnt = 0u;
+    for (int c = 0; c < p.C; ++c) {
+        const int64_t seg = row * p.C + c;
+        const int cnt = p.ws_cnt[seg];
+        const uint32_t* sk = p.ws_key + seg * p.k;
+        const int32_t* si = p.ws_idx + seg * p.k;
+        for (int t0 = 0; t0 < cnt; t0 += kMergeTile) {
+            const int te = (cnt - t0) < kMergeTile ? (cnt - t0) : kMergeTile;
+            for (int base = warp * 32; base < te; base += NT) {
+                const int j = base + lane;
+                const bool valid = j < te;
+                const uint32_t key = valid ? sk[t0 + j] : 0u;
+                const uint32_t col = valid ? static_cast<uint32_t>(si[t0 + j]) : 0u;
+                const bool hit = valid && key >= lo_g && (!hasT || key > T);
+                const uint32_t keys[1] = {key};
+                if (__any_sync(0xFFFFFFFFu, hit))
+                    wcnt += warp_append<KeyT, 1>(hit ? 1u : 0u, keys, col, ckey, cidx, ctrl, p.cap, lane);
+            }
+            if (lane == 0) ctrl->block_cnt[blk & 1][warp] = wcnt;
+            wcnt = 0u;
+            __syncthreads();
+            uint32_t add = 0u;
+#pragma unroll
+            for (int w = 0; w < NT / 32; ++w) add += ctrl->block_cnt[blk & 1][w];
+            n += static_cast<int>(add);
+            ++blk;
+            if (n >= p.k + p.B2) {
+                const uint32_t lo_k = hasT ? T : lo_g;
+                T = compact<KeyT, NT, 0>(ckey, cidx, hist, ctrl, n, p.k, lo_k, ctrl->maxkey, tid);
+                hasT = true;
+                n = p.k;
+            }
+        }
+    }
+    OutTarget out;
+    out.vals = p.out_vals;
+    out.idx = p.out_idx;
+    out.base = row * static_cast<int64_t>(p.k);
+    out.to_keys = false;
+    out.esize = ES;
+    final_select<KeyT, NT, false>(ckey, cidx, hist, hist, ctrl, n, p.k, hasT ? T : lo_g, ctrl->maxkey, 1, out, true,
+                                  tid);
+}
+
+// ================================================================ host ============
+
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    int smem_per_sm = 0;
+    bool ok = false;
+};
+
+static std::mutex g_mu;
+static DevInfo g_dev[64];
+static std::atomic<uint32_t> g_epoch{0};
+
+struct Workspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+static Workspace g_ws[64];
+
+static bool dev_info(int dev, DevInfo& out) {
+    if (dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ok) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return false;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+            return false;
+        d.ok = true;
+    }
+    out = d;
+    return true;
+}
+
+struct Plan {
+    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm;
+    int64_t m;
+    size_t smem, merge_smem, ws_bytes;
+    int merge_cap;
+    size_t off_gT, off_key, off_idx, off_cnt;
+};
+
+static ds_status validate(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
+                          int32_t B, int32_t B2, const void* out_vals, const int32_t* out_idx) {
+    if (dtype != DS_BF16 && dtype != DS_FP32) return DS_ERR_INVALID_ARG;
+    if (rows < 0 || N < 1 || k < 1 || k > N || B < 1 || B2 < 1 || row_stride < N) return DS_ERR_INVALID_ARG;
+    if (rows > 0 && (!x || !out_vals || !out_idx)) return DS_ERR_INVALID_ARG;
+    const int es = dtype == DS_BF16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out_vals) |
+         reinterpret_cast<uintptr_t>(out_idx)) & 15u)
+        return DS_ERR_ALIGNMENT;
+    if (rows > 1 && (row_stride * es) % 16 != 0) return DS_ERR_ALIGNMENT;
+    if (k > kMaxK || N >= (int64_t(1) << 31)) return DS_ERR_UNSUPPORTED;
+    if ((static_cast<int64_t>(B) * es) % 16 != 0) return DS_ERR_UNSUPPORTED;
+    return DS_OK;
+}
+
+static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t B, int32_t B2,
+                           const ds_options* opt, Plan& P) {
+    DevInfo di;
+    if (!dev_info(dev, di)) return DS_ERR_CUDA;
+    P.dev = dev;
+    P.es = dtype == DS_BF16 ? 2 : 4;
+    P.m = (N + B - 1) / B;
+    P.chunk = B < kChunkBytesMax / P.es ? B : kChunkBytesMax / P.es;
+    const int64_t cap64 = static_cast<int64_t>(k) + B + B2;
+    if (cap64 > (int64_t(1) << 20)) return DS_ERR_UNSUPPORTED;
+    P.cap = static_cast<int>(cap64);
+    int parts = opt ? opt->parts : 0;
+    if (parts < 0) return DS_ERR_INVALID_ARG;
+    if (parts == 0) {
+        parts = 1;
+        const int64_t maxp = P.m / 4 > 1 ? P.m / 4 : 1;
+        while (rows * parts < di.sms && parts * 2 <= maxp && parts < 256) parts *= 2;
+        while ((P.m + parts - 1) / parts > kPermMax) parts *= 2;
+        if (parts > P.m) return DS_ERR_UNSUPPORTED;
+    } else {
+        if (parts > P.m || (P.m + parts - 1) / parts > kPermMax) return DS_ERR_UNSUPPORTED;
+    }
+    P.parts = parts;
+    P.perm_cap = static_cast<int>((P.m + parts - 1) / parts);
+    int G = opt ? opt->cluster : 0;
+    if (G < 0 || G > 16) return DS_ERR_INVALID_ARG;
+    if (G == 0) {
+        G = 1;
+        while (G * 2 <= 8 && parts % (G * 2) == 0) G *= 2;
+    }
+    if (parts % G != 0) return DS_ERR_INVALID_ARG;
+    P.G = G;
+    P.C = parts / G;
+    if (opt && opt->stats && parts != 1) return DS_ERR_INVALID_ARG;
+    // Ring depth: the deepest ring (3..kMaxStages) that still lets two CTAs share an SM;
+    // otherwise the deepest ring that fits one CTA (at least 2 stages).
+    P.stages = 0;
+    for (int s = kMaxStages; s >= 3; --s) {
+        const size_t need = scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
+        if (2 * (need + 1024) <= static_cast<size_t>(di.smem_per_sm)) {
+            P.stages = s;
+            break;
+        }
+    }
+    if (P.stages == 0) {
+        for (int s = kMaxStages; s >= 2; --s) {
+            const size_t need = scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
+            if (need <= static_cast<size_t>(di.smem_optin)) {
+                P.stages = s;
+                break;
+            }
+        }
+    }
+    if (P.stages == 0) return DS_ERR_UNSUPPORTED;
+    P.smem = scan_layout(P.es, P.chunk, P.stages, P.cap, G, P.perm_cap).total;
+    P.ctas_per_sm = static_cast<int>(di.smem_per_sm / (P.smem + 1024));
+    if (P.ctas_per_sm < 1) P.ctas_per_sm = 1;
+    P.ws_bytes = 0;
+    P.merge_smem = 0;
+    P.merge_cap = 0;
+    if (P.C > 1) {
+        P.merge_cap = k + kMergeTile + B2;
+        P.merge_smem = merge_layout(P.es, P.merge_cap).total;
+        if (P.merge_smem > static_cast<size_t>(di.smem_optin)) return DS_ERR_UNSUPPORTED;
+        size_t off = 0;
+        P.off_gT = off;
+        off = align_up(off + rows * 8, 256);
+        P.off_key = off;
+        off = align_up(off + static_cast<size_t>(rows) * P.C * k * 4, 256);
+        P.off_idx = off;
+        off = align_up(off + static_cast<size_t>(rows) * P.C * k * 4, 256);
+        P.off_cnt = off;
+        off = align_up(off + static_cast<size_t>(rows) * P.C * 4, 256);
+        P.ws_bytes = off;
+    }
+    return DS_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit (and allows 16-CTA clusters) once per
+// device; later calls that need no more than what was set make no runtime call, so a
+// call under stream capture only launches.
+template <typename Kern>
+static cudaError_t set_smem(Kern kern, int slot, int dev, size_t bytes, bool nonportable) {
+    static size_t done[4][64];
+    static bool np_done[4][64];
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (done[slot][dev] < bytes) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+        if (e != cudaSuccess) return e;
+        done[slot][dev] = bytes;
+    }
+    if (nonportable && !np_done[slot][dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+        np_done[slot][dev] = true;
+    }
+    return cudaSuccess;
+}
+
+template <typename KeyT>
+static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
+                        int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, long long* stats,
+                        char* ws, cudaStream_t stream) {
+    ScanParams sp;
+    sp.x = static_cast<const char*>(x);
+    sp.rows = rows;
+    sp.N = N;
+    sp.stride_bytes = row_stride * P.es;
+    sp.m = P.m;
+    sp.k = k;
+    sp.B = B;
+    sp.B2 = B2;
+    sp.seed = seed;
+    sp.out_vals = out_vals;
+    sp.out_idx = out_idx;
+    sp.stats = stats;
+    sp.parts = P.parts;
+    sp.G = P.G;
+    sp.C = P.C;
+    sp.chunk = P.chunk;
+    sp.stages = P.stages;
+    sp.cap = P.cap;
+    sp.perm_cap = P.perm_cap;
+    sp.epoch = 0;
+    sp.gT = nullptr;
+    sp.ws_key = nullptr;
+    sp.ws_idx = nullptr;
+    sp.ws_cnt = nullptr;
+    if (P.C > 1) {
+        uint32_t e = g_epoch.fetch_add(1) + 1;
+        if (e == 0) e = g_epoch.fetch_add(1) + 1;
+        sp.epoch = e;
+        sp.gT = reinterpret_cast<unsigned long long*>(ws + P.off_gT);
+        sp.ws_key = reinterpret_cast<uint32_t*>(ws + P.off_key);
+        sp.ws_idx = reinterpret_cast<int32_t*>(ws + P.off_idx);
+        sp.ws_cnt = reinterpret_cast<int32_t*>(ws + P.off_cnt);
+    }
+    auto kern = ds_scan_kernel<KeyT>;
+    const int slot = sizeof(KeyT) == 2 ? 0 : 1;
+    if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(rows * P.parts), 1, 1);
+    cfg.blockDim = dim3(kScanThreads, 1, 1);
+    cfg.dynamicSmemBytes = P.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (P.G > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = P.G;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, kern, sp) != cudaSuccess) return DS_ERR_CUDA;
+    if (P.C > 1) {
+        MergeParams mp;
+        mp.ws_key = sp.ws_key;
+        mp.ws_idx = sp.ws_idx;
+        mp.ws_cnt = sp.ws_cnt;
+        mp.C = P.C;
+        mp.k = k;
+        mp.B2 = B2;
+        mp.cap = P.merge_cap;
+        mp.epoch = sp.epoch;
+        mp.gT = sp.gT;
+        mp.out_vals = out_vals;
+        mp.out_idx = out_idx;
+        auto mk = ds_merge_kernel<KeyT>;
+        if (set_smem(mk, slot + 2, P.dev, P.merge_smem, false) != cudaSuccess) return DS_ERR_CUDA;
+        mk<<<static_cast<unsigned>(rows), kMergeThreads, P.merge_smem, stream>>>(mp);
+        if (cudaGetLastError() != cudaSuccess) return DS_ERR_CUDA;
+    }
+    return DS_OK;
+}
+
+static ds_status library_workspace(int dev, size_t bytes, cudaStream_t stream, void** out) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    Workspace& w = g_ws[dev];
+    if (w.bytes >= bytes) {
+        *out = w.ptr;
+        return DS_OK;
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DS_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return DS_ERR_WORKSPACE;
+    if (w.ptr) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return DS_ERR_CUDA;
+        cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+    }
+    void* p = nullptr;
+    const size_t grow = bytes + bytes / 4;
+    if (cudaMalloc(&p, grow) != cudaSuccess) return DS_ERR_CUDA;
+    if (cudaMemset(p, 0, grow) != cudaSuccess) {
+        cudaFree(p);
+        return DS_ERR_CUDA;
+    }
+    w.ptr = p;
+    w.bytes = grow;
+    *out = p;
+    return DS_OK;
+}
+
+}  // namespace dsk
+
+using namespace dsk;
+
+extern "C" {
+
+ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t B, int32_t B2,
+                      const ds_options* options, ds_plan* plan) {
+    if (!plan) return DS_ERR_INVALID_ARG;
+    if (dtype != DS_BF16 && dtype != DS_FP32) return DS_ERR_INVALID_ARG;
+    if (rows < 0 || N < 1 || k < 1 || k > N || B < 1 || B2 < 1) return DS_ERR_INVALID_ARG;
+    const int es = dtype == DS_BF16 ? 2 : 4;
+    if (k > kMaxK || N >= (int64_t(1) << 31) || (static_cast<int64_t>(B) * es) % 16 != 0) return DS_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+    Plan P;
+    const ds_status st = make_plan(dev, dtype, rows, N, k, B, B2, options, P);
+    if (st != DS_OK) return st;
+    plan->parts = P.parts;
+    plan->cluster = P.G;
+    plan->threads = kScanThreads;
+    plan->chunk_elems = P.chunk;
+    plan->stages = P.stages;
+    plan->capacity = P.cap;
+    plan->smem_bytes = static_cast<int64_t>(P.smem);
+    plan->workspace_bytes = static_cast<int64_t>(P.ws_bytes);
+    plan->ctas_per_sm = P.ctas_per_sm;
+    plan->merge_launch = P.C > 1 ? 1 : 0;
+    return DS_OK;
+}
+
+ds_status ds_workspace_bytes(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t B, int32_t B2,
+                             const ds_options* options, size_t* bytes) {
+    if (!bytes) return DS_ERR_INVALID_ARG;
+    ds_plan pl;
+    const ds_status st = ds_get_plan(dtype, rows, N, k, B, B2, options, &pl);
+    if (st != DS_OK) return st;
+    *bytes = static_cast<size_t>(pl.workspace_bytes);
+    return DS_OK;
+}
+
+ds_status ds_topk_ex(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
+                     int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx,
+                     const ds_options* options, cudaStream_t stream) {
+    ds_status st = validate(x, dtype, rows, N, row_stride, k, B, B2, out_vals, out_idx);
+    if (st != DS_OK) return st;
+    if (rows == 0) return DS_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return DS_ERR_CUDA;
+    Plan P;
+    st = make_plan(dev, dtype, rows, N, k, B, B2, options, P);
+    if (st != DS_OK) return st;
+    if (rows * P.parts > 0x7FFFFFFFLL) return DS_ERR_UNSUPPORTED;
+    char* ws = nullptr;
+    if (P.ws_bytes > 0) {
+        if (options && options->workspace) {
+            if (options->workspace_bytes < P.ws_bytes) return DS_ERR_WORKSPACE;
+            if (reinterpret_cast<uintptr_t>(options->workspace) & 255u) return DS_ERR_ALIGNMENT;
+            ws = static_cast<char*>(options->workspace);
+        } else {
+            void* p = nullptr;
+            st = library_workspace(dev, P.ws_bytes, stream, &p);
+            if (st != DS_OK) return st;
+            ws = static_cast<char*>(p);
+        }
+    }
+    long long* stats = options ? reinterpret_cast<long long*>(options->stats) : nullptr;
+    if (dtype == DS_BF16)
+        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, stream);
+    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, stream);
+}
+
+ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k, int32_t B,
+                  int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, cudaStream_t stream) {
+    return ds_topk_ex(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, stream);
+}
+
+ds_status ds_get_device_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return DS_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, dsk::g_ds_status, sizeof(v)) != cudaSuccess) return DS_ERR_CUDA;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(dsk::g_ds_status, &zero, sizeof(zero)) != cudaSuccess) return DS_ERR_CUDA;
+    if (v & kErrTimeout) return DS_ERR_TIMEOUT;
+    if (v & (kErrOverflow | kErrInternal)) return DS_ERR_INTERNAL;
+    return DS_OK;
+}
+
+const char* ds_status_string(ds_status s) {
+    switch (s) {
+        case DS_OK: return "ok";
+        case DS_ERR_INVALID_ARG: return "invalid argument";
+        case DS_ERR_ALIGNMENT: return "misaligned pointer or row stride";
+        case DS_ERR_UNSUPPORTED: return "unsupported size or parameter";
+        case DS_ERR_CUDA: return "CUDA runtime error";
+        case DS_ERR_TIMEOUT: return "device-side wait timed out";
+        case DS_ERR_INTERNAL: return "device-side consistency check failed";
+        case DS_ERR_WORKSPACE: return "workspace too small or unavailable";
+    }
+    return "unknown status";
+}
+
+const char* ds_version(void) { return "ds_topk 0.1 sm_103a"; }
+
+ds_status ds_block_order(uint64_t seed, int64_t row, int64_t first_block, int32_t nblocks, int32_t* out_perm,
+                         cudaStream_t stream) {
+    if (!out_perm || nblocks < 1 || nblocks > kPermMax || row < 0 || first_block < 0) return DS_ERR_INVALID_ARG;
+    ds_block_order_kernel<<<1, 256, 0, stream>>>(seed, row, first_block, nblocks, out_perm);
+    return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+ds_status ds_wait_probe(int64_t cycles, cudaStream_t stream) {
+    if (cycles < 0 || cycles > kSpinLimit) return DS_ERR_INVALID_ARG;
+    ds_wait_probe_kernel<<<1, 32, 0, stream>>>(cycles);
+    return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+}  // extern "C"
