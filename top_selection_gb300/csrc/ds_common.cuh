@@ -14,6 +14,7 @@ namespace dsk {
 // ------------------------------------------------------------------ limits --------
 constexpr int kDigitBits = 11;                 // radix-select digit width
 constexpr int kBins = 1 << kDigitBits;         // 2048 histogram bins
+constexpr int kScratchWords = 4096;            // histogram, or the hole and fill lists (2 x 4096 u16)
 constexpr int kMaxK = 4096;                    // largest k the pages support
 constexpr int kPermMax = 1024;                 // blocks one CTA may visit
 constexpr int kMaxStages = 8;                  // deepest copy ring
@@ -103,6 +104,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase completes or
+// `hint_ns` nanoseconds pass, so that waiting warps do not occupy issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (a shared::cluster address from mapa),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with cluster-scope acquire: after it succeeds, writes that other CTAs released
+// with their arrivals are visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // 1-D bulk copy global -> this CTA's shared memory, completion counted in bytes on bar.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                          uint64_t policy) {
@@ -144,6 +181,15 @@ __device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
 __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.relaxed.cluster.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.relaxed.cluster.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
     return v;
 }
 

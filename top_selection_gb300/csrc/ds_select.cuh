@@ -34,16 +34,20 @@ struct Ctrl {
     int issued[kMaxStages];      // copies issued per stage (producer)
     int observed[kMaxStages];    // copies seen complete per stage (consumers)
     int cnt;                     // append cursor of the candidate buffer
-    uint32_t maxkey;             // largest key appended so far
+    uint32_t maxkey;             // largest key appended (reduced from the threads at each select)
     uint32_t sharedT;            // cluster-shared threshold key (authoritative in rank 0), 0 = none
     uint32_t gmax;               // cluster-wide largest key (rank 0)
     int abort;                   // a bounded wait ran out: skip the remaining waits
     int bstar;                   // pivot search results
     uint32_t above;
-    uint32_t eq_taken, holes, fills;
+    uint32_t bcount;             // keys in the pivot bin
     uint32_t out_gt, out_eq;     // output cursors (rank 0 of the cluster)
-    uint32_t warp_tot[32];
+    uint32_t cta_gt, cta_eq;     // this CTA's reserved output ranges
+    uint32_t fp_tot[32];         // pivot-search scratch
+    uint32_t warp_tot[2][32];    // team-scan scratch, two rows used alternately (2 x 16 words)
     uint32_t block_cnt[2][32];   // per-warp appends of the current block, by block parity
+    uint64_t csync[6];           // consumer-only cluster syncs of the warm-up (one arrival per CTA)
+    uint32_t ticket;             // warm-up tickets of pivot-equal keys (rank 0)
     int fin_n;                   // consumer state handed to the whole CTA after the scan
     int fin_hasT;
     uint32_t fin_T;
@@ -52,12 +56,14 @@ struct Ctrl {
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,
 // raises the CTA's abort flag and returns false; it also returns false at once when the
 // abort flag is already up.
+// Each try_wait suspends the thread in hardware for up to 20 us, so a waiting warp costs
+// no issue slots and no shared-memory bandwidth.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctrl* ctrl) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*reinterpret_cast<volatile int*>(&ctrl->abort)) return false;
-        if (mbar_try_wait(bar, parity)) return true;
         if (clock64() - t0 > kSpinLimit) {
             set_status(kErrTimeout);
             *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
@@ -66,44 +72,37 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, Ctr
     }
 }
 
+// Barrier over the first NTH threads: named barrier BAR (0 is the CTA barrier).
 template <int NTH, int BAR>
 __device__ __forceinline__ void team_sync() {
-    if (BAR == 0 && NTH == 0) {
-        __syncthreads();
-    } else {
-        named_bar_sync(BAR, NTH);
-    }
+    named_bar_sync(BAR, NTH);
 }
 
-// Warp append of up to VEC elements per lane.  `mask` selects the lane's elements,
-// keys[e] / cols[e] describe element e.  Returns the number the whole warp appended.
-template <typename KeyT, int VEC>
-__device__ __forceinline__ uint32_t warp_append(uint32_t mask, const uint32_t (&keys)[VEC], uint32_t col0,
-                                                KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int cap, int lane) {
-    const uint32_t c = __popc(mask);
-    const uint32_t incl = warp_incl_scan(c, lane);
-    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+// Exclusive prefix sum of v over the team's threads in thread order, plus the team total.
+// Two back-to-back scans must use different rows.
+template <int NTH, int BAR>
+__device__ __forceinline__ uint32_t team_excl_scan(uint32_t v, Ctrl* ctrl, int row, uint32_t& total, int tid) {
+    constexpr int NW = NTH / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t incl = warp_incl_scan(v, lane);
+    if (lane == 31) ctrl->warp_tot[row][warp] = incl;
+    team_sync<NTH, BAR>();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const uint32_t t = ctrl->warp_tot[row][w];
+        all += t;
+        before += (w < warp) ? t : 0u;
+    }
+    total = all;
+    return before + incl - v;
+}
+
+// Reserves `tot` consecutive candidate slots for the warp; returns the first one.
+__device__ __forceinline__ uint32_t warp_reserve(Ctrl* ctrl, uint32_t tot, int lane) {
     uint32_t base = 0;
     if (lane == 0) base = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->cnt), tot);
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    uint32_t pos = base + incl - c;
-    uint32_t mk = 0;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-        if (mask & (1u << e)) {
-            if (pos < static_cast<uint32_t>(cap)) {
-                ckey[pos] = static_cast<KeyT>(keys[e]);
-                cidx[pos] = col0 + e;
-            } else {
-                set_status(kErrOverflow);
-            }
-            ++pos;
-            mk = max(mk, keys[e]);
-        }
-    }
-    mk = warp_max(mk);
-    if (lane == 0 && tot) atomicMax(&ctrl->maxkey, mk);
-    return tot;
+    return __shfl_sync(0xFFFFFFFFu, base, 0);
 }
 
 // Finds the bin holding the krem-th largest key counted in h[0..nbins).  Every thread
@@ -130,12 +129,12 @@ __device__ __forceinline__ void find_pivot_bin(const uint32_t* h, int nbins, uin
         const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, d);
         if (lane + d < 32) suf += t;
     }
-    if (lane == 0) ctrl->warp_tot[warp] = suf;
+    if (lane == 0) ctrl->fp_tot[warp] = suf;
     team_sync<NTH, BAR>();
     uint32_t higher = 0, all = 0;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
-        const uint32_t t = ctrl->warp_tot[w];
+        const uint32_t t = ctrl->fp_tot[w];
         all += t;
         if (w > warp) higher += t;
     }
@@ -147,6 +146,7 @@ __device__ __forceinline__ void find_pivot_bin(const uint32_t* h, int nbins, uin
             if (acc < krem && acc + c[j] >= krem) {
                 ctrl->bstar = tid * PER + j;
                 ctrl->above = acc;
+                ctrl->bcount = c[j];
             }
             acc += c[j];
         }
@@ -157,110 +157,340 @@ __device__ __forceinline__ void find_pivot_bin(const uint32_t* h, int nbins, uin
     above = ctrl->above;
 }
 
+__device__ __forceinline__ uint32_t group_key(const uint4& g, int e, int es) {
+    const uint32_t w = (es == 2) ? ((e >> 1) == 0 ? g.x : (e >> 1) == 1 ? g.y : (e >> 1) == 2 ? g.z : g.w)
+                                 : (e == 0 ? g.x : e == 1 ? g.y : e == 2 ? g.z : g.w);
+    return (es == 2) ? ((e & 1) ? (w >> 16) : (w & 0xFFFFu)) : w;
+}
+
+// gsum[b] = sum over the cluster's CTAs of their hist[b], b < nbins.  Threads take groups
+// of four bins and issue every CTA's 16-byte remote load before adding, so the remote
+// round trips overlap instead of serialising.  hist and gsum must hold whole groups.
+template <int NTH>
+__device__ __forceinline__ void cluster_hist_sum(const uint32_t* hist, uint32_t* gsum, int nbins, int G, int tid) {
+    const int ng = (nbins + 3) / 4;
+    for (int g = tid; g < ng; g += NTH) {
+        uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+        for (int r0 = 0; r0 < G; r0 += 4) {  // four CTAs' loads in flight at a time
+            uint4 v[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r0 + r < G) v[r] = ld_cluster_v4(map_rank(hist + 4 * g, r0 + r));
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r0 + r < G) {
+                    acc.x += v[r].x;
+                    acc.y += v[r].y;
+                    acc.z += v[r].z;
+                    acc.w += v[r].w;
+                }
+            }
+        }
+        reinterpret_cast<uint4*>(gsum)[g] = acc;
+    }
+}
+
 // Digit shift for the key range [lo, hi].
 __device__ __forceinline__ int range_shift(uint32_t lo, uint32_t hi) {
     const int s = bit_length(hi - lo) - kDigitBits;
     return s > 0 ? s : 0;
 }
 
-// RadixSelectTopK on the team's own buffer: keeps exactly k of the n entries (n > k), the
-// k largest keys, in positions [0, k).  lo/hi bound every key.  Returns the k-th key.
-// Entries that stay are not moved; entries from [k, n) fill the holes in [0, k).
-template <typename KeyT, int NTH, int BAR>
-__device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k, uint32_t lo,
-                            uint32_t hi, int tid) {
-    const int lane = tid & 31, warp = tid >> 5;
-    uint32_t krem = static_cast<uint32_t>(k);
-    uint32_t pivot;
-    while (true) {
+// Histogram of (key - lo) >> s for the keys of [0, n) inside [lo, hi].
+// Calls f(i, key) for every key of [0, n) owned by thread `tid`: thread t takes the
+// 16-byte groups t, t + NTH, ... (16 / sizeof(KeyT) keys each, in index order), so a warp
+// reads contiguous 512-byte rows.  Only the last group pays for bounds checks; the
+// candidate buffer is padded to whole groups.
+template <typename KeyT, int NTH, typename F>
+__device__ __forceinline__ void for_each_key(const KeyT* ckey, int n, int tid, F&& f) {
+    constexpr int ES = sizeof(KeyT), GK = 16 / ES;
+    const int full = n / GK;
+    const uint4* g4 = reinterpret_cast<const uint4*>(ckey);
+    int g = tid;
+#pragma unroll 2
+    for (; g < full; g += NTH) {
+        const uint4 v = g4[g];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (ES == 2) {
+                f(g * GK + 2 * q, w[q] & 0xFFFFu);
+                f(g * GK + 2 * q + 1, w[q] >> 16);
+            } else {
+                f(g * GK + q, w[q]);
+            }
+        }
+    }
+    if (g == full && full * GK < n) {
+        const uint4 v = g4[g];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (ES == 2) {
+                if (g * GK + 2 * q < n) f(g * GK + 2 * q, w[q] & 0xFFFFu);
+                if (g * GK + 2 * q + 1 < n) f(g * GK + 2 * q + 1, w[q] >> 16);
+            } else {
+                if (g * GK + q < n) f(g * GK + q, w[q]);
+            }
+        }
+    }
+}
+
+// Calls f(i0, keys, valid) for each 16-byte group of keys owned by thread `tid` (groups
+// t, t + NTH, ...): i0 is the index of the group's first key, keys[] its GK keys and
+// valid a bit mask of the keys below n.
+template <typename KeyT, int NTH, typename F>
+__device__ __forceinline__ void for_each_group(const KeyT* ckey, int n, int tid, F&& f) {
+    constexpr int ES = sizeof(KeyT), GK = 16 / ES;
+    const int ng = (n + GK - 1) / GK;
+    const uint4* g4 = reinterpret_cast<const uint4*>(ckey);
+#pragma unroll 2
+    for (int g = tid; g < ng; g += NTH) {
+        const uint4 v = g4[g];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t keys[GK];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (ES == 2) {
+                keys[2 * q] = w[q] & 0xFFFFu;
+                keys[2 * q + 1] = w[q] >> 16;
+            } else {
+                keys[q] = w[q];
+            }
+        }
+        const int left = n - g * GK;
+        const uint32_t valid = left >= GK ? ((1u << GK) - 1u) : ((1u << left) - 1u);
+        f(g * GK, keys, valid);
+    }
+}
+
+template <typename KeyT, int NTH>
+__device__ __forceinline__ void build_hist(const KeyT* ckey, int n, uint32_t lo, uint32_t hi, int s, uint32_t* hist,
+                                           int tid, bool all_in_range) {
+    if (all_in_range) {
+        for_each_key<KeyT, NTH>(ckey, n, tid, [&](int, uint32_t kk) { atomicAdd(&hist[(kk - lo) >> s], 1u); });
+    } else {
+        for_each_key<KeyT, NTH>(ckey, n, tid, [&](int, uint32_t kk) {
+            if (kk - lo <= hi - lo) atomicAdd(&hist[(kk - lo) >> s], 1u);
+        });
+    }
+}
+
+// The key of rank krem (1 = largest) among the keys in [lo, hi] of the team's buffer
+// (and, with CL, of the buffers of every CTA of the cluster), by radix passes over
+// adaptive digits.  On return krem is the number of pivot-equal keys to keep.  take_all
+// is set when the range holds fewer than krem keys (then every key in range is kept).
+// hist must be zero on entry; it is left dirty.
+template <typename KeyT, int NTH, int BAR, bool CL>
+__device__ uint32_t radix_pivot(const KeyT* ckey, int n, uint32_t lo, uint32_t hi, uint32_t& krem, bool& take_all,
+                                uint32_t* hist, uint32_t* ghist, int G, Ctrl* ctrl, int tid, uint32_t* eq_count = nullptr,
+                                bool all_in_range = false) {
+    take_all = false;
+    for (int pass = 0;; ++pass) {
         const int s = range_shift(lo, hi);
         const int nbins = static_cast<int>((hi - lo) >> s) + 1;
-        for (int b = tid; b < nbins; b += NTH) hist[b] = 0u;
-        team_sync<NTH, BAR>();
-        for (int i = tid; i < n; i += NTH) {
-            const uint32_t kk = ckey[i];
-            if (kk >= lo && kk <= hi) atomicAdd(&hist[(kk - lo) >> s], 1u);
+        build_hist<KeyT, NTH>(ckey, n, lo, hi, s, hist, tid, pass == 0 && all_in_range);
+        const uint32_t* hsum = hist;
+        if (CL) {
+            cluster_sync_all();
+            cluster_hist_sum<NTH>(hist, ghist, nbins, G, tid);
+            hsum = ghist;
         }
         team_sync<NTH, BAR>();
         int bstar;
         uint32_t above, total;
-        find_pivot_bin<NTH, BAR>(hist, nbins, krem, ctrl, tid, bstar, above, total);
-        if (total < krem) {  // cannot happen for n > k; keep the team consistent anyway
-            set_status(kErrInternal);
-            bstar = 0;
-            above = 0;
+        find_pivot_bin<NTH, BAR>(hsum, nbins, krem, ctrl, tid, bstar, above, total);
+        if (CL) cluster_sync_all();  // every CTA is done reading this pass's histograms
+        if (total < krem) {
+            take_all = true;
+            return lo;
         }
         krem -= above;
-        lo = lo + (static_cast<uint32_t>(bstar) << s);
+        lo += static_cast<uint32_t>(bstar) << s;
         if (s == 0) {
-            pivot = lo;
-            break;
+            if (eq_count) *eq_count = ctrl->bcount;
+            return lo;
         }
         const uint32_t top = lo + ((1u << s) - 1u);
         hi = top < hi ? top : hi;
-        // the next pass rewrites hist and bstar only after two more team barriers
+        for (int b = tid; b < ((nbins + 3) & ~3); b += NTH) hist[b] = 0u;
+        team_sync<NTH, BAR>();
     }
-    // keep: key > pivot, or key == pivot with a ticket below the quota
+}
+
+// Team-wide largest key: reduces every thread's running maximum into ctrl->maxkey and
+// clears the histogram.  Ends with a team barrier.
+template <int NTH, int BAR>
+__device__ __forceinline__ uint32_t reduce_max_and_clear(uint32_t tmax, uint32_t* hist, Ctrl* ctrl, int tid) {
+    const uint32_t wm = warp_max(tmax);
+    if ((tid & 31) == 0) atomicMax(&ctrl->maxkey, wm);
+    for (int b = tid; b < kBins; b += NTH) hist[b] = 0u;
+    team_sync<NTH, BAR>();
+    return ctrl->maxkey;
+}
+
+// Exclusive prefix sums of two values at once (one pair of barriers).
+template <int NTH, int BAR>
+__device__ __forceinline__ void team_excl_scan2(uint32_t a, uint32_t b, Ctrl* ctrl, int row, uint32_t& pa,
+                                                uint32_t& pb, uint32_t& ta, uint32_t& tb, int tid) {
+    constexpr int NW = NTH / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint32_t ia = warp_incl_scan(a, lane), ib = warp_incl_scan(b, lane);
+    if (lane == 31) {
+        ctrl->warp_tot[row][warp] = ia;
+        ctrl->warp_tot[row][16 + warp] = ib;
+    }
+    team_sync<NTH, BAR>();
+    uint32_t ba = 0, bb = 0, sa = 0, sb = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const uint32_t x = ctrl->warp_tot[row][w], y = ctrl->warp_tot[row][16 + w];
+        sa += x;
+        sb += y;
+        ba += (w < warp) ? x : 0u;
+        bb += (w < warp) ? y : 0u;
+    }
+    pa = ba + ia - a;
+    pb = bb + ib - b;
+    ta = sa;
+    tb = sb;
+}
+
+// RadixSelectTopK on the team's own buffer: keeps exactly k of the n entries (n > k), the
+// k largest keys, in positions [0, k).  Keys lie in [lo, ...]; tmax is the thread's
+// largest appended key.  Returns the k-th key.  Entries that stay are not moved; entries
+// from [k, n) fill the holes in [0, k).
+//   One counting pass gives, per thread, the sure holes (key < pivot, i < k), the sure
+// fills (key > pivot, i >= k) and the pivot-equal keys on each side of k.  Pivot-equal
+// keys draw tickets in thread order (a thread's keys below k come before its keys at or
+// above k); the first `quota` are kept.  A listing pass writes the hole positions and
+// fill sources, and the moves then run from the two lists, so no load waits on a store
+// to the array it reads.
+template <typename KeyT, int NTH, int BAR>
+__device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k, uint32_t lo,
+                            uint32_t tmax, int tid) {
+    const uint32_t hi = reduce_max_and_clear<NTH, BAR>(tmax, hist, ctrl, tid);
+    uint32_t krem = static_cast<uint32_t>(k);
+    bool take_all;
+    uint32_t eqn = 0;
+    const uint32_t pivot =
+        radix_pivot<KeyT, NTH, BAR, false>(ckey, n, lo, hi, krem, take_all, hist, hist, 1, ctrl, tid, &eqn, true);
+    if (take_all) set_status(kErrInternal);  // n > k keys all lie in [lo, hi]
     const uint32_t quota = krem;
-    if (tid == 0) {
-        ctrl->eq_taken = 0;
-        ctrl->holes = 0;
-        ctrl->fills = 0;
+    constexpr int GK = 16 / sizeof(KeyT);
+    // Per group of GK keys: bit masks of the keys above, equal to and below the pivot,
+    // and of the keys below position k; counts are popcounts of their combinations.
+    const auto masks = [&](int i0, const uint32_t (&kk)[GK], uint32_t valid, uint32_t& gt, uint32_t& eq,
+                           uint32_t& lt, uint32_t& low) {
+        gt = 0u;
+        eq = 0u;
+#pragma unroll
+        for (int e = 0; e < GK; ++e) {
+            gt |= (kk[e] > pivot ? 1u : 0u) << e;
+            eq |= (kk[e] == pivot ? 1u : 0u) << e;
+        }
+        gt &= valid;
+        eq &= valid;
+        lt = valid & ~(gt | eq);
+        const int below = k - i0;  // keys of the group below position k
+        low = below >= GK ? ((1u << GK) - 1u) : (below <= 0 ? 0u : ((1u << below) - 1u));
+    };
+    // The first MASKED groups of each thread keep their masks in registers for the listing
+    // pass (GK bits each, 32 bits of "greater" and 32 of "equal"); later groups recompute.
+    constexpr int MASKED = 32 / GK;
+    uint32_t gt_keep = 0u, eq_keep_m = 0u;
+    uint32_t hdef = 0, fdef = 0, eqlo = 0, eqhi = 0;
+    {
+        int slot = 0;
+        for_each_group<KeyT, NTH>(ckey, n, tid, [&](int i0, const uint32_t (&kk)[GK], uint32_t valid) {
+            uint32_t gt, eq, lt, low;
+            masks(i0, kk, valid, gt, eq, lt, low);
+            hdef += __popc(lt & low);
+            fdef += __popc(gt & ~low);
+            eqlo += __popc(eq & low);
+            eqhi += __popc(eq & ~low);
+            if (slot < MASKED) {
+                gt_keep |= gt << (slot * GK);
+                eq_keep_m |= eq << (slot * GK);
+            }
+            ++slot;
+        });
     }
-    team_sync<NTH, BAR>();
-    uint16_t* holes = reinterpret_cast<uint16_t*>(hist);  // k <= 4096 positions fit
-    for (int base = warp * 32; base < k; base += NTH) {
-        const int i = base + lane;
-        const bool valid = i < k;
-        const uint32_t kk = valid ? static_cast<uint32_t>(ckey[i]) : 0u;
-        const bool gt = valid && kk > pivot;
-        const bool eq = valid && kk == pivot;
-        const uint32_t emask = __ballot_sync(0xFFFFFFFFu, eq);
-        uint32_t tb = 0;
-        if (emask) {
-            if (lane == 0) tb = atomicAdd(&ctrl->eq_taken, __popc(emask));
-            tb = __shfl_sync(0xFFFFFFFFu, tb, 0);
+    // tickets: pivot-equal keys before this thread
+    uint32_t e0, junk, te, tj;
+    team_excl_scan2<NTH, BAR>(eqlo + eqhi, 0u, ctrl, 0, e0, junk, te, tj, tid);
+    const uint32_t keep_lo = quota > e0 ? min(quota - e0, eqlo) : 0u;
+    const uint32_t keep_hi = quota > e0 + eqlo ? min(quota - e0 - eqlo, eqhi) : 0u;
+    uint32_t h0, f0, th, tf;
+    team_excl_scan2<NTH, BAR>(hdef + eqlo - keep_lo, fdef + keep_hi, ctrl, 1, h0, f0, th, tf, tid);
+    uint16_t* holes = reinterpret_cast<uint16_t*>(hist);  // k <= 4096 positions
+    uint16_t* srcs = holes + kMaxK;                      // k <= 4096 sources
+    uint32_t h = h0, f = f0, e = e0;
+    const auto list_group = [&](int i0, uint32_t valid, uint32_t gt, uint32_t eq) {
+        const int below = k - i0;
+        const uint32_t low = below >= GK ? ((1u << GK) - 1u) : (below <= 0 ? 0u : ((1u << below) - 1u));
+        uint32_t eq_keep = 0u;
+        uint32_t m = eq;
+        while (m) {  // pivot-equal keys kept by ticket, in index order
+            const int b = __ffs(m) - 1;
+            m &= m - 1u;
+            if (e++ < quota) eq_keep |= 1u << b;
         }
-        const bool keep = gt || (eq && tb + __popc(emask & lanemask_lt()) < quota);
-        const bool hole = valid && !keep;
-        const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hole);
-        if (hmask) {
-            uint32_t hb = 0;
-            if (lane == 0) hb = atomicAdd(&ctrl->holes, __popc(hmask));
-            hb = __shfl_sync(0xFFFFFFFFu, hb, 0);
-            if (hole) holes[hb + __popc(hmask & lanemask_lt())] = static_cast<uint16_t>(i);
+        const uint32_t keep = gt | eq_keep;
+        uint32_t hm = valid & low & ~keep;
+        uint32_t fm = keep & ~low;
+        while (hm) {
+            const int b = __ffs(hm) - 1;
+            hm &= hm - 1u;
+            holes[h++] = static_cast<uint16_t>(i0 + b);
         }
-    }
-    team_sync<NTH, BAR>();
-    for (int base = k + warp * 32; base < n; base += NTH) {
-        const int i = base + lane;
-        const bool valid = i < n;
-        const uint32_t kk = valid ? static_cast<uint32_t>(ckey[i]) : 0u;
-        const bool gt = valid && kk > pivot;
-        const bool eq = valid && kk == pivot;
-        const uint32_t emask = __ballot_sync(0xFFFFFFFFu, eq);
-        uint32_t tb = 0;
-        if (emask) {
-            if (lane == 0) tb = atomicAdd(&ctrl->eq_taken, __popc(emask));
-            tb = __shfl_sync(0xFFFFFFFFu, tb, 0);
+        while (fm) {
+            const int b = __ffs(fm) - 1;
+            fm &= fm - 1u;
+            srcs[f++] = static_cast<uint16_t>(i0 + b);
         }
-        const bool keep = gt || (eq && tb + __popc(emask & lanemask_lt()) < quota);
-        const uint32_t kmask = __ballot_sync(0xFFFFFFFFu, keep);
-        if (kmask) {
-            uint32_t fb = 0;
-            if (lane == 0) fb = atomicAdd(&ctrl->fills, __popc(kmask));
-            fb = __shfl_sync(0xFFFFFFFFu, fb, 0);
-            if (keep) {
-                const uint32_t slot = fb + __popc(kmask & lanemask_lt());
-                if (slot < static_cast<uint32_t>(k)) {
-                    const int j = holes[slot];
-                    ckey[j] = static_cast<KeyT>(kk);
-                    cidx[j] = cidx[i];
+    };
+    {
+        const int ng = (n + GK - 1) / GK;
+        int slot = 0;
+        int g = tid;
+        for (; g < ng && slot < MASKED; g += NTH, ++slot) {
+            const int left = n - g * GK;
+            const uint32_t valid = left >= GK ? ((1u << GK) - 1u) : ((1u << left) - 1u);
+            const uint32_t gm = (gt_keep >> (slot * GK)) & ((1u << GK) - 1u);
+            const uint32_t em = (eq_keep_m >> (slot * GK)) & ((1u << GK) - 1u);
+            const int below = k - g * GK;
+            // groups entirely at or above k with nothing kept, and groups entirely below k
+            // with everything kept, contribute no hole and no fill
+            if (em == 0u && ((below <= 0 && gm == 0u) || (below >= GK && gm == valid))) continue;
+            list_group(g * GK, valid, gm, em);
+        }
+        const uint4* g4 = reinterpret_cast<const uint4*>(ckey);
+        for (; g < ng; g += NTH) {
+            const uint4 v = g4[g];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t kk[GK];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (GK == 8) {
+                    kk[2 * q] = w[q] & 0xFFFFu;
+                    kk[2 * q + 1] = w[q] >> 16;
                 } else {
-                    set_status(kErrInternal);
+                    kk[q] = w[q];
                 }
             }
+            const int left = n - g * GK;
+            const uint32_t valid = left >= GK ? ((1u << GK) - 1u) : ((1u << left) - 1u);
+            uint32_t gt, eq, lt, low;
+            masks(g * GK, kk, valid, gt, eq, lt, low);
+            list_group(g * GK, valid, gt, eq);
         }
+    }
+    team_sync<NTH, BAR>();
+    for (uint32_t m = tid; m < th; m += NTH) {
+        const int j = holes[m], i = srcs[m];
+        ckey[j] = ckey[i];
+        cidx[j] = cidx[i];
     }
     if (tid == 0) ctrl->cnt = k;
     team_sync<NTH, BAR>();
@@ -279,87 +509,56 @@ struct OutTarget {
 // Final RadixSelectTopK over the union of the candidates of the cluster's CTAs (CL) or of
 // this CTA alone.  All NT threads of every CTA call it.  lo0 bounds every key that may
 // belong to the answer from below; keys below it are ignored.  Writes min(k, kept) entries
-// and returns that count (meaningful in rank 0; identical everywhere).
+// and returns that count (identical in every CTA of the cluster).  Each CTA reserves its
+// output ranges with one atomic on rank 0's cursors.
 template <typename KeyT, int NT, bool CL>
 __device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_t* hist, uint32_t* ghist, Ctrl* ctrl,
                                  int n, int k, uint32_t lo0, uint32_t hi0, int G, OutTarget out, bool write_ok,
                                  int tid) {
-    const int lane = tid & 31, warp = tid >> 5;
-    uint32_t lo = lo0, hi = hi0;
+    for (int b = tid; b < kBins; b += NT) hist[b] = 0u;
+    __syncthreads();
     uint32_t krem = static_cast<uint32_t>(k);
-    bool take_all = false;
-    uint32_t pivot = 0, total0 = 0;
-    if (hi0 < lo0) {
-        take_all = true;  // nothing in range
-    } else {
-        for (int pass = 0;; ++pass) {
-            const int s = range_shift(lo, hi);
-            const int nbins = static_cast<int>((hi - lo) >> s) + 1;
-            for (int b = tid; b < nbins; b += NT) hist[b] = 0u;
-            __syncthreads();
-            for (int i = tid; i < n; i += NT) {
-                const uint32_t kk = ckey[i];
-                if (kk >= lo && kk <= hi) atomicAdd(&hist[(kk - lo) >> s], 1u);
-            }
-            const uint32_t* hsum = hist;
-            if (CL) {
-                cluster_sync_all();
-                for (int b = tid; b < nbins; b += NT) {
-                    uint32_t g = 0;
-                    for (int r = 0; r < G; ++r) g += ld_cluster_u32(map_rank(hist + b, r));
-                    ghist[b] = g;
-                }
-                hsum = ghist;
-            }
-            __syncthreads();
-            int bstar;
-            uint32_t above, total;
-            find_pivot_bin<NT, 0>(hsum, nbins, krem, ctrl, tid, bstar, above, total);
-            if (CL) cluster_sync_all();  // all remote reads of hist done before it is cleared
-            if (pass == 0) total0 = total;
-            if (total < krem) {  // fewer than k keys in range: keep them all
-                take_all = true;
-                break;
-            }
-            krem -= above;
-            lo = lo + (static_cast<uint32_t>(bstar) << s);
-            if (s == 0) {
-                pivot = lo;
-                break;
-            }
-            const uint32_t top = lo + ((1u << s) - 1u);
-            hi = top < hi ? top : hi;
-            __syncthreads();
+    bool take_all = true;
+    uint32_t pivot = 0;
+    if (hi0 >= lo0)
+        pivot = radix_pivot<KeyT, NT, 0, CL>(ckey, n, lo0, hi0, krem, take_all, hist, ghist, G, ctrl, tid);
+    const uint32_t quota = krem;
+    uint32_t gc = 0, ec = 0;
+    for (int i = tid; i < n; i += NT) {
+        const uint32_t kk = ckey[i];
+        const bool inr = kk >= lo0 && kk <= hi0;
+        gc += (take_all ? inr : (inr && kk > pivot)) ? 1u : 0u;
+        ec += (!take_all && inr && kk == pivot) ? 1u : 0u;
+    }
+    uint32_t tot;
+    const uint32_t pre = team_excl_scan<NT, 0>(gc | (ec << 16), ctrl, 0, tot, tid);
+    if (tid == 0) {
+        const uint32_t GT = tot & 0xFFFFu, EQ = tot >> 16;
+        if (CL) {
+            ctrl->cta_gt = GT ? atom_cluster_add_u32(map_rank(&ctrl->out_gt, 0), GT) : 0u;
+            ctrl->cta_eq = EQ ? atom_cluster_add_u32(map_rank(&ctrl->out_eq, 0), EQ) : 0u;
+        } else {
+            ctrl->cta_gt = 0u;
+            ctrl->cta_eq = 0u;
         }
     }
-    const uint32_t quota = krem;
-    const uint32_t kept = take_all ? total0 : static_cast<uint32_t>(k);
-    const uint32_t a_gt = CL ? map_rank(&ctrl->out_gt, 0) : 0u;
-    const uint32_t a_eq = CL ? map_rank(&ctrl->out_eq, 0) : 0u;
-    for (int base = warp * 32; base < n; base += NT) {
-        const int i = base + lane;
-        const bool valid = i < n;
-        const uint32_t kk = valid ? static_cast<uint32_t>(ckey[i]) : 0u;
-        const bool inr = valid && kk >= lo0 && kk <= hi0;
-        const bool gt = take_all ? inr : (inr && kk > pivot);
-        const bool eq = !take_all && inr && kk == pivot;
-        const uint32_t gmask = __ballot_sync(0xFFFFFFFFu, gt);
-        const uint32_t emask = __ballot_sync(0xFFFFFFFFu, eq);
-        uint32_t gb = 0, eb = 0;
-        if (lane == 0) {
-            if (gmask) gb = CL ? atom_cluster_add_u32(a_gt, __popc(gmask)) : atomicAdd(&ctrl->out_gt, __popc(gmask));
-            if (emask) eb = CL ? atom_cluster_add_u32(a_eq, __popc(emask)) : atomicAdd(&ctrl->out_eq, __popc(emask));
-        }
-        gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
-        eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
+    __syncthreads();
+    uint32_t g = ctrl->cta_gt + (pre & 0xFFFFu);
+    uint32_t e = ctrl->cta_eq + (pre >> 16);
+    // kept entries: all keys in range when take_all (the cluster's total of them), else k
+    uint32_t kept = static_cast<uint32_t>(k);
+    for (int i = tid; i < n; i += NT) {
+        const uint32_t kk = ckey[i];
+        const bool inr = kk >= lo0 && kk <= hi0;
         int64_t slot = -1;
-        if (gt) slot = gb + __popc(gmask & lanemask_lt());
-        if (eq) {
-            const uint32_t t = eb + __popc(emask & lanemask_lt());
+        if (take_all ? inr : (inr && kk > pivot)) {
+            slot = g++;
+        } else if (!take_all && inr && kk == pivot) {
+            const uint32_t t = e++;
             if (t < quota) slot = static_cast<int64_t>(k - quota) + t;
         }
         if (slot >= 0 && write_ok) {
-            if (slot < kept) {
+            if (slot < k) {
                 const int64_t o = out.base + slot;
                 if (out.to_keys) {
                     static_cast<uint32_t*>(out.vals)[o] = kk;
@@ -376,6 +575,8 @@ __device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_
     }
     if (CL) cluster_sync_all();
     else __syncthreads();
+    // (with CL only rank 0's count is meaningful: its cursor saw every CTA's reservation)
+    if (take_all) kept = CL ? ctrl->out_gt : (tot & 0xFFFFu);
     return kept;
 }
 

@@ -64,7 +64,7 @@ __host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages,
     L.cidx = off;
     off += align_up(static_cast<size_t>(cap) * 4, 16);
     L.hist = off;
-    off += kBins * 4;
+    off += kScratchWords * 4;
     L.ghist = off;
     if (G > 1) off += kBins * 4;
     L.perm = off;
@@ -87,7 +87,7 @@ __host__ __device__ inline MergeLayout merge_layout(int es, int cap) {
     L.cidx = off;
     off += align_up(static_cast<size_t>(cap) * 4, 16);
     L.hist = off;
-    off += kBins * 4;
+    off += kScratchWords * 4;
     L.ctrl = off;
     off += align_up(sizeof(Ctrl), 16);
     L.total = off;
@@ -133,56 +133,200 @@ __device__ __forceinline__ uint32_t pass_bits(uint32_t a, uint32_t thr) {
     return a < thr ? 1u : 0u;
 }
 
+// Filters one staged chunk: thread t reads 16-byte vectors t, t + NC, ... (up to 4), so a
+// warp reads contiguous 512-byte rows of shared memory.  One warp vote decides whether
+// anything passed; a warp with survivors reserves its slots with one shared atomic.
+// When every element passes (T = -inf) and the warp's vectors are all full, slots are
+// assigned lane-interleaved so that the stores are bank-conflict free.
+// Warp exclusive prefix of per-lane counts c < 64 and the warp total, from six
+// independent ballots of the count's bit planes (no serial shuffle chain).
+__device__ __forceinline__ uint32_t warp_prefix_small(uint32_t c, uint32_t& total) {
+    const uint32_t lt = lanemask_lt();
+    uint32_t pre = 0u, tot = 0u;
+#pragma unroll
+    for (int b = 0; b < 6; ++b) {
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, (c >> b) & 1u);
+        pre += static_cast<uint32_t>(__popc(m & lt)) << b;
+        tot += static_cast<uint32_t>(__popc(m)) << b;
+    }
+    total = tot;
+    return pre;
+}
+
+// Filters one staged chunk: thread t reads 16-byte vectors t, t + NC, ... (up to 4), so a
+// warp reads contiguous 512-byte rows of shared memory.  A balanced max (T >= +0) or min
+// (T <= -0) tree over the raw words decides whether any element passes; only then are
+// bit masks built.  A warp with survivors reserves its slots with one shared atomic.
+// When every element passes (T = -inf) and the warp's vectors are all full, slots are
+// assigned lane-interleaved so that the stores are bank-conflict free.
 template <typename KeyT, int MODE>
 __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uint32_t col0, uint32_t thr, KeyT* ckey,
-                                                 uint32_t* cidx, Ctrl* ctrl, int cap, int warp, int lane) {
+                                                 uint32_t* cidx, Ctrl* ctrl, int cap, int tid, uint32_t& tmax) {
     constexpr int NC = kNCW * 32;
     constexpr int ES = sizeof(KeyT);
     constexpr int VEC = 16 / ES;
-    uint32_t appended = 0;
-    for (int base = warp * 32; base < nvec; base += NC) {
-        const int vi = base + lane;
-        const bool valid = vi < nvec;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) v = src[vi];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t mask;
-        if (MODE == 0) {
-            mask = valid ? ((1u << VEC) - 1u) : 0u;
-        } else {
-            mask = 0u;
+    constexpr int V = 4;
+    const int lane = tid & 31;
+    uint4 v[V];
+    int nv = 0;  // this thread's valid vectors (a prefix of j = 0 .. V-1)
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (ES == 4) {
-                    mask |= pass_bits<MODE>(w[q], thr) << q;
-                } else {
-                    mask |= pass_bits<MODE>(w[q] << 16, thr) << (2 * q);
-                    mask |= pass_bits<MODE>(w[q], thr) << (2 * q + 1);
+    for (int j = 0; j < V; ++j) {
+        const int vi = tid + j * NC;
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (vi < nvec) {
+            v[j] = src[vi];
+            ++nv;
+        }
+    }
+    if (MODE != 0) {
+        // any element above T?  words compare exactly for their high element; the low
+        // element is compared after shifting it up (see pass_bits)
+        uint32_t r[2 * V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const uint32_t e0 = v[j].x, e1 = v[j].y, e2 = v[j].z, e3 = v[j].w;
+            uint32_t a, b;
+            if (MODE == 1) {
+                a = static_cast<uint32_t>(max(static_cast<int32_t>(e0), static_cast<int32_t>(e1)));
+                b = static_cast<uint32_t>(max(static_cast<int32_t>(e2), static_cast<int32_t>(e3)));
+                if (ES == 2) {
+                    a = static_cast<uint32_t>(max(static_cast<int32_t>(a),
+                                                  max(static_cast<int32_t>(e0 << 16), static_cast<int32_t>(e1 << 16))));
+                    b = static_cast<uint32_t>(max(static_cast<int32_t>(b),
+                                                  max(static_cast<int32_t>(e2 << 16), static_cast<int32_t>(e3 << 16))));
+                }
+                if (j >= nv) a = b = 0x80000000u;  // neutral for a signed max
+            } else {
+                a = min(e0, e1);
+                b = min(e2, e3);
+                if (ES == 2) {
+                    a = min(a, min(e0 << 16, e1 << 16));
+                    b = min(b, min(e2 << 16, e3 << 16));
+                }
+                if (j >= nv) a = b = 0xFFFFFFFFu;  // neutral for an unsigned min
+            }
+            r[2 * j] = a;
+            r[2 * j + 1] = b;
+        }
+#pragma unroll
+        for (int w = 1; w < 2 * V; w *= 2) {
+#pragma unroll
+            for (int i = 0; i + w < 2 * V; i += 2 * w) {
+                r[i] = (MODE == 1) ? static_cast<uint32_t>(max(static_cast<int32_t>(r[i]), static_cast<int32_t>(r[i + w])))
+                                   : min(r[i], r[i + w]);
+            }
+        }
+        const bool any = pass_bits<MODE>(r[0], thr) != 0u;
+        if (!__any_sync(0xFFFFFFFFu, any)) return 0u;
+    }
+    uint32_t mask = 0u;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        if (j < nv) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t bits;
+            if (MODE == 0) {
+                bits = (1u << VEC) - 1u;
+            } else {
+                uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (ES == 4) {
+                        b0 |= pass_bits<MODE>(w[q], thr) << q;
+                    } else {
+                        b0 |= pass_bits<MODE>(w[q] << 16, thr) << (2 * q);
+                        b1 |= pass_bits<MODE>(w[q], thr) << (2 * q + 1);
+                    }
+                }
+                bits = b0 | b1;
+            }
+            mask |= bits << (j * VEC);
+        }
+    }
+    const uint32_t c = __popc(mask);
+    if (MODE == 0) {
+        // every vector of the warp full: lane-interleaved slots
+        const int warp_first = tid - lane;
+        int full_v = 0;
+#pragma unroll
+        for (int j = 0; j < V; ++j) full_v += (warp_first + j * NC + 31 < nvec) ? 1 : 0;
+        const bool uniform = __all_sync(0xFFFFFFFFu, c == static_cast<uint32_t>(full_v * VEC)) && full_v > 0;
+        if (uniform) {
+            const uint32_t tot = 32u * full_v * VEC;
+            const uint32_t base = warp_reserve(ctrl, tot, lane);
+            if (base + tot > static_cast<uint32_t>(cap)) {
+                set_status(kErrOverflow);
+                return tot;
+            }
+#pragma unroll
+            for (int j = 0; j < V; ++j) {
+                if (j < full_v) {
+                    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                    const uint32_t col = col0 + static_cast<uint32_t>(tid + j * NC) * VEC;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (ES == 4) {
+                            const uint32_t key = key_f32(w[q]);
+                            const uint32_t pos = base + (j * 4 + q) * 32 + lane;
+                            ckey[pos] = static_cast<KeyT>(key);
+                            cidx[pos] = col + q;
+                            tmax = max(tmax, key);
+                        } else {
+                            // two bf16 keys at once: each half inverted if its sign is set,
+                            // else its sign bit set
+                            const uint32_t kk = w[q] ^ ((((w[q] >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
+                            const uint32_t pos = base + ((j * 4 + q) * 32 + lane) * 2;
+                            if ((base & 1u) == 0u) {
+                                *reinterpret_cast<uint32_t*>(ckey + pos) = kk;
+                                *reinterpret_cast<uint2*>(cidx + pos) = make_uint2(col + 2 * q, col + 2 * q + 1);
+                            } else {
+                                ckey[pos] = static_cast<KeyT>(kk & 0xFFFFu);
+                                ckey[pos + 1] = static_cast<KeyT>(kk >> 16);
+                                cidx[pos] = col + 2 * q;
+                                cidx[pos + 1] = col + 2 * q + 1;
+                            }
+                            tmax = max(tmax, max(kk & 0xFFFFu, kk >> 16));
+                        }
+                    }
                 }
             }
-            if (!valid) mask = 0u;
+            return tot;
         }
-        if (!__any_sync(0xFFFFFFFFu, mask != 0u)) continue;
-        uint32_t keys[VEC];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (ES == 4) {
-                keys[q] = key_f32(w[q]);
-            } else {
-                keys[2 * q] = key_bf16(w[q] & 0xFFFFu);
-                keys[2 * q + 1] = key_bf16(w[q] >> 16);
-            }
-        }
-        appended += warp_append<KeyT, VEC>(mask, keys, col0 + static_cast<uint32_t>(vi) * VEC, ckey, cidx, ctrl, cap,
-                                           lane);
     }
-    return appended;
+    uint32_t tot;
+    const uint32_t pre = warp_prefix_small(c, tot);
+    uint32_t pos = warp_reserve(ctrl, tot, lane) + pre;
+    while (mask) {
+        const int b = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        const int j = b / VEC, e = b % VEC;
+        uint4 vv = v[0];
+        if (j == 1) vv = v[1];
+        if (j == 2) vv = v[2];
+        if (j == 3) vv = v[3];
+        const int q = (e * ES) >> 2;
+        uint32_t w = vv.x;
+        if (q == 1) w = vv.y;
+        if (q == 2) w = vv.z;
+        if (q == 3) w = vv.w;
+        const uint32_t key = (ES == 4) ? key_f32(w) : key_bf16((e & 1) ? (w >> 16) : (w & 0xFFFFu));
+        if (pos < static_cast<uint32_t>(cap)) {
+            ckey[pos] = static_cast<KeyT>(key);
+            cidx[pos] = col0 + static_cast<uint32_t>(tid + j * NC) * VEC + e;
+        } else {
+            set_status(kErrOverflow);
+        }
+        ++pos;
+        tmax = max(tmax, key);
+    }
+    return tot;
 }
 
 // Elements of the row's last < 16 bytes, read straight from global memory (one per lane).
 template <typename KeyT>
 __device__ __forceinline__ uint32_t filter_tail(const char* xrow, int64_t c_first, int count, bool have, uint32_t tk,
-                                                KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int cap, int lane) {
+                                                KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int cap, int lane,
+                                                uint32_t& tmax) {
     constexpr int ES = sizeof(KeyT);
     const bool valid = lane < count;
     uint32_t key = 0u;
@@ -191,9 +335,19 @@ __device__ __forceinline__ uint32_t filter_tail(const char* xrow, int64_t c_firs
         else key = key_f32(reinterpret_cast<const uint32_t*>(xrow)[c_first + lane]);
     }
     const bool hit = valid && (!have || key > tk);
-    const uint32_t keys[1] = {key};
-    return warp_append<KeyT, 1>(hit ? 1u : 0u, keys, static_cast<uint32_t>(c_first + lane), ckey, cidx, ctrl, cap,
-                                lane);
+    const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
+    if (!hmask) return 0u;
+    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
+    if (hit) {
+        if (pos < static_cast<uint32_t>(cap)) {
+            ckey[pos] = static_cast<KeyT>(key);
+            cidx[pos] = static_cast<uint32_t>(c_first + lane);
+        } else {
+            set_status(kErrOverflow);
+        }
+        tmax = max(tmax, key);
+    }
+    return __popc(hmask);
 }
 
 __device__ __forceinline__ void threshold_mode(int es, bool have, uint32_t tk, int& mode, uint32_t& thr) {
@@ -269,9 +423,234 @@ __global__ void ds_wait_probe_kernel(long long limit) {
     }
 }
 
+// ---------------------------------------------------------------- warm-up ---------
+// Split rows start from the union of the first chunks of the cluster's CTAs: the k
+// largest keys of that union are selected directly from the staged chunks (histograms
+// summed over distributed shared memory), only they are appended, and their smallest key
+// becomes every CTA's threshold T.  This is DeepSelect's first compaction taken over a
+// window that spans the cluster (the pages' implementations likewise raise T from an
+// initial window before the steady scan): the cluster then holds exactly k keys >= T,
+// which is all the later filter and final selection rely on.
+
+// Sync among the consumer warps of every CTA of the cluster (the producer warp keeps
+// streaming): local named barrier, one remote arrival per CTA on every CTA's barrier
+// `idx`, then a bounded cluster-scope wait on the local one.
+__device__ __forceinline__ void consumer_cluster_sync(Ctrl* ctrl, int idx, int G, int tid) {
+    named_bar_sync(1, kNCW * 32);
+    if (G <= 1) return;
+    if (tid == 0) {
+        fence_acq_rel_cluster();
+        for (int r = 0; r < G; ++r) mbar_arrive_remote(map_rank(&ctrl->csync[idx], r));
+    }
+    if (mbar_try_wait_cluster(&ctrl->csync[idx], 0, 20000u)) return;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(&ctrl->csync[idx], 0, 20000u)) {
+        if (*reinterpret_cast<volatile int*>(&ctrl->abort)) return;
+        if (clock64() - t0 > kSpinLimit) {
+            set_status(kErrTimeout);
+            *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+            return;
+        }
+    }
+}
+
+// Keys of one staged chunk held by thread `tid`: vectors tid, tid + NC, ... plus, for
+// warp 0, up to 15 tail bytes read from global memory (one element per lane).
+template <typename KeyT, typename F>
+__device__ __forceinline__ void for_chunk_keys(const uint4* src, int nvec, const char* xrow, int64_t tail_first,
+                                               int tail_n, int tid, F&& f) {
+    constexpr int NC = kNCW * 32;
+    constexpr int ES = sizeof(KeyT);
+    constexpr int VEC = 16 / ES;
+    for (int vi = tid; vi < nvec; vi += NC) {
+        const uint4 v = src[vi];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (ES == 2) {
+                f(vi * VEC + 2 * q, key_bf16(w[q] & 0xFFFFu));
+                f(vi * VEC + 2 * q + 1, key_bf16(w[q] >> 16));
+            } else {
+                f(vi * VEC + q, key_f32(w[q]));
+            }
+        }
+    }
+    if (tid < tail_n) {
+        const uint32_t key = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + tid])
+                                     : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + tid]);
+        f(nvec * VEC + tid, key);
+    }
+}
+
+// Warp append of one key per lane (hit lanes only); returns the warp's count.
+template <typename KeyT>
+__device__ __forceinline__ uint32_t append_one(bool hit, uint32_t key, uint32_t col, KeyT* ckey, uint32_t* cidx,
+                                               Ctrl* ctrl, int cap, int lane, uint32_t& tmax) {
+    const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
+    if (!hmask) return 0u;
+    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
+    if (hit) {
+        if (pos < static_cast<uint32_t>(cap)) {
+            ckey[pos] = static_cast<KeyT>(key);
+            cidx[pos] = col;
+        } else {
+            set_status(kErrOverflow);
+        }
+        tmax = max(tmax, key);
+    }
+    return __popc(hmask);
+}
+
+// The warm-up selection over the first chunk of every CTA of the cluster.  Consumers
+// only.  On return hasT/T hold the new threshold (unchanged when the union holds fewer
+// than k keys, in which case every key was appended) and wcnt counts this warp's appends.
+template <typename KeyT>
+__device__ void warmup_select(const uint4* src, int nvec, const char* xrow, int64_t tail_first, int tail_n,
+                              uint32_t col0, int k, int G, uint32_t* hA, uint32_t* hB, uint32_t* gsum, KeyT* ckey,
+                              uint32_t* cidx, Ctrl* ctrl, int cap, int tid, bool& hasT, uint32_t& T, uint32_t& tmax,
+                              uint32_t& wcnt) {
+    constexpr int NC = kNCW * 32;
+    constexpr int ES = sizeof(KeyT);
+    constexpr int VEC = 16 / ES;
+    const int lane = tid & 31;
+    uint32_t lo = 0u, hi = ES == 2 ? 0xFFFFu : 0xFFFFFFFFu;
+    uint32_t krem = static_cast<uint32_t>(k);
+    bool take_all = false;
+    uint32_t pivot = 0u;
+    int level = 0;
+    for (;; ++level) {
+        const int s = range_shift(lo, hi);
+        const int nbins = static_cast<int>((hi - lo) >> s) + 1;
+        uint32_t* h = (level & 1) ? hB : hA;
+        for (int b = tid; b < ((nbins + 3) & ~3); b += NC) h[b] = 0u;
+        named_bar_sync(1, NC);
+        for_chunk_keys<KeyT>(src, nvec, xrow, tail_first, tail_n, tid, [&](int, uint32_t kk) {
+            if (kk - lo <= hi - lo) atomicAdd(&h[(kk - lo) >> s], 1u);
+        });
+        consumer_cluster_sync(ctrl, level, G, tid);
+        const uint32_t* hs = h;
+        if (G > 1) {
+            cluster_hist_sum<NC>(h, gsum, nbins, G, tid);
+            named_bar_sync(1, NC);
+            hs = gsum;
+        }
+        int bstar;
+        uint32_t above, total;
+        find_pivot_bin<NC, 1>(hs, nbins, krem, ctrl, tid, bstar, above, total);
+        if (total < krem) {  // the union holds fewer than k keys: keep them all
+            take_all = true;
+            break;
+        }
+        krem -= above;
+        lo += static_cast<uint32_t>(bstar) << s;
+        if (s == 0) {
+            pivot = lo;
+            break;
+        }
+        const uint32_t top = lo + ((1u << s) - 1u);
+        hi = top < hi ? top : hi;
+    }
+    const uint32_t quota = krem;
+    const uint32_t a_ticket = G > 1 ? map_rank(&ctrl->ticket, 0) : 0u;
+    // filter the chunk against the pivot; pivot-equal keys draw cluster-wide tickets
+    for (int vi0 = tid - lane; vi0 < nvec; vi0 += NC) {  // warp-uniform rounds, one vector per lane
+        const int vi = vi0 + lane;
+        uint32_t keys[VEC];
+        uint32_t valid = 0u;
+        if (vi < nvec) {
+            const uint4 v = src[vi];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (ES == 2) {
+                    keys[2 * q] = key_bf16(w[q] & 0xFFFFu);
+                    keys[2 * q + 1] = key_bf16(w[q] >> 16);
+                } else {
+                    keys[q] = key_f32(w[q]);
+                }
+            }
+            valid = (1u << VEC) - 1u;
+        } else {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) keys[e] = 0u;
+        }
+        uint32_t gt = 0u, eq = 0u;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            gt |= ((take_all || keys[e] > pivot) ? 1u : 0u) << e;
+            eq |= ((!take_all && keys[e] == pivot) ? 1u : 0u) << e;
+        }
+        gt &= valid;
+        eq &= valid;
+        if (__any_sync(0xFFFFFFFFu, eq != 0u)) {
+            const uint32_t c = __popc(eq);
+            const uint32_t incl = warp_incl_scan(c, lane);
+            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t base = 0u;
+            if (lane == 0) base = G > 1 ? atom_cluster_add_u32(a_ticket, tot) : atomicAdd(&ctrl->ticket, tot);
+            base = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
+            uint32_t m = eq;
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1u;
+                if (base++ < quota) gt |= 1u << b;
+            }
+        }
+        // append this lane's kept keys
+        const uint32_t c = __popc(gt);
+        if (__any_sync(0xFFFFFFFFu, c != 0u)) {
+            const uint32_t incl = warp_incl_scan(c, lane);
+            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            uint32_t pos = warp_reserve(ctrl, tot, lane) + incl - c;
+            uint32_t m = gt;
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1u;
+                uint32_t key = keys[0];
+#pragma unroll
+                for (int e = 1; e < VEC; ++e)
+                    if (b == e) key = keys[e];
+                if (pos < static_cast<uint32_t>(cap)) {
+                    ckey[pos] = static_cast<KeyT>(key);
+                    cidx[pos] = col0 + static_cast<uint32_t>(vi) * VEC + b;
+                } else {
+                    set_status(kErrOverflow);
+                }
+                ++pos;
+                tmax = max(tmax, key);
+            }
+            wcnt += tot;
+        }
+    }
+    // tail elements (row end, < 16 bytes): warp 0
+    if (tail_n > 0 && tid < 32) {
+        const bool valid = lane < tail_n;
+        uint32_t key = 0u;
+        if (valid)
+            key = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane])
+                          : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane]);
+        bool keep = valid && (take_all || key > pivot);
+        const bool eqk = valid && !take_all && key == pivot;
+        const uint32_t em = __ballot_sync(0xFFFFFFFFu, eqk);
+        if (em) {
+            uint32_t base = 0u;
+            if (lane == 0) base = G > 1 ? atom_cluster_add_u32(a_ticket, __popc(em)) : atomicAdd(&ctrl->ticket, __popc(em));
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            if (eqk && base + __popc(em & lanemask_lt()) < quota) keep = true;
+        }
+        wcnt += append_one<KeyT>(keep, key, static_cast<uint32_t>(tail_first + lane), ckey, cidx, ctrl, cap, lane,
+                                 tmax);
+    }
+    if (!take_all) {
+        hasT = true;
+        T = pivot;
+    }
+    consumer_cluster_sync(ctrl, level + 1, G, tid);  // every remote read of this CTA is done
+}
+
 // ---------------------------------------------------------------- scan kernel -----
 template <typename KeyT>
-__global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanParams p) {
+__global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanParams p) {
     constexpr int NC = kNCW * 32;
     constexpr int NT = kScanThreads;
     constexpr int ES = sizeof(KeyT);
@@ -298,13 +677,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
     const int chunk_bytes = p.chunk * ES;
     const bool shared_T = p.G > 1 || p.C > 1;
 
-    if (tid == 0) {
+    {
         int* z = reinterpret_cast<int*>(ctrl);
-        for (size_t i = 0; i < sizeof(Ctrl) / sizeof(int); ++i) z[i] = 0;
+        for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&ctrl->full[s], 1);
             mbar_init(&ctrl->empty[s], kNCW);
         }
+        for (int c = 0; c < 6; ++c) mbar_init(&ctrl->csync[c], p.G);
         fence_mbar_init();
     }
     block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
@@ -348,6 +731,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
         bool hasT = false;
         uint32_t T = 0u;
         uint32_t wcnt = 0u;
+        uint32_t tmax = 0u;
+        uint32_t sh_next = 0u;  // shared threshold loaded during the previous block
         long long sA = 0, sR = 0, sW = 0, sMax = 0;
         for (int i = 0; i < mp; ++i) {
             const int64_t lo = static_cast<int64_t>(perm[i]) * p.B;
@@ -355,18 +740,20 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
             bool have = hasT;
             uint32_t tk = T;
             if (shared_T) {
-                uint32_t sh = 0u;
-                if (lane == 0) {
-                    if (p.G > 1) sh = ld_cluster_u32(a_shT);
-                    if (p.C > 1) {
-                        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-                        if (static_cast<uint32_t>(g >> 32) == p.epoch) sh = max(sh, static_cast<uint32_t>(g));
-                    }
-                }
-                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
+                const uint32_t sh = __shfl_sync(0xFFFFFFFFu, sh_next, 0);
                 if (sh != 0u && (!have || sh > tk)) {
                     tk = sh;
                     have = true;
+                }
+                // issue the load for the next block now; it completes while this one runs
+                if (lane == 0) {
+                    uint32_t t = 0u;
+                    if (p.G > 1) t = ld_cluster_u32(a_shT);
+                    if (p.C > 1) {
+                        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+                        if (static_cast<uint32_t>(g >> 32) == p.epoch) t = max(t, static_cast<uint32_t>(g));
+                    }
+                    sh_next = t;
                 }
             }
             int mode;
@@ -376,17 +763,34 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
                 const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
                 const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
                 const int s = seq % p.stages, use = seq / p.stages;
-                if (wait_bounded(&ctrl->full[s], use & 1, ctrl)) {
-                    if (tid == 0) ctrl->observed[s] = use + 1;
+                const bool got = wait_bounded(&ctrl->full[s], use & 1, ctrl);
+                if (got && tid == 0) ctrl->observed[s] = use + 1;
+                if (seq == 0 && p.parts > 1) {
+                    // split rows: the first chunk of every CTA feeds the cluster warm-up
+                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
+                    const int tail = static_cast<int>(ce - bytes / ES);
+                    warmup_select<KeyT>(src, got ? static_cast<int>(bytes / 16) : 0, xrow, c0 + bytes / ES,
+                                        got ? tail : 0, static_cast<uint32_t>(c0), p.k, p.G, hist,
+                                        hist + kScratchWords / 2, ghist, ckey, cidx, ctrl, p.cap, tid, hasT, T, tmax,
+                                        wcnt);
+                    if (tid == 0 && hasT && shared_T) {
+                        if (p.G > 1) red_cluster_max_u32(a_shT, T);
+                        if (p.C > 1)
+                            atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
+                    }
+                    if (hasT) threshold_mode(ES, true, T, mode, thr);
+                    have = have || hasT;
+                    tk = hasT ? T : tk;
+                } else if (got) {
                     const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
                     const int nvec = static_cast<int>(bytes / 16);
                     const uint32_t col0 = static_cast<uint32_t>(c0);
-                    if (mode == 0) wcnt += filter_chunk<KeyT, 0>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
-                    else if (mode == 1) wcnt += filter_chunk<KeyT, 1>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
-                    else wcnt += filter_chunk<KeyT, 2>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, warp, lane);
+                    if (mode == 0) wcnt += filter_chunk<KeyT, 0>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
+                    else if (mode == 1) wcnt += filter_chunk<KeyT, 1>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
+                    else wcnt += filter_chunk<KeyT, 2>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
                     const int tail = static_cast<int>(ce - bytes / ES);
                     if (tail > 0 && warp == 0)
-                        wcnt += filter_tail<KeyT>(xrow, c0 + bytes / ES, tail, have, tk, ckey, cidx, ctrl, p.cap, lane);
+                        wcnt += filter_tail<KeyT>(xrow, c0 + bytes / ES, tail, have, tk, ckey, cidx, ctrl, p.cap, lane, tmax);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->empty[s]);
@@ -406,12 +810,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
             }
             if (n >= p.k + p.B2) {
                 const uint32_t lo_k = hasT ? T : 0u;
-                const uint32_t hi_k = ctrl->maxkey;
                 if (tid == 0) {
                     sW += n;
                     sR += 1;
                 }
-                T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, lo_k, hi_k, tid);
+                T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, lo_k, tmax, tid);
                 hasT = true;
                 n = p.k;
                 if (tid == 0 && shared_T) {
@@ -421,6 +824,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) ds_scan_kernel(const ScanPara
                 }
             }
         }
+        const uint32_t wm = warp_max(tmax);
+        if (lane == 0) atomicMax(&ctrl->maxkey, wm);
         if (tid == 0) {
             ctrl->fin_n = n;
             ctrl->fin_hasT = hasT ? 1 : 0;
@@ -516,7 +921,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeP
     __syncthreads();
     int n = 0, blk = 0;
     bool hasT = false;
-    uint32_t T = 0u, wcnt = 0u;
+    uint32_t T = 0u, wcnt = 0u, tmax = 0u;
     for (int c = 0; c < p.C; ++c) {
         const int64_t seg = row * p.C + c;
         const int cnt = p.ws_cnt[seg];
@@ -528,11 +933,21 @@ __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeP
                 const int j = base + lane;
                 const bool valid = j < te;
                 const uint32_t key = valid ? sk[t0 + j] : 0u;
-                const uint32_t col = valid ? static_cast<uint32_t>(si[t0 + j]) : 0u;
                 const bool hit = valid && key >= lo_g && (!hasT || key > T);
-                const uint32_t keys[1] = {key};
-                if (__any_sync(0xFFFFFFFFu, hit))
-                    wcnt += warp_append<KeyT, 1>(hit ? 1u : 0u, keys, col, ckey, cidx, ctrl, p.cap, lane);
+                const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
+                if (hmask) {
+                    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
+                    if (hit) {
+                        if (pos < static_cast<uint32_t>(p.cap)) {
+                            ckey[pos] = static_cast<KeyT>(key);
+                            cidx[pos] = static_cast<uint32_t>(si[t0 + j]);
+                        } else {
+                            set_status(kErrOverflow);
+                        }
+                        tmax = max(tmax, key);
+                    }
+                    wcnt += __popc(hmask);
+                }
             }
             if (lane == 0) ctrl->block_cnt[blk & 1][warp] = wcnt;
             wcnt = 0u;
@@ -544,12 +959,17 @@ __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeP
             ++blk;
             if (n >= p.k + p.B2) {
                 const uint32_t lo_k = hasT ? T : lo_g;
-                T = compact<KeyT, NT, 0>(ckey, cidx, hist, ctrl, n, p.k, lo_k, ctrl->maxkey, tid);
+                T = compact<KeyT, NT, 0>(ckey, cidx, hist, ctrl, n, p.k, lo_k, tmax, tid);
                 hasT = true;
                 n = p.k;
             }
         }
     }
+    {
+        const uint32_t wm = warp_max(tmax);
+        if (lane == 0) atomicMax(&ctrl->maxkey, wm);
+    }
+    __syncthreads();
     OutTarget out;
     out.vals = p.out_vals;
     out.idx = p.out_idx;
