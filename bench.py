@@ -218,6 +218,7 @@ def run_gpu(args):
     import synth
     import top_selection_gb300 as ds
     from top_selection_gb300 import build as tbuild
+    from top_selection_gb300.sharding import max_over_ranks, row_range
 
     ws, rank, local = _dist()
     dev = torch.device("cuda", local)
@@ -232,7 +233,10 @@ def run_gpu(args):
         dist.barrier()
     ds.load()
 
-    w = synth.indexer_bf16()
+    # weak scaling: rank r owns global rows [lo, hi) of a ROWS*ws batch (its own copy of
+    # the workload shape, drawn with its own seed); no data-path collective
+    lo, hi = row_range(ROWS * ws, ws, rank)
+    w = synth.indexer_bf16(seed=2001 + rank, rows=hi - lo)
     host = torch.from_numpy(w.x.view(np.int16))
     x0 = host.to(dev)
     props = torch.cuda.get_device_properties(dev)
@@ -303,11 +307,7 @@ def run_gpu(args):
     status = ds.ds_get_device_status(sptr)
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    t_max = ms
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms, device=dev)
     ms_per_step = t_max / args.steps
     value = ws * step_bytes * args.steps / (t_max * 1e-3) / 1e9
 
@@ -349,11 +349,7 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
     e2e = {"value": round(ws * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
            "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": ROWS * K_TOP * (2 + 4),
            "steps": e_steps}
