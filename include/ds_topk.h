@@ -159,6 +159,37 @@ ds_status ds_block_order(uint64_t seed, int64_t row, int64_t first_block, int32_
  * reports it.  Checks the failure path of the device-side waits without a GPU fault. */
 ds_status ds_wait_probe(int64_t cycles, cudaStream_t stream);
 
+/*
+ * ds_topk_noalloc -- ds_topk_ex for callers that cannot allocate device memory.
+ *
+ * This entry point has no counterpart in the pages; it exists for callers that may not
+ * call cudaMalloc: code that runs while a CUDA graph is being captured (where an
+ * allocation would break or escape the capture), serving loops that forbid allocator
+ * calls because cudaMalloc/cudaFree can synchronise the device and stall other work,
+ * and processes whose caching allocator has already reserved nearly all device memory.
+ *
+ * Arguments are those of ds_topk_ex, with `parts` and `cluster` as in ds_options
+ * (0 = library choice).  When the launch needs scratch memory (a row split over more
+ * than one thread-block cluster) it uses a fixed array compiled into the library's
+ * device image instead of a workspace: at most ds_noalloc_scratch_bytes() bytes
+ * (4 MiB; about rows * clusters_per_row * k * 8 bytes are needed); a launch that would
+ * need more returns DS_ERR_WORKSPACE.  The array exists on every device that loads the
+ * library until the process exits.  It calls no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ * The first call on a device that needs the scratch looks up its device address (with
+ * that device current); make that first call before any stream capture.  All calls
+ * share the one array: calls whose work overlaps on the GPU (for instance on different
+ * streams) race on it and must be ordered by the caller.
+ */
+ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N,
+                          int64_t row_stride, int32_t k, int32_t B, int32_t B2, uint64_t seed,
+                          void* out_vals, int32_t* out_idx, int32_t parts, int32_t cluster,
+                          cudaStream_t stream);
+
+/* Size of the fixed scratch array ds_topk_noalloc uses, in bytes. */
+size_t ds_noalloc_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,8 @@ import threading
 __all__ = [
     "DS_BF16", "DS_FP32", "DS_NSTAT", "DSError", "ds_topk", "ds_topk_ex", "ds_get_plan",
     "ds_workspace_bytes", "ds_get_device_status", "ds_status_string", "ds_version",
-    "ds_block_order", "ds_wait_probe", "topk", "library_path", "load",
+    "ds_block_order", "ds_wait_probe", "ds_topk_noalloc", "ds_noalloc_scratch_bytes", "topk",
+    "library_path", "load",
 ]
 
 DS_BF16 = 0
@@ -96,6 +97,10 @@ def load():
         lib.ds_block_order.restype = ctypes.c_int
         lib.ds_wait_probe.argtypes = [i64, vp]
         lib.ds_wait_probe.restype = ctypes.c_int
+        lib.ds_topk_noalloc.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, u64, vp, vp, i32, i32, vp]
+        lib.ds_topk_noalloc.restype = ctypes.c_int
+        lib.ds_noalloc_scratch_bytes.argtypes = []
+        lib.ds_noalloc_scratch_bytes.restype = ctypes.c_size_t
         _lib = lib
         return lib
 
@@ -157,6 +162,19 @@ def ds_block_order(seed, row, first_block, nblocks, out_perm, stream=0) -> int:
 
 def ds_wait_probe(cycles, stream=0) -> int:
     return load().ds_wait_probe(int(cycles), int(stream) or None)
+
+
+def ds_topk_noalloc(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, parts=0, cluster=0,
+                    stream=0) -> int:
+    """ds_topk for callers that cannot allocate: scratch comes from a fixed array in the
+    library (see include/ds_topk.h).  Raw device pointers; returns the ds_status code."""
+    return load().ds_topk_noalloc(int(x) or None, dtype, rows, N, row_stride, k, B, B2, seed,
+                                  int(out_vals) or None, int(out_idx) or None, parts, cluster,
+                                  int(stream) or None)
+
+
+def ds_noalloc_scratch_bytes() -> int:
+    return int(load().ds_noalloc_scratch_bytes())
 
 
 # ------------------------------------------------------------------ torch helper ----

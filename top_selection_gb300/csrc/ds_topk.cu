@@ -999,6 +999,12 @@ struct Workspace {
 };
 static Workspace g_ws[64];
 
+// Scratch for ds_topk_noalloc: a fixed array in the library's device image.  Every device
+// that loads the library holds it until the process exits; calls share it.
+constexpr size_t kStaticWorkspaceBytes = size_t(4) << 20;
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWorkspaceBytes];
+static void* g_static_ws_addr[64];  // device address of g_static_ws, per device
+
 static bool dev_info(int dev, DevInfo& out) {
     if (dev < 0 || dev >= 64) return false;
     std::lock_guard<std::mutex> lk(g_mu);
@@ -1323,6 +1329,47 @@ ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t
                   int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, cudaStream_t stream) {
     return ds_topk_ex(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, stream);
 }
+
+// The same launch as ds_topk_ex, for callers that must not allocate: when the launch
+// needs scratch (rows split over several clusters) it uses g_static_ws instead of a
+// cudaMalloc'ed workspace.  Host code cannot use the array's name as a device address,
+// so the first call on each device (with that device current) looks the address up
+// with cudaGetSymbolAddress and keeps it.  Nothing in the scratch has to start at zero:
+// the per-row shared thresholds carry a call number and stale ones are ignored, and the
+// partial results and their counts are written before they are read in the same call.
+ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
+                          int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, int32_t parts,
+                          int32_t cluster, cudaStream_t stream) {
+    ds_status st = validate(x, dtype, rows, N, row_stride, k, B, B2, out_vals, out_idx);
+    if (st != DS_OK) return st;
+    if (rows == 0) return DS_OK;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return DS_ERR_CUDA;
+    ds_options opt = {};
+    opt.parts = parts;
+    opt.cluster = cluster;
+    Plan P;
+    st = make_plan(dev, dtype, rows, N, k, B, B2, &opt, P);
+    if (st != DS_OK) return st;
+    if (rows * P.parts > 0x7FFFFFFFLL) return DS_ERR_UNSUPPORTED;
+    if (P.ws_bytes > kStaticWorkspaceBytes) return DS_ERR_WORKSPACE;
+    char* ws = nullptr;
+    if (P.ws_bytes > 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!g_static_ws_addr[dev]) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_static_ws) != cudaSuccess || !addr) return DS_ERR_CUDA;
+            g_static_ws_addr[dev] = addr;
+        }
+        ws = static_cast<char*>(g_static_ws_addr[dev]);
+    }
+    if (dtype == DS_BF16)
+        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, stream);
+    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, stream);
+}
+
+size_t ds_noalloc_scratch_bytes(void) { return kStaticWorkspaceBytes; }
 
 ds_status ds_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return DS_ERR_CUDA;
