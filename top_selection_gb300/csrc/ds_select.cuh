@@ -46,6 +46,8 @@ struct Ctrl {
     uint32_t fp_tot[32];         // pivot-search scratch
     uint32_t warp_tot[2][32];    // team-scan scratch, two rows used alternately (2 x 16 words)
     uint32_t block_cnt[2][32];   // per-warp appends of the current block, by block parity
+    int compact_req;             // split rows: a warp saw the buffer reach k + B2
+    int done_warps;              // split rows: consumer warps that have filtered all their chunks
     uint64_t csync[6];           // consumer-only cluster syncs of the warm-up (one arrival per CTA)
     uint32_t ticket;             // warm-up tickets of pivot-equal keys (rank 0)
     int fin_n;                   // consumer state handed to the whole CTA after the scan
@@ -368,13 +370,13 @@ __device__ __forceinline__ void team_excl_scan2(uint32_t a, uint32_t b, Ctrl* ct
 // to the array it reads.
 template <typename KeyT, int NTH, int BAR>
 __device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k, uint32_t lo,
-                            uint32_t tmax, int tid) {
+                            uint32_t tmax, int tid, bool all_in_range = true) {
     const uint32_t hi = reduce_max_and_clear<NTH, BAR>(tmax, hist, ctrl, tid);
     uint32_t krem = static_cast<uint32_t>(k);
     bool take_all;
     uint32_t eqn = 0;
-    const uint32_t pivot =
-        radix_pivot<KeyT, NTH, BAR, false>(ckey, n, lo, hi, krem, take_all, hist, hist, 1, ctrl, tid, &eqn, true);
+    const uint32_t pivot = radix_pivot<KeyT, NTH, BAR, false>(ckey, n, lo, hi, krem, take_all, hist, hist, 1, ctrl,
+                                                              tid, &eqn, all_in_range);
     if (take_all) set_status(kErrInternal);  // n > k keys all lie in [lo, hi]
     const uint32_t quota = krem;
     constexpr int GK = 16 / sizeof(KeyT);

@@ -47,6 +47,8 @@ constexpr int kScanThreads = (kNCW + 1) * 32;
 constexpr int kMergeThreads = kNCW * 32;
 constexpr int kChunkBytesMax = 16384;   // one bulk copy
 constexpr int kMergeTile = 2048;        // entries per merge block
+constexpr int kPageMax = 64;            // split rows: candidate slots a warp reserves at a time
+constexpr uint32_t kSentinelIdx = 0xFFFFFFFFu;  // column of an unused slot (its key is 0)
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -133,11 +135,6 @@ __device__ __forceinline__ uint32_t pass_bits(uint32_t a, uint32_t thr) {
     return a < thr ? 1u : 0u;
 }
 
-// Filters one staged chunk: thread t reads 16-byte vectors t, t + NC, ... (up to 4), so a
-// warp reads contiguous 512-byte rows of shared memory.  One warp vote decides whether
-// anything passed; a warp with survivors reserves its slots with one shared atomic.
-// When every element passes (T = -inf) and the warp's vectors are all full, slots are
-// assigned lane-interleaved so that the stores are bank-conflict free.
 // Warp exclusive prefix of per-lane counts c < 64 and the warp total, from six
 // independent ballots of the count's bit planes (no serial shuffle chain).
 __device__ __forceinline__ uint32_t warp_prefix_small(uint32_t c, uint32_t& total) {
@@ -153,22 +150,27 @@ __device__ __forceinline__ uint32_t warp_prefix_small(uint32_t c, uint32_t& tota
     return pre;
 }
 
-// Filters one staged chunk: thread t reads 16-byte vectors t, t + NC, ... (up to 4), so a
-// warp reads contiguous 512-byte rows of shared memory.  A balanced max (T >= +0) or min
-// (T <= -0) tree over the raw words decides whether any element passes; only then are
-// bit masks built.  A warp with survivors reserves its slots with one shared atomic.
-// When every element passes (T = -inf) and the warp's vectors are all full, slots are
-// assigned lane-interleaved so that the stores are bank-conflict free.
+// Filters one staged chunk and appends its survivors without atomics.  Each consumer
+// thread loads its vectors (t, t + NC, ... up to 4) into registers and the warp releases
+// the ring stage at once; survivors are marked in a bit mask (a max/min tree first
+// decides whether anything passes at all); each warp publishes its count, and after one
+// consumer barrier every warp knows its offset from the counts of the warps before it.
+// Warp 0 also takes the row's last < 16 bytes (one element per lane, from global memory).
+// Returns the chunk's survivor count, identical in every consumer thread; survivors go to
+// positions [n, n + count) in warp order.
 template <typename KeyT, int MODE>
-__device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uint32_t col0, uint32_t thr, KeyT* ckey,
-                                                 uint32_t* cidx, Ctrl* ctrl, int cap, int tid, uint32_t& tmax) {
+__device__ __forceinline__ uint32_t filter_chunk_sync(const uint4* src, int nvec, uint32_t col0, uint32_t thr,
+                                                      const char* xrow, int64_t tail_first, int tail_n, bool have,
+                                                      uint32_t tk, uint64_t* empty_bar, KeyT* ckey, uint32_t* cidx,
+                                                      Ctrl* ctrl, int cap, int tid, int n, int parity,
+                                                      uint32_t& tmax) {
     constexpr int NC = kNCW * 32;
     constexpr int ES = sizeof(KeyT);
     constexpr int VEC = 16 / ES;
     constexpr int V = 4;
-    const int lane = tid & 31;
+    const int lane = tid & 31, warp = tid >> 5;
     uint4 v[V];
-    int nv = 0;  // this thread's valid vectors (a prefix of j = 0 .. V-1)
+    int nv = 0;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
         const int vi = tid + j * NC;
@@ -178,9 +180,17 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
             ++nv;
         }
     }
+    uint32_t tkey = 0u;
+    bool thit = false;
+    if (warp == 0 && lane < tail_n) {
+        tkey = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane])
+                       : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane]);
+        thit = !have || tkey > tk;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);  // the stage is free: everything is in registers
+    bool any = true;
     if (MODE != 0) {
-        // any element above T?  words compare exactly for their high element; the low
-        // element is compared after shifting it up (see pass_bits)
         uint32_t r[2 * V];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
@@ -195,7 +205,7 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
                     b = static_cast<uint32_t>(max(static_cast<int32_t>(b),
                                                   max(static_cast<int32_t>(e2 << 16), static_cast<int32_t>(e3 << 16))));
                 }
-                if (j >= nv) a = b = 0x80000000u;  // neutral for a signed max
+                if (j >= nv) a = b = 0x80000000u;
             } else {
                 a = min(e0, e1);
                 b = min(e2, e3);
@@ -203,7 +213,7 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
                     a = min(a, min(e0 << 16, e1 << 16));
                     b = min(b, min(e2 << 16, e3 << 16));
                 }
-                if (j >= nv) a = b = 0xFFFFFFFFu;  // neutral for an unsigned min
+                if (j >= nv) a = b = 0xFFFFFFFFu;
             }
             r[2 * j] = a;
             r[2 * j + 1] = b;
@@ -216,9 +226,205 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
                                    : min(r[i], r[i + w]);
             }
         }
-        const bool any = pass_bits<MODE>(r[0], thr) != 0u;
-        if (!__any_sync(0xFFFFFFFFu, any)) return 0u;
+        any = __any_sync(0xFFFFFFFFu, pass_bits<MODE>(r[0], thr) != 0u);
     }
+    uint32_t mask = 0u;
+    if (any) {
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            if (j < nv) {
+                const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t bits;
+                if (MODE == 0) {
+                    bits = (1u << VEC) - 1u;
+                } else {
+                    uint32_t b0 = 0u, b1 = 0u;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (ES == 4) {
+                            b0 |= pass_bits<MODE>(w[q], thr) << q;
+                        } else {
+                            b0 |= pass_bits<MODE>(w[q] << 16, thr) << (2 * q);
+                            b1 |= pass_bits<MODE>(w[q], thr) << (2 * q + 1);
+                        }
+                    }
+                    bits = b0 | b1;
+                }
+                mask |= bits << (j * VEC);
+            }
+        }
+    }
+    const uint32_t c = __popc(mask);
+    uint32_t wtot = 0u, pre = 0u;
+    if (__any_sync(0xFFFFFFFFu, c != 0u)) pre = warp_prefix_small(c, wtot);
+    const uint32_t tmask = __ballot_sync(0xFFFFFFFFu, thit);
+    const uint32_t ttot = __popc(tmask);
+    if (lane == 0) ctrl->block_cnt[parity][warp] = wtot + ttot;
+    named_bar_sync(1, NC);
+    uint32_t base = static_cast<uint32_t>(n), total = 0u;
+#pragma unroll
+    for (int w = 0; w < kNCW; ++w) {
+        const uint32_t cw = ctrl->block_cnt[parity][w];
+        base += (w < warp) ? cw : 0u;
+        total += cw;
+    }
+    if (static_cast<uint32_t>(n) + total > static_cast<uint32_t>(cap)) {
+        set_status(kErrOverflow);
+        return 0u;  // nothing written; the buffer keeps its entries (a consistency failure)
+    }
+    if (wtot) {
+        bool done = false;
+        if (MODE == 0) {
+            // whole warp full: lane-interleaved slots (bank-conflict free stores)
+            const int warp_first = tid - lane;
+            int full_v = 0;
+#pragma unroll
+            for (int j = 0; j < V; ++j) full_v += (warp_first + j * NC + 31 < nvec) ? 1 : 0;
+            if (full_v > 0 && wtot == 32u * full_v * VEC && c == static_cast<uint32_t>(full_v * VEC)) {
+                done = true;
+#pragma unroll
+                for (int j = 0; j < V; ++j) {
+                    if (j < full_v) {
+                        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                        const uint32_t col = col0 + static_cast<uint32_t>(tid + j * NC) * VEC;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (ES == 4) {
+                                const uint32_t key = key_f32(w[q]);
+                                const uint32_t pos = base + (j * 4 + q) * 32 + lane;
+                                ckey[pos] = static_cast<KeyT>(key);
+                                cidx[pos] = col + q;
+                                tmax = max(tmax, key);
+                            } else {
+                                // two bf16 keys at once: each half inverted if its sign is set,
+                                // else its sign bit set
+                                const uint32_t kk = w[q] ^ ((((w[q] >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
+                                const uint32_t pos = base + ((j * 4 + q) * 32 + lane) * 2;
+                                if ((base & 1u) == 0u) {
+                                    *reinterpret_cast<uint32_t*>(ckey + pos) = kk;
+                                    *reinterpret_cast<uint2*>(cidx + pos) = make_uint2(col + 2 * q, col + 2 * q + 1);
+                                } else {
+                                    ckey[pos] = static_cast<KeyT>(kk & 0xFFFFu);
+                                    ckey[pos + 1] = static_cast<KeyT>(kk >> 16);
+                                    cidx[pos] = col + 2 * q;
+                                    cidx[pos + 1] = col + 2 * q + 1;
+                                }
+                                tmax = max(tmax, max(kk & 0xFFFFu, kk >> 16));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!done) {
+            uint32_t pos = base + pre;
+            while (mask) {
+                const int b = __ffs(mask) - 1;
+                mask &= mask - 1u;
+                const int j = b / VEC, e = b % VEC;
+                uint4 vv = v[0];
+                if (j == 1) vv = v[1];
+                if (j == 2) vv = v[2];
+                if (j == 3) vv = v[3];
+                const int q = (e * ES) >> 2;
+                uint32_t w = vv.x;
+                if (q == 1) w = vv.y;
+                if (q == 2) w = vv.z;
+                if (q == 3) w = vv.w;
+                const uint32_t key = (ES == 4) ? key_f32(w) : key_bf16((e & 1) ? (w >> 16) : (w & 0xFFFFu));
+                ckey[pos] = static_cast<KeyT>(key);
+                cidx[pos] = col0 + static_cast<uint32_t>(tid + j * NC) * VEC + e;
+                ++pos;
+                tmax = max(tmax, key);
+            }
+        }
+    }
+    if (thit) {
+        const uint32_t pos = base + wtot + __popc(tmask & lanemask_lt());
+        ckey[pos] = static_cast<KeyT>(tkey);
+        cidx[pos] = static_cast<uint32_t>(tail_first + lane);
+        tmax = max(tmax, tkey);
+    }
+    return total;
+}
+
+// Split rows: the filter without a consumer barrier.  Each warp appends into its own
+// page of the candidate buffer (slots [pg_cur, pg_end), reserved with one shared atomic
+// per page), so warps never wait for each other between chunks.  A page that cannot take
+// the warp's survivors is filled first and the rest goes to a new page.  When a
+// reservation reaches `trigger` (k + B2) the warp raises ctrl->compact_req; every warp
+// checks it before its next chunk.  page is the reservation size (0: exact reservations).
+template <typename KeyT, int MODE>
+__device__ __forceinline__ void filter_chunk_paged(const uint4* src, int nvec, uint32_t col0, uint32_t thr,
+                                                   const char* xrow, int64_t tail_first, int tail_n, bool have,
+                                                   uint32_t tk, uint64_t* empty_bar, KeyT* ckey, uint32_t* cidx,
+                                                   Ctrl* ctrl, int cap, int tid, uint32_t& pg_cur, uint32_t& pg_end,
+                                                   uint32_t page, uint32_t trigger, uint32_t& tmax) {
+    constexpr int NC = kNCW * 32;
+    constexpr int ES = sizeof(KeyT);
+    constexpr int VEC = 16 / ES;
+    constexpr int V = 4;
+    const int lane = tid & 31, warp = tid >> 5;
+    uint4 v[V];
+    int nv = 0;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        const int vi = tid + j * NC;
+        v[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (vi < nvec) {
+            v[j] = src[vi];
+            ++nv;
+        }
+    }
+    uint32_t tkey = 0u;
+    bool thit = false;
+    if (warp == 0 && lane < tail_n) {
+        tkey = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane])
+                       : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane]);
+        thit = !have || tkey > tk;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_bar);  // the stage is free: everything is in registers
+    bool any = true;
+    if (MODE != 0) {
+        uint32_t r[2 * V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+            const uint32_t e0 = v[j].x, e1 = v[j].y, e2 = v[j].z, e3 = v[j].w;
+            uint32_t a, b;
+            if (MODE == 1) {
+                a = static_cast<uint32_t>(max(static_cast<int32_t>(e0), static_cast<int32_t>(e1)));
+                b = static_cast<uint32_t>(max(static_cast<int32_t>(e2), static_cast<int32_t>(e3)));
+                if (ES == 2) {
+                    a = static_cast<uint32_t>(max(static_cast<int32_t>(a),
+                                                  max(static_cast<int32_t>(e0 << 16), static_cast<int32_t>(e1 << 16))));
+                    b = static_cast<uint32_t>(max(static_cast<int32_t>(b),
+                                                  max(static_cast<int32_t>(e2 << 16), static_cast<int32_t>(e3 << 16))));
+                }
+                if (j >= nv) a = b = 0x80000000u;
+            } else {
+                a = min(e0, e1);
+                b = min(e2, e3);
+                if (ES == 2) {
+                    a = min(a, min(e0 << 16, e1 << 16));
+                    b = min(b, min(e2 << 16, e3 << 16));
+                }
+                if (j >= nv) a = b = 0xFFFFFFFFu;
+            }
+            r[2 * j] = a;
+            r[2 * j + 1] = b;
+        }
+#pragma unroll
+        for (int w = 1; w < 2 * V; w *= 2) {
+#pragma unroll
+            for (int i = 0; i + w < 2 * V; i += 2 * w) {
+                r[i] = (MODE == 1) ? static_cast<uint32_t>(max(static_cast<int32_t>(r[i]), static_cast<int32_t>(r[i + w])))
+                                   : min(r[i], r[i + w]);
+            }
+        }
+        any = __any_sync(0xFFFFFFFFu, (pass_bits<MODE>(r[0], thr) != 0u) || thit);
+    }
+    if (!any) return;
     uint32_t mask = 0u;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
@@ -243,59 +449,31 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
             mask |= bits << (j * VEC);
         }
     }
-    const uint32_t c = __popc(mask);
-    if (MODE == 0) {
-        // every vector of the warp full: lane-interleaved slots
-        const int warp_first = tid - lane;
-        int full_v = 0;
-#pragma unroll
-        for (int j = 0; j < V; ++j) full_v += (warp_first + j * NC + 31 < nvec) ? 1 : 0;
-        const bool uniform = __all_sync(0xFFFFFFFFu, c == static_cast<uint32_t>(full_v * VEC)) && full_v > 0;
-        if (uniform) {
-            const uint32_t tot = 32u * full_v * VEC;
-            const uint32_t base = warp_reserve(ctrl, tot, lane);
-            if (base + tot > static_cast<uint32_t>(cap)) {
-                set_status(kErrOverflow);
-                return tot;
-            }
-#pragma unroll
-            for (int j = 0; j < V; ++j) {
-                if (j < full_v) {
-                    const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                    const uint32_t col = col0 + static_cast<uint32_t>(tid + j * NC) * VEC;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if (ES == 4) {
-                            const uint32_t key = key_f32(w[q]);
-                            const uint32_t pos = base + (j * 4 + q) * 32 + lane;
-                            ckey[pos] = static_cast<KeyT>(key);
-                            cidx[pos] = col + q;
-                            tmax = max(tmax, key);
-                        } else {
-                            // two bf16 keys at once: each half inverted if its sign is set,
-                            // else its sign bit set
-                            const uint32_t kk = w[q] ^ ((((w[q] >> 15) & 0x00010001u) * 0x7FFFu) | 0x80008000u);
-                            const uint32_t pos = base + ((j * 4 + q) * 32 + lane) * 2;
-                            if ((base & 1u) == 0u) {
-                                *reinterpret_cast<uint32_t*>(ckey + pos) = kk;
-                                *reinterpret_cast<uint2*>(cidx + pos) = make_uint2(col + 2 * q, col + 2 * q + 1);
-                            } else {
-                                ckey[pos] = static_cast<KeyT>(kk & 0xFFFFu);
-                                ckey[pos + 1] = static_cast<KeyT>(kk >> 16);
-                                cidx[pos] = col + 2 * q;
-                                cidx[pos + 1] = col + 2 * q + 1;
-                            }
-                            tmax = max(tmax, max(kk & 0xFFFFu, kk >> 16));
-                        }
-                    }
-                }
-            }
-            return tot;
-        }
-    }
+    const uint32_t c = __popc(mask) + (thit ? 1u : 0u);
     uint32_t tot;
     const uint32_t pre = warp_prefix_small(c, tot);
-    uint32_t pos = warp_reserve(ctrl, tot, lane) + pre;
+    if (tot == 0u) return;
+    // slots: the rest of the current page, then a fresh page for what does not fit
+    const uint32_t rem = pg_end - pg_cur;
+    uint32_t fresh = 0u;
+    if (tot > rem) {
+        const uint32_t need = tot - rem;
+        const uint32_t size = need > page ? need : page;
+        uint32_t b = 0u;
+        if (lane == 0) {
+            b = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->cnt), size);
+            if (b + size >= trigger) *reinterpret_cast<volatile int*>(&ctrl->compact_req) = 1;
+        }
+        fresh = __shfl_sync(0xFFFFFFFFu, b, 0);
+        if (fresh + size > static_cast<uint32_t>(cap)) {
+            set_status(kErrOverflow);
+            return;
+        }
+        pg_end = fresh + size;
+    }
+    const uint32_t cur = pg_cur;
+    pg_cur = (tot > rem) ? fresh + (tot - rem) : cur + tot;
+    uint32_t q = pre;
     while (mask) {
         const int b = __ffs(mask) - 1;
         mask &= mask - 1u;
@@ -304,22 +482,35 @@ __device__ __forceinline__ uint32_t filter_chunk(const uint4* src, int nvec, uin
         if (j == 1) vv = v[1];
         if (j == 2) vv = v[2];
         if (j == 3) vv = v[3];
-        const int q = (e * ES) >> 2;
+        const int qq = (e * ES) >> 2;
         uint32_t w = vv.x;
-        if (q == 1) w = vv.y;
-        if (q == 2) w = vv.z;
-        if (q == 3) w = vv.w;
+        if (qq == 1) w = vv.y;
+        if (qq == 2) w = vv.z;
+        if (qq == 3) w = vv.w;
         const uint32_t key = (ES == 4) ? key_f32(w) : key_bf16((e & 1) ? (w >> 16) : (w & 0xFFFFu));
-        if (pos < static_cast<uint32_t>(cap)) {
-            ckey[pos] = static_cast<KeyT>(key);
-            cidx[pos] = col0 + static_cast<uint32_t>(tid + j * NC) * VEC + e;
-        } else {
-            set_status(kErrOverflow);
-        }
-        ++pos;
+        const uint32_t pos = q < rem ? cur + q : fresh + (q - rem);
+        ckey[pos] = static_cast<KeyT>(key);
+        cidx[pos] = col0 + static_cast<uint32_t>(tid + j * NC) * VEC + e;
+        ++q;
         tmax = max(tmax, key);
     }
-    return tot;
+    if (thit) {
+        const uint32_t pos = q < rem ? cur + q : fresh + (q - rem);
+        ckey[pos] = static_cast<KeyT>(tkey);
+        cidx[pos] = static_cast<uint32_t>(tail_first + lane);
+        tmax = max(tmax, tkey);
+    }
+}
+
+// Marks the unused rest of the warp's page as empty (key 0, column kSentinelIdx): below
+// every threshold, so no selection counts it.
+template <typename KeyT>
+__device__ __forceinline__ void close_page(KeyT* ckey, uint32_t* cidx, uint32_t& pg_cur, uint32_t& pg_end, int lane) {
+    for (uint32_t pos = pg_cur + lane; pos < pg_end; pos += 32) {
+        ckey[pos] = static_cast<KeyT>(0u);
+        cidx[pos] = kSentinelIdx;
+    }
+    pg_cur = pg_end = 0u;
 }
 
 // Elements of the row's last < 16 bytes, read straight from global memory (one per lane).
@@ -730,10 +921,30 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         int n = 0;
         bool hasT = false;
         uint32_t T = 0u;
-        uint32_t wcnt = 0u;
+        uint32_t badd = 0u;     // appends of the current block
         uint32_t tmax = 0u;
         uint32_t sh_next = 0u;  // shared threshold loaded during the previous block
         long long sA = 0, sR = 0, sW = 0, sMax = 0;
+        // split rows: per-warp pages of the candidate buffer, compaction on request
+        const bool split = p.parts > 1;
+        uint32_t pg_cur = 0u, pg_end = 0u;
+        const uint32_t trigger = static_cast<uint32_t>(p.k + p.B2);
+        uint32_t page_size = static_cast<uint32_t>(p.B2) / (2u * kNCW);
+        if (page_size > static_cast<uint32_t>(kPageMax)) page_size = kPageMax;
+        // every consumer warp arrives here, in the loop or after its last chunk
+        const auto split_compact = [&]() {
+            close_page<KeyT>(ckey, cidx, pg_cur, pg_end, lane);
+            named_bar_sync(2, NC);
+            n = ctrl->cnt;
+            if (tid == 0) ctrl->compact_req = 0;
+            T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, hasT ? T : 0u, tmax, tid, false);
+            hasT = true;
+            n = p.k;
+            if (tid == 0 && shared_T) {
+                if (p.G > 1) red_cluster_max_u32(a_shT, T);
+                if (p.C > 1) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
+            }
+        };
         for (int i = 0; i < mp; ++i) {
             const int64_t lo = static_cast<int64_t>(perm[i]) * p.B;
             const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
@@ -763,16 +974,32 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
                 const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
                 const int s = seq % p.stages, use = seq / p.stages;
+                if (split && seq > 0) {
+                    int req = 0;
+                    if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                    if (__shfl_sync(0xFFFFFFFFu, req, 0)) {
+                        split_compact();
+                        threshold_mode(ES, true, T, mode, thr);
+                        have = true;
+                        tk = T;
+                    }
+                }
                 const bool got = wait_bounded(&ctrl->full[s], use & 1, ctrl);
                 if (got && tid == 0) ctrl->observed[s] = use + 1;
                 if (seq == 0 && p.parts > 1) {
                     // split rows: the first chunk of every CTA feeds the cluster warm-up
                     const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
                     const int tail = static_cast<int>(ce - bytes / ES);
+                    uint32_t wcnt = 0u;
                     warmup_select<KeyT>(src, got ? static_cast<int>(bytes / 16) : 0, xrow, c0 + bytes / ES,
                                         got ? tail : 0, static_cast<uint32_t>(c0), p.k, p.G, hist,
                                         hist + kScratchWords / 2, ghist, ckey, cidx, ctrl, p.cap, tid, hasT, T, tmax,
                                         wcnt);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctrl->empty[s]);
+                    // the warm-up appended through the shared cursor; its final sync makes it exact
+                    n = ctrl->cnt;
+                    badd += static_cast<uint32_t>(n);
                     if (tid == 0 && hasT && shared_T) {
                         if (p.G > 1) red_cluster_max_u32(a_shT, T);
                         if (p.C > 1)
@@ -781,33 +1008,50 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                     if (hasT) threshold_mode(ES, true, T, mode, thr);
                     have = have || hasT;
                     tk = hasT ? T : tk;
-                } else if (got) {
+                } else if (split) {
                     const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
-                    const int nvec = static_cast<int>(bytes / 16);
+                    const int nvec = got ? static_cast<int>(bytes / 16) : 0;
+                    const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
                     const uint32_t col0 = static_cast<uint32_t>(c0);
-                    if (mode == 0) wcnt += filter_chunk<KeyT, 0>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
-                    else if (mode == 1) wcnt += filter_chunk<KeyT, 1>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
-                    else wcnt += filter_chunk<KeyT, 2>(src, nvec, col0, thr, ckey, cidx, ctrl, p.cap, tid, tmax);
-                    const int tail = static_cast<int>(ce - bytes / ES);
-                    if (tail > 0 && warp == 0)
-                        wcnt += filter_tail<KeyT>(xrow, c0 + bytes / ES, tail, have, tk, ckey, cidx, ctrl, p.cap, lane, tmax);
+                    const int64_t tfirst = c0 + bytes / ES;
+                    const uint32_t page = (hasT && T != 0u) ? page_size : 0u;
+                    if (mode == 0)
+                        filter_chunk_paged<KeyT, 0>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
+                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
+                    else if (mode == 1)
+                        filter_chunk_paged<KeyT, 1>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
+                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
+                    else
+                        filter_chunk_paged<KeyT, 2>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
+                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
+                } else {
+                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
+                    const int nvec = got ? static_cast<int>(bytes / 16) : 0;
+                    const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
+                    const uint32_t col0 = static_cast<uint32_t>(c0);
+                    const int64_t tfirst = c0 + bytes / ES;
+                    uint32_t add;
+                    if (mode == 0)
+                        add = filter_chunk_sync<KeyT, 0>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
+                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                    else if (mode == 1)
+                        add = filter_chunk_sync<KeyT, 1>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
+                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                    else
+                        add = filter_chunk_sync<KeyT, 2>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
+                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                    n += static_cast<int>(add);
+                    badd += add;
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctrl->empty[s]);
                 ++seq;
             }
-            // end of block: agree on |C| and compact at >= k + B2
-            if (lane == 0) ctrl->block_cnt[i & 1][warp] = wcnt;
-            wcnt = 0u;
-            named_bar_sync(1, NC);
-            uint32_t add = 0u;
-#pragma unroll
-            for (int w = 0; w < kNCW; ++w) add += ctrl->block_cnt[i & 1][w];
-            n += static_cast<int>(add);
+            // end of block (one CTA per row): |C| is known in every thread; compact at >= k + B2
+            if (split) continue;
             if (tid == 0) {
-                sA += add;
+                sA += badd;
                 sMax = n > sMax ? n : sMax;
             }
+            badd = 0u;
             if (n >= p.k + p.B2) {
                 const uint32_t lo_k = hasT ? T : 0u;
                 if (tid == 0) {
@@ -823,6 +1067,36 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                         atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
                 }
             }
+        }
+        if (split) {
+            // A warp out of chunks still joins any compaction another warp requested:
+            // it reads the count of finished warps before the request flag, so a request
+            // raised by the last warp before it finished is always seen.
+            close_page<KeyT>(ckey, cidx, pg_cur, pg_end, lane);
+            __threadfence_block();
+            if (lane == 0) atomicAdd(&ctrl->done_warps, 1);
+            const long long t0 = clock64();
+            while (true) {
+                int d = 0, f = 0;
+                if (lane == 0) {
+                    d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
+                    __threadfence_block();
+                    f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                }
+                d = __shfl_sync(0xFFFFFFFFu, d, 0);
+                f = __shfl_sync(0xFFFFFFFFu, f, 0);
+                if (f) {
+                    split_compact();
+                    continue;
+                }
+                if (d >= kNCW) break;
+                if (clock64() - t0 > kSpinLimit) {  // cannot happen; keep the CTA alive
+                    set_status(kErrTimeout);
+                    break;
+                }
+            }
+            named_bar_sync(1, NC);
+            n = ctrl->cnt;
         }
         const uint32_t wm = warp_max(tmax);
         if (lane == 0) atomicMax(&ctrl->maxkey, wm);
@@ -1052,9 +1326,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.es = dtype == DS_BF16 ? 2 : 4;
     P.m = (N + B - 1) / B;
     P.chunk = B < kChunkBytesMax / P.es ? B : kChunkBytesMax / P.es;
-    const int64_t cap64 = static_cast<int64_t>(k) + B + B2;
+    int64_t cap64 = static_cast<int64_t>(k) + B + B2;
     if (cap64 > (int64_t(1) << 20)) return DS_ERR_UNSUPPORTED;
-    P.cap = static_cast<int>(cap64);
     int parts = opt ? opt->parts : 0;
     if (parts < 0) return DS_ERR_INVALID_ARG;
     if (parts == 0) {
@@ -1067,6 +1340,9 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         if (parts > P.m || (P.m + parts - 1) / parts > kPermMax) return DS_ERR_UNSUPPORTED;
     }
     P.parts = parts;
+    // split rows append through per-warp pages: room for one partly used page per warp
+    if (parts > 1) cap64 += static_cast<int64_t>(kNCW) * kPageMax;
+    P.cap = static_cast<int>(cap64);
     P.perm_cap = static_cast<int>((P.m + parts - 1) / parts);
     int G = opt ? opt->cluster : 0;
     if (G < 0 || G > 16) return DS_ERR_INVALID_ARG;
