@@ -35,8 +35,8 @@ struct Ctrl {
     int observed[kMaxStages];    // copies seen complete per stage (consumers)
     int cnt;                     // append cursor of the candidate buffer
     uint32_t maxkey;             // largest key appended (reduced from the threads at each select)
-    uint32_t sharedT;            // cluster-shared threshold key (authoritative in rank 0), 0 = none
-    uint32_t gmax;               // cluster-wide largest key (rank 0)
+    uint32_t sharedT;            // cluster-shared threshold key (each CTA's copy), 0 = none
+    uint32_t gmax;               // cluster-wide largest key (each CTA's copy)
     int abort;                   // a bounded wait ran out: skip the remaining waits
     int bstar;                   // pivot search results
     uint32_t above;

@@ -42,13 +42,13 @@
 
 namespace dsk {
 
-constexpr int kNCW = 8;                 // consumer warps per CTA
+constexpr int kNCW = 8;                        // consumer warps per CTA
 constexpr int kScanThreads = (kNCW + 1) * 32;
 constexpr int kMergeThreads = kNCW * 32;
-constexpr int kChunkBytesMax = 16384;   // one bulk copy
-constexpr int kMergeTile = 2048;        // entries per merge block
-constexpr int kPageMax = 64;            // split rows: candidate slots a warp reserves at a time
-constexpr uint32_t kSentinelIdx = 0xFFFFFFFFu;  // column of an unused slot (its key is 0)
+constexpr int kChunkBytesMax = 16384;          // one bulk copy
+constexpr int kMergeTile = 2048;               // entries per merge block
+constexpr int kPageMax = 64;                   // split rows: candidate slots a warp reserves at a time
+constexpr uint32_t kSentinelIdx = 0xFFFFFFFFu; // column of an unused slot (its key is 0)
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -840,8 +840,14 @@ __device__ void warmup_select(const uint4* src, int nvec, const char* xrow, int6
 }
 
 // ---------------------------------------------------------------- scan kernel -----
-template <typename KeyT>
+template <typename KeyT, int KIND>
 __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanParams p) {
+    // KIND 0: one CTA per row; 1: rows split over CTAs without a cluster; 2: rows split
+    // over the CTAs of clusters (p.G > 1).  Each kind is its own instantiation, so a kernel
+    // carries only the code of its own path.
+    constexpr bool SPLIT = KIND != 0;
+    constexpr bool CL = KIND == 2;
+    const bool MC = SPLIT && p.C > 1;  // rows split over several clusters
     constexpr int NC = kNCW * 32;
     constexpr int NT = kScanThreads;
     constexpr int ES = sizeof(KeyT);
@@ -851,7 +857,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
     uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
-    uint32_t* ghist = p.G > 1 ? reinterpret_cast<uint32_t*>(smem + L.ghist) : hist;
+    uint32_t* ghist = CL ? reinterpret_cast<uint32_t*>(smem + L.ghist) : hist;
     int32_t* perm = reinterpret_cast<int32_t*>(smem + L.perm);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
 
@@ -860,13 +866,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     const int64_t row = cta / p.parts;
     const int part = static_cast<int>(cta % p.parts);
     const int cl = part / p.G;
-    const uint32_t crank = p.G > 1 ? cluster_ctarank() : 0u;
+    const uint32_t crank = CL ? cluster_ctarank() : 0u;
     const int64_t b0 = static_cast<int64_t>(part) * p.m / p.parts;
     const int64_t b1 = static_cast<int64_t>(part + 1) * p.m / p.parts;
     const int mp = static_cast<int>(b1 - b0);
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
-    const bool shared_T = p.G > 1 || p.C > 1;
+    const bool shared_T = CL || MC;
 
     {
         int* z = reinterpret_cast<int*>(ctrl);
@@ -882,8 +888,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         fence_mbar_init();
     }
     block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
-    if (p.G > 1) cluster_sync_all();  // every CTA's control block is initialised
-    const uint32_t a_shT = p.G > 1 ? map_rank(&ctrl->sharedT, 0) : 0u;
+    if (CL) cluster_sync_all();  // every CTA's control block is initialised
+    // The cluster's shared threshold lives in every CTA's own ctrl->sharedT: a CTA that
+    // raises it writes a max into all G copies, and readers load their local copy.
+    const auto publish_T = [&](uint32_t t) {
+        for (int r = 0; r < p.G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
+    };
 
     if (warp == kNCW) {
         // ------------------------------ producer: bulk copies in block order ------
@@ -923,10 +933,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         uint32_t T = 0u;
         uint32_t badd = 0u;     // appends of the current block
         uint32_t tmax = 0u;
-        uint32_t sh_next = 0u;  // shared threshold loaded during the previous block
+        uint32_t sh_next = 0u;  // other clusters' threshold, loaded during the previous block
         long long sA = 0, sR = 0, sW = 0, sMax = 0;
         // split rows: per-warp pages of the candidate buffer, compaction on request
-        const bool split = p.parts > 1;
         uint32_t pg_cur = 0u, pg_end = 0u;
         const uint32_t trigger = static_cast<uint32_t>(p.k + p.B2);
         uint32_t page_size = static_cast<uint32_t>(p.B2) / (2u * kNCW);
@@ -941,8 +950,8 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
             hasT = true;
             n = p.k;
             if (tid == 0 && shared_T) {
-                if (p.G > 1) red_cluster_max_u32(a_shT, T);
-                if (p.C > 1) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
+                if (CL) publish_T(T);
+                if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
             }
         };
         for (int i = 0; i < mp; ++i) {
@@ -951,20 +960,17 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
             bool have = hasT;
             uint32_t tk = T;
             if (shared_T) {
-                const uint32_t sh = __shfl_sync(0xFFFFFFFFu, sh_next, 0);
+                uint32_t sh = sh_next;
+                if (CL && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
                 if (sh != 0u && (!have || sh > tk)) {
                     tk = sh;
                     have = true;
                 }
-                // issue the load for the next block now; it completes while this one runs
-                if (lane == 0) {
-                    uint32_t t = 0u;
-                    if (p.G > 1) t = ld_cluster_u32(a_shT);
-                    if (p.C > 1) {
-                        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-                        if (static_cast<uint32_t>(g >> 32) == p.epoch) t = max(t, static_cast<uint32_t>(g));
-                    }
-                    sh_next = t;
+                // the global load for the next block is issued now; it completes while this one runs
+                if (MC && lane == 0) {
+                    const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+                    sh_next = static_cast<uint32_t>(g >> 32) == p.epoch ? static_cast<uint32_t>(g) : 0u;
                 }
             }
             int mode;
@@ -974,7 +980,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
                 const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
                 const int s = seq % p.stages, use = seq / p.stages;
-                if (split && seq > 0) {
+                if (SPLIT && seq > 0) {
                     int req = 0;
                     if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
                     if (__shfl_sync(0xFFFFFFFFu, req, 0)) {
@@ -986,7 +992,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 }
                 const bool got = wait_bounded(&ctrl->full[s], use & 1, ctrl);
                 if (got && tid == 0) ctrl->observed[s] = use + 1;
-                if (seq == 0 && p.parts > 1) {
+                if (SPLIT && seq == 0) {
                     // split rows: the first chunk of every CTA feeds the cluster warm-up
                     const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
                     const int tail = static_cast<int>(ce - bytes / ES);
@@ -1001,14 +1007,14 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                     n = ctrl->cnt;
                     badd += static_cast<uint32_t>(n);
                     if (tid == 0 && hasT && shared_T) {
-                        if (p.G > 1) red_cluster_max_u32(a_shT, T);
-                        if (p.C > 1)
+                        if (CL) publish_T(T);
+                        if (MC)
                             atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
                     }
                     if (hasT) threshold_mode(ES, true, T, mode, thr);
                     have = have || hasT;
                     tk = hasT ? T : tk;
-                } else if (split) {
+                } else if (SPLIT) {
                     const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
                     const int nvec = got ? static_cast<int>(bytes / 16) : 0;
                     const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
@@ -1046,7 +1052,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 ++seq;
             }
             // end of block (one CTA per row): |C| is known in every thread; compact at >= k + B2
-            if (split) continue;
+            if (SPLIT) continue;
             if (tid == 0) {
                 sA += badd;
                 sMax = n > sMax ? n : sMax;
@@ -1062,13 +1068,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 hasT = true;
                 n = p.k;
                 if (tid == 0 && shared_T) {
-                    if (p.G > 1) red_cluster_max_u32(a_shT, T);
-                    if (p.C > 1)
+                    if (CL) publish_T(T);
+                    if (MC)
                         atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
                 }
             }
         }
-        if (split) {
+        if (SPLIT) {
             // A warp out of chunks still joins any compaction another warp requested:
             // it reads the count of finished warps before the request flag, so a request
             // raised by the last warp before it finished is always seen.
@@ -1128,25 +1134,25 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
 
     // ------------------------------ final selection over the cluster --------------
     uint32_t lo_own = hasT ? T : 0u;
-    if (p.C > 1) {
+    if (MC) {
         const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
         if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_own = max(lo_own, static_cast<uint32_t>(g));
     }
     uint32_t lo0, hi0;
-    if (p.G > 1) {
-        if (tid == 0) {
-            red_cluster_max_u32(map_rank(&ctrl->gmax, 0), ctrl->maxkey);
-            red_cluster_max_u32(a_shT, lo_own);
+    if (CL) {
+        if (tid < p.G) {
+            red_cluster_max_u32(map_rank(&ctrl->gmax, tid), ctrl->maxkey);
+            red_cluster_max_u32(map_rank(&ctrl->sharedT, tid), lo_own);
         }
         cluster_sync_all();
-        lo0 = ld_cluster_u32(a_shT);
-        hi0 = ld_cluster_u32(map_rank(&ctrl->gmax, 0));
+        lo0 = *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT);
+        hi0 = *reinterpret_cast<volatile uint32_t*>(&ctrl->gmax);
     } else {
         lo0 = lo_own;
         hi0 = ctrl->maxkey;
     }
     OutTarget out;
-    if (p.C > 1) {
+    if (MC) {
         out.vals = p.ws_key;
         out.idx = p.ws_idx;
         out.base = (row * p.C + cl) * static_cast<int64_t>(p.k);
@@ -1160,11 +1166,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     out.esize = ES;
     const bool write_ok = !ctrl->abort;
     uint32_t kept;
-    if (p.G > 1)
+    if constexpr (CL)
         kept = final_select<KeyT, NT, true>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, p.G, out, write_ok, tid);
     else
         kept = final_select<KeyT, NT, false>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, 1, out, write_ok, tid);
-    if (p.C > 1 && crank == 0 && tid == 0) p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(kept);
+    if (MC && crank == 0 && tid == 0) p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(kept);
 }
 
 // ---------------------------------------------------------------- merge kernel ----
@@ -1403,8 +1409,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
 // call under stream capture only launches.
 template <typename Kern>
 static cudaError_t set_smem(Kern kern, int slot, int dev, size_t bytes, bool nonportable) {
-    static size_t done[4][64];
-    static bool np_done[4][64];
+    static size_t done[8][64];
+    static bool np_done[8][64];
     std::lock_guard<std::mutex> lk(g_mu);
     if (done[slot][dev] < bytes) {
         cudaError_t e =
@@ -1458,8 +1464,17 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
         sp.ws_idx = reinterpret_cast<int32_t*>(ws + P.off_idx);
         sp.ws_cnt = reinterpret_cast<int32_t*>(ws + P.off_cnt);
     }
-    auto kern = ds_scan_kernel<KeyT>;
-    const int slot = sizeof(KeyT) == 2 ? 0 : 1;
+    void (*kern)(ScanParams);
+    int slot = sizeof(KeyT) == 2 ? 0 : 1;
+    if (P.parts == 1) {
+        kern = ds_scan_kernel<KeyT, 0>;
+    } else if (P.G == 1) {
+        kern = ds_scan_kernel<KeyT, 1>;
+        slot += 2;
+    } else {
+        kern = ds_scan_kernel<KeyT, 2>;
+        slot += 4;
+    }
     if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows * P.parts), 1, 1);
@@ -1492,7 +1507,8 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
         mp.out_vals = out_vals;
         mp.out_idx = out_idx;
         auto mk = ds_merge_kernel<KeyT>;
-        if (set_smem(mk, slot + 2, P.dev, P.merge_smem, false) != cudaSuccess) return DS_ERR_CUDA;
+        if (set_smem(mk, 6 + (sizeof(KeyT) == 2 ? 0 : 1), P.dev, P.merge_smem, false) != cudaSuccess)
+            return DS_ERR_CUDA;
         mk<<<static_cast<unsigned>(rows), kMergeThreads, P.merge_smem, stream>>>(mp);
         if (cudaGetLastError() != cudaSuccess) return DS_ERR_CUDA;
     }
