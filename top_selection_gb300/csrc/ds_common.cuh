@@ -17,7 +17,7 @@ constexpr int kBins = 1 << kDigitBits;         // 2048 histogram bins
 constexpr int kScratchWords = 4096;            // histogram, or the hole and fill lists (2 x 4096 u16)
 constexpr int kMaxK = 4096;                    // largest k the pages support
 constexpr int kPermMax = 1024;                 // blocks one CTA may visit
-constexpr int kMaxStages = 8;                  // deepest copy ring
+constexpr int kMaxStages = 16;                 // deepest copy ring
 constexpr long long kSpinLimit = 2000000000LL; // ~1 s of SM clock for any single wait
 
 // device status bits (OR-ed into the per-device status word)
@@ -148,6 +148,34 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "%4;" ::"r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// 1-D bulk copy from this CTA's shared memory into another CTA of the cluster: dst and
+// bar are shared::cluster addresses (from mapa) in the receiving CTA, whose mbarrier
+// counts the bytes.  Addresses and size are multiples of 16 bytes.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory visible to bulk copies.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Packed threshold compares.  Each result lane is all ones where a > b or the two are
+// unordered (either is NaN), else zero: 16-bit lanes for two bf16 values per word.
+__device__ __forceinline__ uint32_t set_gtu_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("set.gtu.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t set_gtu_f32(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("set.gtu.u32.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(a)), "f"(__uint_as_float(b)));
+    return d;
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

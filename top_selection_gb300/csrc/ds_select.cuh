@@ -50,6 +50,13 @@ struct Ctrl {
     int done_warps;              // split rows: consumer warps that have filtered all their chunks
     uint64_t csync[6];           // consumer-only cluster syncs of the warm-up (one arrival per CTA)
     uint32_t ticket;             // warm-up tickets of pivot-equal keys (rank 0)
+    int fail_base;               // split rows: first slot of a reservation that did not fit
+    uint64_t wbar;               // split rows: warm-up exchange of group maxima
+    uint64_t xbar[2];            // split rows: final-select histogram exchange, by pass parity
+    uint32_t sel_gt[16];         // split rows: keys above the final pivot, per CTA of the cluster
+    uint32_t sel_eq[16];         // split rows: keys equal to the final pivot, per CTA
+    uint32_t cur_gt, cur_eq;     // split rows: this CTA's output cursors
+    uint32_t wedge;              // split rows: smallest key of the warm-up's pivot bucket
     int fin_n;                   // consumer state handed to the whole CTA after the scan
     int fin_hasT;
     uint32_t fin_T;
@@ -369,7 +376,7 @@ __device__ __forceinline__ void team_excl_scan2(uint32_t a, uint32_t b, Ctrl* ct
 // fill sources, and the moves then run from the two lists, so no load waits on a store
 // to the array it reads.
 template <typename KeyT, int NTH, int BAR>
-__device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k, uint32_t lo,
+__device__ __noinline__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k, uint32_t lo,
                             uint32_t tmax, int tid, bool all_in_range = true) {
     const uint32_t hi = reduce_max_and_clear<NTH, BAR>(tmax, hist, ctrl, tid);
     uint32_t krem = static_cast<uint32_t>(k);
@@ -425,8 +432,8 @@ __device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ct
     const uint32_t keep_hi = quota > e0 + eqlo ? min(quota - e0 - eqlo, eqhi) : 0u;
     uint32_t h0, f0, th, tf;
     team_excl_scan2<NTH, BAR>(hdef + eqlo - keep_lo, fdef + keep_hi, ctrl, 1, h0, f0, th, tf, tid);
-    uint16_t* holes = reinterpret_cast<uint16_t*>(hist);  // k <= 4096 positions
-    uint16_t* srcs = holes + kMaxK;                      // k <= 4096 sources
+    uint16_t* holes = reinterpret_cast<uint16_t*>(hist);  // at most k positions
+    uint16_t* srcs = holes + k;                          // at most k sources
     uint32_t h = h0, f = f0, e = e0;
     const auto list_group = [&](int i0, uint32_t valid, uint32_t gt, uint32_t eq) {
         const int below = k - i0;
@@ -444,12 +451,14 @@ __device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ct
         while (hm) {
             const int b = __ffs(hm) - 1;
             hm &= hm - 1u;
-            holes[h++] = static_cast<uint16_t>(i0 + b);
+            if (h < static_cast<uint32_t>(k)) holes[h] = static_cast<uint16_t>(i0 + b);
+            ++h;
         }
         while (fm) {
             const int b = __ffs(fm) - 1;
             fm &= fm - 1u;
-            srcs[f++] = static_cast<uint16_t>(i0 + b);
+            if (f < static_cast<uint32_t>(k)) srcs[f] = static_cast<uint16_t>(i0 + b);
+            ++f;
         }
     };
     {
@@ -489,10 +498,14 @@ __device__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ct
         }
     }
     team_sync<NTH, BAR>();
-    for (uint32_t m = tid; m < th; m += NTH) {
+    if (th != tf || th > static_cast<uint32_t>(k)) set_status(kErrInternal);  // every hole has one fill
+    const uint32_t moves = min(min(th, tf), static_cast<uint32_t>(k));
+    for (uint32_t m = tid; m < moves; m += NTH) {
         const int j = holes[m], i = srcs[m];
-        ckey[j] = ckey[i];
-        cidx[j] = cidx[i];
+        if (j < k && i < n) {
+            ckey[j] = ckey[i];
+            cidx[j] = cidx[i];
+        }
     }
     if (tid == 0) ctrl->cnt = k;
     team_sync<NTH, BAR>();

@@ -1,0 +1,688 @@
+// ds_split.cuh -- DeepSelect on rows split over several CTAs (a thread-block cluster per
+// group of G parts, and optionally C clusters per row).
+//
+// DeepSelect-deep-dive.md, "Implementation", has the CTAs of a cluster scan parts of one
+// row, share the threshold T through distributed shared memory and merge their
+// candidates.  This kernel keeps that structure and arranges the work for short critical
+// paths on sm_103a:
+//
+//   * A producer warp issues every chunk of the part into a ring of bulk-copy stages at
+//     once (the whole part when it fits), in the part's Philox block order.
+//   * Warm-up: the first chunk of every CTA is reduced to group maxima (the largest key
+//     of each group of g consecutive elements).  The CTAs exchange them with bulk copies
+//     into each other's shared memory, and every CTA derives the same threshold from the
+//     union: T sits just below the 2048-bin top-digit bucket that holds the k-th largest
+//     group maximum.  At least k groups have a maximum at or above that bucket, so at
+//     least k elements of the cluster are kept above T: every element at or below T is
+//     outside the top k (the threshold invariant of the deep dive's proof).
+//   * Filter: each consumer warp owns whole chunks (chunk q goes to warp (q - 1) mod 8),
+//     so chunks are filtered in parallel.  Lanes read 16-byte vectors, compare packed
+//     values against T with one instruction per word, count survivors, reserve their
+//     slots with one shared atomic per warp and write them.  A reservation that does not
+//     fit makes every warp join a RadixSelectTopK compaction of the CTA's buffer to k
+//     (which raises T); the warp then resumes where it stopped.
+//   * Final: the cluster selects the k largest keys of the union of its buffers by
+//     most-significant-digit radix passes over 1024 bins.  Each pass, every CTA pushes
+//     its histogram to every other CTA; all CTAs then hold the same sums, find the same
+//     pivot bin, and know every CTA's count above the pivot, so each writes its share of
+//     the output at offsets it computes itself.
+//
+// The packed compare is "greater or unordered" against a float threshold chosen so that
+// every element whose key exceeds T passes (NaNs always pass, and -0 passes a -0
+// threshold); elements that pass without exceeding T are extra candidates that the
+// key-based selections never pick, since at least k keys above T exist.
+#pragma once
+
+namespace dsk {
+
+constexpr int kXBits = 9;               // final-select digit width
+constexpr int kXBins = 1 << kXBits;     // final-select bins per pass (exchanged as uint16)
+constexpr int kWarmMaxBytes = 16384;    // group maxima exchanged by the warm-up, all CTAs
+
+struct SplitLayout {
+    size_t ring, ckey, cidx, scratch, wx, xf, perm, ctrl, total;
+};
+
+// Scratch: the warm-up's 2048-bin histogram, the final select's histogram, and the
+// compaction's hole and fill lists (k uint16 each).
+__host__ __device__ inline size_t split_scratch_bytes(int k) {
+    const size_t lists = static_cast<size_t>(4) * k;
+    return align_up(lists > kBins * 4 ? lists : static_cast<size_t>(kBins) * 4, 16);
+}
+
+// wm: group maxima per CTA in the warm-up (a multiple of 256).  Regions that other CTAs
+// write into (wx: the warm-up's maxima, xf: two rounds of the final select's uint16
+// histograms) are separate from the copy ring and from each other, so a CTA that runs
+// ahead never writes over memory a slower CTA still uses.
+__host__ __device__ inline SplitLayout split_layout(int es, int chunk, int stages, int cap, int G, int wm, int k,
+                                                   int perm_cap) {
+    SplitLayout L;
+    size_t off = 0;
+    L.ring = off;
+    off += align_up(static_cast<size_t>(stages) * chunk * es, 128);
+    L.ckey = off;
+    off += align_up(static_cast<size_t>(cap) * es, 16);
+    L.cidx = off;
+    off += align_up(static_cast<size_t>(cap) * 4, 16);
+    L.scratch = off;
+    off += split_scratch_bytes(k);
+    L.wx = off;
+    off += align_up(static_cast<size_t>(G) * wm * es, 16);
+    L.xf = off;
+    off += align_up(static_cast<size_t>(4) * kXBins * G, 16);
+    L.perm = off;
+    off += align_up(static_cast<size_t>(perm_cap) * 4, 16);
+    L.ctrl = off;
+    off += align_up(sizeof(Ctrl), 16);
+    L.total = off;
+    return L;
+}
+
+// Bits of the float compare threshold for key T (see the file comment).  No threshold:
+// a NaN, against which every value compares unordered.
+template <typename KeyT>
+__device__ __forceinline__ uint32_t compare_bits(bool has, uint32_t T) {
+    if (sizeof(KeyT) == 2) {
+        uint32_t t = 0x7FC0u;
+        if (has) {
+            const uint32_t b = unkey_bf16(T);
+            if ((b & 0x7F80u) == 0x7F80u && (b & 0x7Fu)) t = (b & 0x8000u) ? 0x7FC0u : 0x7F80u;
+            else if (b == 0x8000u) t = 0x8001u;
+            else t = b;
+        }
+        return t | (t << 16);
+    } else {
+        if (!has) return 0x7FC00000u;
+        const uint32_t b = unkey_f32(T);
+        if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x7FFFFFu)) return (b & 0x80000000u) ? 0x7FC00000u : 0x7F800000u;
+        if (b == 0x80000000u) return 0x80000001u;
+        return b;
+    }
+}
+
+// Bounded wait with cluster-scope acquire (data other CTAs pushed is visible after it).
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity, Ctrl* ctrl) {
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<volatile int*>(&ctrl->abort)) return false;
+        if (clock64() - t0 > kSpinLimit) {
+            set_status(kErrTimeout);
+            *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+            return false;
+        }
+    }
+}
+
+// One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
+// last tail_n elements from global memory) against the compare bits tb and appends the
+// survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
+// ...); `pass` is the first pass to run and, when a reservation does not fit the buffer,
+// the pass to resume after the compaction (the function then returns false and has
+// written nothing of that pass).
+template <typename KeyT>
+__device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint32_t col0, const char* xrow,
+                                           int64_t tail_first, int tail_n, uint32_t tb, KeyT* ckey, uint32_t* cidx,
+                                           Ctrl* ctrl, uint32_t cap, int lane, int& pass, uint32_t& tmax) {
+    constexpr int ES = sizeof(KeyT);
+    constexpr int EPV = 16 / ES;          // elements per vector
+    constexpr int MW = 16 * EPV / 32;     // mask words per pass and lane
+    const uint4* vec = reinterpret_cast<const uint4*>(stage);
+    const uint32_t lt = lanemask_lt();
+    const int npass = nvec > 0 ? (nvec + 511) / 512 : (tail_n > 0 ? 1 : 0);
+    for (; pass < npass; ++pass) {
+        const int p0 = pass * 512;
+        uint32_t m[MW];
+#pragma unroll
+        for (int w = 0; w < MW; ++w) m[w] = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int v = p0 + lane + 32 * i;
+            if (v < nvec) {
+                const uint4 x = vec[v];
+                uint32_t bits;
+                if (ES == 2) {
+                    const uint32_t r0 = set_gtu_bf16x2(x.x, tb) & 0x10001u, r1 = set_gtu_bf16x2(x.y, tb) & 0x10001u;
+                    const uint32_t r2 = set_gtu_bf16x2(x.z, tb) & 0x10001u, r3 = set_gtu_bf16x2(x.w, tb) & 0x10001u;
+                    const uint32_t y = r0 | (r1 << 2) | (r2 << 4) | (r3 << 6);  // element 2q at bit 2q, 2q+1 at 2q+16
+                    bits = (y | (y >> 15)) & 0xFFu;
+                } else {
+                    bits = (set_gtu_f32(x.x, tb) & 1u) | (set_gtu_f32(x.y, tb) & 2u) | (set_gtu_f32(x.z, tb) & 4u) |
+                           (set_gtu_f32(x.w, tb) & 8u);
+                }
+                m[(i * EPV) / 32] |= bits << ((i * EPV) % 32);
+            }
+        }
+        // the row's last elements (fewer than 16 bytes), one per lane, in the first pass
+        uint32_t tkey = 0u;
+        bool thit = false;
+        if (pass == 0 && lane < tail_n) {
+            if (ES == 2) {
+                const uint32_t h = reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane];
+                thit = (set_gtu_bf16x2(h | (h << 16), tb) & 1u) != 0u;
+                tkey = key_bf16(h);
+            } else {
+                const uint32_t h = reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane];
+                thit = set_gtu_f32(h, tb) != 0u;
+                tkey = key_f32(h);
+            }
+        }
+        uint32_t c = thit ? 1u : 0u;
+#pragma unroll
+        for (int w = 0; w < MW; ++w) c += __popc(m[w]);
+        // warp exclusive prefix of c <= 129 from its eight bit planes
+        uint32_t pre = 0u, tot = 0u;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const uint32_t plane = __ballot_sync(0xFFFFFFFFu, (c >> b) & 1u);
+            pre += static_cast<uint32_t>(__popc(plane & lt)) << b;
+            tot += static_cast<uint32_t>(__popc(plane)) << b;
+        }
+        if (tot == 0u) continue;
+        uint32_t base = 0u;
+        int fits = 1;
+        if (lane == 0) {
+            base = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->cnt), tot);
+            if (base + tot > cap) {
+                fits = 0;
+                atomicMin(&ctrl->fail_base, static_cast<int>(base));
+                *reinterpret_cast<volatile int*>(&ctrl->compact_req) = 1;
+            }
+        }
+        if (!__shfl_sync(0xFFFFFFFFu, fits, 0)) return false;
+        uint32_t pos = __shfl_sync(0xFFFFFFFFu, base, 0) + pre;
+#pragma unroll
+        for (int w = 0; w < MW; ++w) {
+            uint32_t mm = m[w];
+            while (mm) {
+                const int b = w * 32 + __ffs(mm) - 1;
+                mm &= mm - 1u;
+                const int col = (p0 + lane + 32 * (b / EPV)) * EPV + (b % EPV);  // element of the chunk
+                const uint32_t raw = ES == 2 ? reinterpret_cast<const uint16_t*>(stage)[col]
+                                             : reinterpret_cast<const uint32_t*>(stage)[col];
+                const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+                ckey[pos] = static_cast<KeyT>(key);
+                cidx[pos] = col0 + static_cast<uint32_t>(col);
+                ++pos;
+                tmax = max(tmax, key);
+            }
+        }
+        if (thit) {
+            ckey[pos] = static_cast<KeyT>(tkey);
+            cidx[pos] = static_cast<uint32_t>(tail_first + lane);
+            tmax = max(tmax, tkey);
+        }
+    }
+    return true;
+}
+
+template <typename KeyT>
+__global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanParams p) {
+    constexpr int NC = kNCW * 32;
+    constexpr int NT = kScanThreads;
+    constexpr int ES = sizeof(KeyT);
+    constexpr int EPV = 16 / ES;
+    constexpr int KW = 8 * ES;  // key width in bits
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int G = p.G;
+    const int wm = p.wm;
+    const SplitLayout L = split_layout(ES, p.chunk, p.stages, p.cap, G, wm, p.k, p.perm_cap);
+    uint8_t* ring = smem + L.ring;
+    KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
+    uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.scratch);
+    KeyT* wx = reinterpret_cast<KeyT*>(smem + L.wx);
+    int32_t* perm = reinterpret_cast<int32_t*>(smem + L.perm);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t cta = blockIdx.x;
+    const int64_t row = cta / p.parts;
+    const int part = static_cast<int>(cta % p.parts);
+    const int cl = part / G;
+    const uint32_t crank = G > 1 ? cluster_ctarank() : 0u;
+    const int64_t b0 = static_cast<int64_t>(part) * p.m / p.parts;
+    const int64_t b1 = static_cast<int64_t>(part + 1) * p.m / p.parts;
+    const int mp = static_cast<int>(b1 - b0);
+    const char* xrow = p.x + row * p.stride_bytes;
+    const int chunk_bytes = p.chunk * ES;
+    const int cpb = (p.B + p.chunk - 1) / p.chunk;  // chunk slots per block
+    const int nq = mp * cpb;
+    const bool MC = p.C > 1;
+    const uint32_t cap = static_cast<uint32_t>(p.cap);
+
+    {
+        int* z = reinterpret_cast<int*>(ctrl);
+        for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&ctrl->full[s], 1);
+            mbar_init(&ctrl->empty[s], 1);
+        }
+        mbar_init(&ctrl->wbar, 1);
+        mbar_init(&ctrl->xbar[0], 1);
+        mbar_init(&ctrl->xbar[1], 1);
+        ctrl->fail_base = 0x7FFFFFFF;
+        fence_mbar_init();
+    }
+    block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
+    if (G > 1) cluster_sync_all();  // every CTA's barriers are initialised before any remote use
+
+    // chunk slot q: block perm[q / cpb], sub-chunk q % cpb (empty past the row's end)
+    const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) {
+        const int64_t lo = static_cast<int64_t>(perm[q / cpb]) * p.B;
+        const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
+        c0 = lo + static_cast<int64_t>(q % cpb) * p.chunk;
+        ce = c0 < hi ? ((hi - c0) < p.chunk ? (hi - c0) : p.chunk) : 0;
+    };
+    const auto publish_T = [&](uint32_t t) {
+        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
+        if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
+    };
+
+    if (warp == kNCW) {
+        // ------------------------------ producer ------------------------------------
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int q = 0; q < nq; ++q) {
+                int64_t c0, ce;
+                chunk_at(q, c0, ce);
+                const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+                const int s = q % p.stages, use = q / p.stages;
+                if (use > 0 && !wait_bounded(&ctrl->empty[s], (use - 1) & 1, ctrl)) break;
+                if (bytes) {
+                    mbar_arrive_expect_tx(&ctrl->full[s], bytes);
+                    bulk_g2s(ring + static_cast<size_t>(s) * chunk_bytes, xrow + c0 * ES, bytes, &ctrl->full[s], pol);
+                } else {
+                    mbar_arrive(&ctrl->full[s]);
+                }
+                ctrl->issued[s] = use + 1;
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ consumers -----------------------------------
+        bool hasT = false;
+        uint32_t T = 0u;
+        uint32_t tmax = 0u;
+        uint32_t gnext = 0u;  // other clusters' threshold, loaded one chunk ahead
+        // every consumer warp calls this together (from its chunk loop or the drain)
+        const auto join_compaction = [&]() {
+            named_bar_sync(2, NC);
+            const int fb = *reinterpret_cast<volatile int*>(&ctrl->fail_base);
+            const int cn = *reinterpret_cast<volatile int*>(&ctrl->cnt);
+            int n = fb < cn ? fb : cn;
+            n = n < p.cap ? n : p.cap;  // (a bound only: reservations never pass cap)
+            named_bar_sync(2, NC);
+            if (tid == 0) {
+                ctrl->compact_req = 0;
+                ctrl->fail_base = 0x7FFFFFFF;
+            }
+            // The threshold bounds the cluster's union, not this buffer alone, so the
+            // compaction ranks every key of the buffer.
+            const uint32_t piv = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, 0u, tmax, tid, true);
+            T = hasT && T > piv ? T : piv;
+            hasT = true;
+            if (tid == 0) publish_T(T);
+        };
+        // A warp waiting for its next chunk holds no stage, so it joins any compaction
+        // requested meanwhile (the requesting warp holds a stage the producer may need
+        // before it can fill this one).  Decisions are warp-uniform.
+        const auto wait_data = [&](uint64_t* bar, uint32_t parity) -> bool {
+            if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+            const long long t0 = clock64();
+            while (true) {
+                if (__all_sync(0xFFFFFFFFu, mbar_try_wait_sleep(bar, parity, 2000u))) return true;
+                int f = 0, a = 0;
+                if (lane == 0) {
+                    f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                    a = *reinterpret_cast<volatile int*>(&ctrl->abort);
+                }
+                if (__shfl_sync(0xFFFFFFFFu, a, 0)) return false;
+                if (__shfl_sync(0xFFFFFFFFu, f, 0)) join_compaction();
+                if (clock64() - t0 > kSpinLimit) {
+                    if (lane == 0) {
+                        set_status(kErrTimeout);
+                        *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+                    }
+                    return false;
+                }
+            }
+        };
+
+        // ---- warm-up on chunk 0 (all consumer warps) ----
+        int64_t c00, ce0;
+        chunk_at(0, c00, ce0);
+        const uint32_t bytes0 = static_cast<uint32_t>(ce0 * ES) & ~15u;
+        const int nvec0 = static_cast<int>(bytes0 / 16);
+        const int tail0 = static_cast<int>(ce0 - bytes0 / ES);
+        const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
+        if (tid == 0 && got0) ctrl->observed[0] = 1;
+        {
+            // group maxima: thread t owns vectors t, t + NC, ... (VT of them) and splits
+            // their elements into R groups of consecutive vectors
+            const int R = wm / 256;
+            const int VT = (p.chunk * ES / 16 + NC - 1) / NC;
+            const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
+            for (int b = tid; b < kBins; b += NC) hist[b] = 0u;
+            const uint4* v0 = reinterpret_cast<const uint4*>(ring);
+            for (int r = 0; r < R; ++r) {
+                uint32_t gmax = 0u;
+                for (int j = r * vpg; j < (r + 1) * vpg && j < VT; ++j) {
+                    const int v = tid + j * NC;
+                    if (got0 && v < nvec0) {
+                        const uint4 x = v0[v];
+                        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            if (ES == 2) {
+                                gmax = max(gmax, max(key_bf16(w4[q] & 0xFFFFu), key_bf16(w4[q] >> 16)));
+                            } else {
+                                gmax = max(gmax, key_f32(w4[q]));
+                            }
+                        }
+                    }
+                }
+                wx[crank * wm + tid * R + r] = static_cast<KeyT>(gmax);
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1, NC);
+            if (G > 1) {
+                if (tid == 0) {
+                    const uint32_t bytes = static_cast<uint32_t>(wm) * ES;
+                    mbar_arrive_expect_tx(&ctrl->wbar, bytes * static_cast<uint32_t>(G - 1));
+                    for (int r = 0; r < G; ++r)
+                        if (r != static_cast<int>(crank))
+                            bulk_s2s_cluster(map_rank(wx + crank * wm, r), wx + crank * wm, bytes,
+                                             map_rank(&ctrl->wbar, r));
+                }
+                wait_bounded_cluster(&ctrl->wbar, 0, ctrl);
+            }
+            // histogram of the union's maxima by their top 11 key bits
+            for (int j = tid; j < G * wm; j += NC) {
+                const uint32_t kk = wx[j];
+                if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
+            }
+            named_bar_sync(1, NC);
+            int bstar;
+            uint32_t above, total;
+            find_pivot_bin<NC, 1>(hist, kBins, static_cast<uint32_t>(p.k), ctrl, tid, bstar, above, total);
+            uint32_t edge = 0u;  // smallest key of the pivot bucket
+            if (total >= static_cast<uint32_t>(p.k)) edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
+            if (edge > 0u) {
+                hasT = true;
+                T = edge - 1u;
+            }
+            if (tid == 0) ctrl->wedge = edge;
+        }
+        // chunk 0's survivors: warp w filters its slice of the vectors, the last warp the tail
+        {
+            const int slice = ((nvec0 + kNCW - 1) / kNCW + 31) & ~31;
+            const int v_lo = warp * slice < nvec0 ? warp * slice : nvec0;
+            const int v_hi = v_lo + slice < nvec0 ? v_lo + slice : nvec0;
+            int pass = 0;
+            if (got0)
+                warp_chunk<KeyT>(ring + static_cast<size_t>(v_lo) * 16, v_hi - v_lo,
+                                 static_cast<uint32_t>(c00) + static_cast<uint32_t>(v_lo * EPV), xrow,
+                                 c00 + bytes0 / ES, warp == kNCW - 1 ? tail0 : 0, compare_bits<KeyT>(hasT, T), ckey,
+                                 cidx, ctrl, cap, lane, pass, tmax);
+            named_bar_sync(1, NC);
+            if (tid == 0) {
+                mbar_arrive(&ctrl->empty[0]);
+                if (hasT && (G > 1 || MC)) publish_T(T);
+            }
+        }
+
+        // ---- every other chunk: one warp each ----
+        for (int q = 1 + warp; q < nq; q += kNCW) {
+            int req = 0;
+            if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+            if (__shfl_sync(0xFFFFFFFFu, req, 0)) join_compaction();
+            // the threshold: this CTA's, the cluster's and the other clusters'
+            uint32_t tk = T;
+            bool have = hasT;
+            {
+                uint32_t sh = gnext;
+                if (G > 1 && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
+                if (sh != 0u && (!have || sh > tk)) {
+                    tk = sh;
+                    have = true;
+                }
+                if (MC && lane == 0) {
+                    const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+                    gnext = static_cast<uint32_t>(g >> 32) == p.epoch ? static_cast<uint32_t>(g) : 0u;
+                }
+            }
+            int64_t c0, ce;
+            chunk_at(q, c0, ce);
+            const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+            const int s = q % p.stages, use = q / p.stages;
+            const bool got = wait_data(&ctrl->full[s], use & 1);
+            if (lane == 0 && got) ctrl->observed[s] = use + 1;
+            if (hasT && (!have || T > tk)) {  // a compaction ran while the warp waited
+                tk = T;
+                have = true;
+            }
+            if (got && ce > 0) {
+                const int nvec = static_cast<int>(bytes / 16);
+                const int tail = static_cast<int>(ce - bytes / ES);
+                int pass = 0;
+                while (!warp_chunk<KeyT>(ring + static_cast<size_t>(s) * chunk_bytes, nvec, static_cast<uint32_t>(c0),
+                                         xrow, c0 + bytes / ES, tail, compare_bits<KeyT>(have, tk), ckey, cidx, ctrl,
+                                         cap, lane, pass, tmax)) {
+                    join_compaction();
+                    if (!have || T > tk) {
+                        tk = T;
+                        have = true;
+                    }
+                    int ab = 0;
+                    if (lane == 0) ab = *reinterpret_cast<volatile int*>(&ctrl->abort);
+                    if (__shfl_sync(0xFFFFFFFFu, ab, 0)) break;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->empty[s]);
+        }
+        // A warp out of chunks still joins compactions other warps request: it reads the
+        // count of finished warps before the request flag, so a request raised by the
+        // last warp before it finished is always seen.
+        __threadfence_block();
+        if (lane == 0) atomicAdd(&ctrl->done_warps, 1);
+        {
+            const long long t0 = clock64();
+            while (true) {
+                int d = 0, f = 0;
+                if (lane == 0) {
+                    d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
+                    __threadfence_block();
+                    f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                }
+                d = __shfl_sync(0xFFFFFFFFu, d, 0);
+                f = __shfl_sync(0xFFFFFFFFu, f, 0);
+                if (f) {
+                    join_compaction();
+                    continue;
+                }
+                if (d >= kNCW) break;
+                if (clock64() - t0 > kSpinLimit) {  // cannot happen; keep the CTA alive
+                    set_status(kErrTimeout);
+                    break;
+                }
+            }
+        }
+        named_bar_sync(1, NC);
+        if (tid == 0) {
+            ctrl->fin_n = ctrl->cnt < p.cap ? ctrl->cnt : p.cap;
+            ctrl->fin_hasT = hasT ? 1 : 0;
+            ctrl->fin_T = T;
+        }
+    }
+    __syncthreads();
+    if (ctrl->abort && tid == 0) {
+        for (int s = 0; s < p.stages; ++s)
+            if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
+    }
+    __syncthreads();
+
+    // ------------------------------ final selection over the cluster ----------------
+    const int n = ctrl->fin_n;
+    uint32_t lo_own = ctrl->fin_hasT ? ctrl->fin_T : 0u;
+    if (G > 1) lo_own = max(lo_own, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+    if (MC) {
+        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_own = max(lo_own, static_cast<uint32_t>(g));
+    }
+    // Keys below lo_ge are out of play: at least k keys of the cluster's union are at or
+    // above every published threshold and above the warm-up bucket's edge.
+    const uint32_t edge = ctrl->wedge;  // the same in every CTA of the cluster
+    const uint32_t lo_ge = max(lo_own, edge);
+    const uint32_t kmax = KW == 16 ? 0xFFFFu : 0xFFFFFFFFu;
+    const auto in_play = [&](uint32_t kk) { return kk >= lo_ge; };
+    uint32_t lbase = edge, lhi = kmax;
+    int s = edge ? (ES == 2 ? 0 : 13) : (KW - kXBits);
+    uint32_t krem = static_cast<uint32_t>(p.k);
+    uint32_t pivot = 0u;
+    bool take_all = false;
+    uint16_t* xr = reinterpret_cast<uint16_t*>(smem + L.xf);  // two rounds of G histograms
+    for (int lvl = 0;; ++lvl) {
+        uint16_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * kXBins;
+        for (int b = tid; b < kXBins; b += NT) hist[b] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += NT) {
+            const uint32_t kk = ckey[i];
+            if (in_play(kk) && kk >= lbase && kk <= lhi) {
+                const uint32_t d = (kk - lbase) >> s;
+                atomicAdd(&hist[d < kXBins - 1 ? d : kXBins - 1], 1u);
+            }
+        }
+        __syncthreads();
+        for (int b = tid; b < kXBins; b += NT) mine[b] = static_cast<uint16_t>(hist[b]);
+        fence_proxy_async_smem();
+        __syncthreads();
+        uint64_t* xb = &ctrl->xbar[lvl & 1];
+        if (G > 1) {
+            if (tid == 0) {
+                const uint32_t bytes = kXBins * 2u;
+                mbar_arrive_expect_tx(xb, bytes * static_cast<uint32_t>(G - 1));
+                for (int r = 0; r < G; ++r)
+                    if (r != static_cast<int>(crank)) bulk_s2s_cluster(map_rank(mine, r), mine, bytes, map_rank(xb, r));
+            }
+            wait_bounded_cluster(xb, (lvl >> 1) & 1, ctrl);
+        }
+        const uint16_t* all = xr + static_cast<size_t>(lvl & 1) * G * kXBins;
+        for (int b = tid; b < kXBins; b += NT) {
+            uint32_t t = 0u;
+            for (int c = 0; c < G; ++c) t += all[c * kXBins + b];
+            hist[b] = t;
+        }
+        __syncthreads();
+        int bstar;
+        uint32_t above, total;
+        find_pivot_bin<NT, 0>(hist, kXBins, krem, ctrl, tid, bstar, above, total);
+        if (total < krem) {
+            take_all = true;
+            bstar = -1;
+        }
+        // every CTA's keys above the pivot bin (all of them when take_all)
+        for (int c = 0; c < G; ++c) {
+            uint32_t part_sum = 0u;
+            for (int b = bstar + 1 + tid; b < kXBins; b += NT) part_sum += all[c * kXBins + b];
+            part_sum = __reduce_add_sync(0xFFFFFFFFu, part_sum);
+            if (lane == 0 && part_sum) atomicAdd(&ctrl->sel_gt[c], part_sum);
+        }
+        if (take_all) break;
+        krem -= above;
+        const bool exact = s == 0 && bstar < kXBins - 1;
+        if (exact) {
+            pivot = lbase + static_cast<uint32_t>(bstar);
+            if (tid < G) ctrl->sel_eq[tid] = all[tid * kXBins + bstar];
+            break;
+        }
+        if (bstar < kXBins - 1) {
+            lbase += static_cast<uint32_t>(bstar) << s;
+            const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
+            lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
+            s = s > kXBits ? s - kXBits : 0;
+        } else {  // the open top bin: its keys all lie in [lbase + 1023 << s, lhi]
+            lbase += static_cast<uint32_t>(kXBins - 1) << s;
+            const int sb = bit_length(lhi - lbase) - kXBits;
+            s = sb > 0 ? sb : 0;
+        }
+        __syncthreads();
+    }
+    __syncthreads();
+    // this CTA's output slots: keys above the pivot after those of lower ranks, then the
+    // pivot-equal keys by rank until the quota k - (keys above) is used up
+    uint32_t gt_before = 0u, gt_all = 0u, eq_before = 0u;
+    for (int c = 0; c < G; ++c) {
+        const uint32_t g = ctrl->sel_gt[c];
+        gt_all += g;
+        if (c < static_cast<int>(crank)) {
+            gt_before += g;
+            eq_before += ctrl->sel_eq[c];
+        }
+    }
+    const uint32_t quota = take_all ? 0u : static_cast<uint32_t>(p.k) - gt_all;
+    const uint32_t my_eq = take_all ? 0u : ctrl->sel_eq[crank];
+    const uint32_t eq_take = quota > eq_before ? min(quota - eq_before, my_eq) : 0u;
+    const uint32_t eq_first = gt_all + min(eq_before, quota);
+    OutTarget out;
+    if (MC) {
+        out.vals = p.ws_key;
+        out.idx = p.ws_idx;
+        out.base = (row * p.C + cl) * static_cast<int64_t>(p.k);
+        out.to_keys = true;
+    } else {
+        out.vals = p.out_vals;
+        out.idx = p.out_idx;
+        out.base = row * static_cast<int64_t>(p.k);
+        out.to_keys = false;
+    }
+    const bool write_ok = !ctrl->abort;
+    const uint32_t ltm = lanemask_lt();
+    for (int i0 = 0; i0 < n; i0 += NT) {
+        const int i = i0 + tid;
+        uint32_t kk = 0u;
+        bool gt = false, eq = false;
+        if (i < n) {
+            kk = ckey[i];
+            const bool inr = in_play(kk);
+            gt = inr && (take_all || kk > pivot);
+            eq = inr && !take_all && kk == pivot;
+        }
+        const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt), me = __ballot_sync(0xFFFFFFFFu, eq);
+        uint32_t bg = 0u, be = 0u;
+        if (lane == 0) {
+            if (mg) bg = atomicAdd(&ctrl->cur_gt, static_cast<uint32_t>(__popc(mg)));
+            if (me) be = atomicAdd(&ctrl->cur_eq, static_cast<uint32_t>(__popc(me)));
+        }
+        bg = __shfl_sync(0xFFFFFFFFu, bg, 0);
+        be = __shfl_sync(0xFFFFFFFFu, be, 0);
+        int64_t slot = -1;
+        if (gt) slot = gt_before + bg + __popc(mg & ltm);
+        if (eq) {
+            const uint32_t t = be + __popc(me & ltm);
+            if (t < eq_take) slot = eq_first + t;
+        }
+        if (slot >= 0 && write_ok) {
+            if (slot < p.k) {
+                const int64_t o = out.base + slot;
+                if (out.to_keys) static_cast<uint32_t*>(out.vals)[o] = kk;
+                else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
+                else static_cast<uint32_t*>(out.vals)[o] = unkey_f32(kk);
+                out.idx[o] = static_cast<int32_t>(cidx[i]);
+            } else {
+                set_status(kErrInternal);
+            }
+        }
+    }
+    if (take_all && !MC && tid == 0) set_status(kErrInternal);  // a whole row held fewer than k keys in play
+    if (MC && crank == 0 && tid == 0)
+        p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(take_all ? gt_all : static_cast<uint32_t>(p.k));
+    if (G > 1) cluster_sync_all();  // no CTA leaves while another may still read its memory
+}
+
+}  // namespace dsk

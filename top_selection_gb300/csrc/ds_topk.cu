@@ -46,6 +46,7 @@ constexpr int kNCW = 8;                        // consumer warps per CTA
 constexpr int kScanThreads = (kNCW + 1) * 32;
 constexpr int kMergeThreads = kNCW * 32;
 constexpr int kChunkBytesMax = 16384;          // one bulk copy
+constexpr int kLiteralStages = 8;              // deepest ring of one-CTA rows
 constexpr int kMergeTile = 2048;               // entries per merge block
 constexpr int kPageMax = 64;                   // split rows: candidate slots a warp reserves at a time
 constexpr uint32_t kSentinelIdx = 0xFFFFFFFFu; // column of an unused slot (its key is 0)
@@ -106,6 +107,7 @@ struct ScanParams {
     long long* stats;
     int32_t parts, G, C;          // CTAs per row, CTAs per cluster, clusters per row
     int32_t chunk, stages, cap, perm_cap;
+    int32_t wm;                   // split rows: warm-up group maxima per CTA
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
     uint32_t* ws_key;             // per (row, cluster) partial results (C > 1)
@@ -1173,6 +1175,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     if (MC && crank == 0 && tid == 0) p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(kept);
 }
 
+}  // namespace dsk
+
+#include "ds_split.cuh"
+
+namespace dsk {
+
 // ---------------------------------------------------------------- merge kernel ----
 // Finishes rows split over C clusters: DeepSelect over the C partial results of the row
 // (each at most k (key, column) pairs), filtered against the row's shared threshold,
@@ -1302,7 +1310,7 @@ static bool dev_info(int dev, DevInfo& out) {
 }
 
 struct Plan {
-    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm;
+    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm;
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -1346,8 +1354,9 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         if (parts > P.m || (P.m + parts - 1) / parts > kPermMax) return DS_ERR_UNSUPPORTED;
     }
     P.parts = parts;
-    // split rows append through per-warp pages: room for one partly used page per warp
-    if (parts > 1) cap64 += static_cast<int64_t>(kNCW) * kPageMax;
+    // (split rows keep k entries plus one chunk's survivors: a warp reserves a chunk's
+    // slots at once and a reservation that does not fit triggers a compaction; their
+    // capacity is set with the chunk below)
     P.cap = static_cast<int>(cap64);
     P.perm_cap = static_cast<int>((P.m + parts - 1) / parts);
     int G = opt ? opt->cluster : 0;
@@ -1360,27 +1369,69 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.G = G;
     P.C = parts / G;
     if (opt && opt->stats && parts != 1) return DS_ERR_INVALID_ARG;
-    // Ring depth: the deepest ring (3..kMaxStages) that still lets two CTAs share an SM;
-    // otherwise the deepest ring that fits one CTA (at least 2 stages).
-    P.stages = 0;
-    for (int s = kMaxStages; s >= 3; --s) {
-        const size_t need = scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
-        if (2 * (need + 1024) <= static_cast<size_t>(di.smem_per_sm)) {
-            P.stages = s;
-            break;
-        }
-    }
-    if (P.stages == 0) {
-        for (int s = kMaxStages; s >= 2; --s) {
-            const size_t need = scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
-            if (need <= static_cast<size_t>(di.smem_optin)) {
+    P.wm = 0;
+    if (parts > 1) {
+        // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
+        // of the consumer warps (every stage is then used by one warp only, and a warp
+        // never waits on a stage whose previous fill belongs to another warp).  Take the
+        // largest chunk (halving from 16 KB, at least 1 KB) whose layout lets two CTAs
+        // share an SM, 16 stages before 8; else the largest that fits one CTA.
+        const auto warm_groups = [&](int chunk) {
+            // R group maxima per consumer thread (groups of whole vectors), enough for
+            // about 4k in the cluster's union when they fit the exchange
+            const int vt = (chunk * P.es / 16 + kNCW * 32 - 1) / (kNCW * 32);
+            int R = 1;
+            while (R * 2 <= vt && static_cast<int64_t>(G) * 256 * R * 2 * P.es <= kWarmMaxBytes &&
+                   static_cast<int64_t>(G) * 256 * R < 4 * static_cast<int64_t>(k))
+                R *= 2;
+            return 256 * R;
+        };
+        const auto fit = [&](int chunk, int stages, size_t limit) -> bool {
+            const int cap = static_cast<int>(align_up(static_cast<size_t>(k) + chunk, 16 / P.es));
+            const int wm = warm_groups(chunk);
+            const size_t need = split_layout(P.es, chunk, stages, cap, G, wm, k, P.perm_cap).total;
+            if (need > limit) return false;
+            P.chunk = chunk;
+            P.stages = stages;
+            P.cap = cap;
+            P.wm = wm;
+            P.smem = need;
+            return true;
+        };
+        const int unit = 16 / P.es;
+        const int first = B < kChunkBytesMax / P.es ? B : kChunkBytesMax / P.es;
+        const size_t two = static_cast<size_t>(di.smem_per_sm) / 2 - 1024;
+        bool ok = false;
+        for (int c = first; !ok && c * P.es >= 1024; c = (c / 2) / unit * unit)
+            ok = fit(c, 2 * kNCW, two) || fit(c, kNCW, two);
+        for (int c = first; !ok && c * P.es >= 1024; c = (c / 2) / unit * unit)
+            ok = fit(c, kNCW, static_cast<size_t>(di.smem_optin));
+        if (!ok && first * P.es < 1024) ok = fit(first, kNCW, static_cast<size_t>(di.smem_optin));
+        if (!ok) return DS_ERR_UNSUPPORTED;
+    } else {
+        const auto layout_bytes = [&](int s) -> size_t {
+            return scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
+        };
+        // Ring depth: the deepest ring (3..8) that still lets two CTAs share an SM;
+        // otherwise the deepest ring that fits one CTA (at least 2 stages).
+        P.stages = 0;
+        for (int s = kLiteralStages; s >= 3; --s) {
+            if (2 * (layout_bytes(s) + 1024) <= static_cast<size_t>(di.smem_per_sm)) {
                 P.stages = s;
                 break;
             }
         }
+        if (P.stages == 0) {
+            for (int s = kLiteralStages; s >= 2; --s) {
+                if (layout_bytes(s) <= static_cast<size_t>(di.smem_optin)) {
+                    P.stages = s;
+                    break;
+                }
+            }
+        }
+        if (P.stages == 0) return DS_ERR_UNSUPPORTED;
+        P.smem = layout_bytes(P.stages);
     }
-    if (P.stages == 0) return DS_ERR_UNSUPPORTED;
-    P.smem = scan_layout(P.es, P.chunk, P.stages, P.cap, G, P.perm_cap).total;
     P.ctas_per_sm = static_cast<int>(di.smem_per_sm / (P.smem + 1024));
     if (P.ctas_per_sm < 1) P.ctas_per_sm = 1;
     P.ws_bytes = 0;
@@ -1450,6 +1501,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.stages = P.stages;
     sp.cap = P.cap;
     sp.perm_cap = P.perm_cap;
+    sp.wm = P.wm;
     sp.epoch = 0;
     sp.gT = nullptr;
     sp.ws_key = nullptr;
@@ -1468,12 +1520,9 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     int slot = sizeof(KeyT) == 2 ? 0 : 1;
     if (P.parts == 1) {
         kern = ds_scan_kernel<KeyT, 0>;
-    } else if (P.G == 1) {
-        kern = ds_scan_kernel<KeyT, 1>;
-        slot += 2;
     } else {
-        kern = ds_scan_kernel<KeyT, 2>;
-        slot += 4;
+        kern = ds_split_kernel<KeyT>;
+        slot += 2;
     }
     if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
