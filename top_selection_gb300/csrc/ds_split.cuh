@@ -114,6 +114,74 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
     }
 }
 
+// bf16x2 / f32 maximum that ignores NaN operands (a NaN only when both are NaN).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Key of the largest non-NaN value of a packed word set reduced with max_bf16x2 (both
+// halves) or fmaxf, or 0 when only NaNs were seen.  Never above the largest key of the
+// values it came from (it is one of them, or a NaN mapped to 0).
+template <typename KeyT>
+__device__ __forceinline__ uint32_t max_word_key(uint32_t m) {
+    if (sizeof(KeyT) == 2) {
+        const uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+        const uint32_t klo = (lo & 0x7FFFu) > 0x7F80u ? 0u : key_bf16(lo);
+        const uint32_t khi = (hi & 0x7FFFu) > 0x7F80u ? 0u : key_bf16(hi);
+        return max(klo, khi);
+    } else {
+        return (m & 0x7FFFFFFFu) > 0x7F800000u ? 0u : key_f32(m);
+    }
+}
+
+// One warp finds the bin holding the k-th largest count of h[0, nbins) (nbins = 32 * per,
+// per a power of two <= 64): on return bstar is that bin (-1 when the bins hold fewer
+// than k in all), above the count in higher bins and total the count of all bins.  Lane
+// l owns bins [l * per, (l + 1) * per).
+__device__ __forceinline__ void warp_find_pivot(const uint32_t* h, int per, uint32_t k, int lane, int& bstar,
+                                                uint32_t& above, uint32_t& total) {
+    uint32_t sum = 0u;
+    for (int j = 0; j < per; ++j) sum += h[lane * per + j];
+    uint32_t suf = sum;  // bins of lanes >= lane
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, d);
+        if (lane + d < 32) suf += t;
+    }
+    total = __shfl_sync(0xFFFFFFFFu, suf, 0);
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, suf >= k);
+    if (hit == 0u) {
+        bstar = -1;
+        above = 0u;
+        return;
+    }
+    const int L = 31 - __clz(hit);
+    uint32_t acc = __shfl_sync(0xFFFFFFFFu, suf - sum, L);  // bins of lanes above L
+    // lane L's bins, 32 at a time from the top
+    for (int top = per; top > 0; top -= 32) {
+        const int j = top - 32 + lane;  // this lane's bin of the group (j < 0: none)
+        const uint32_t v = j >= 0 ? h[L * per + j] : 0u;
+        uint32_t s2 = v;  // bins j' >= j of the group
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, s2, d);
+            if (lane + d < 32) s2 += t;
+        }
+        const uint32_t h2 = __ballot_sync(0xFFFFFFFFu, j >= 0 && acc + s2 >= k);
+        if (h2) {
+            const int l2 = 31 - __clz(h2);
+            bstar = L * per + top - 32 + l2;
+            above = acc + __shfl_sync(0xFFFFFFFFu, s2 - v, l2);
+            return;
+        }
+        acc += __shfl_sync(0xFFFFFFFFu, s2, 0);
+    }
+    bstar = -1;  // not reached: lane L's bins hold the k-th
+    above = 0u;
+}
+
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
 // last tail_n elements from global memory) against the compare bits tb and appends the
 // survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
@@ -256,11 +324,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&ctrl->full[s], 1);
-            mbar_init(&ctrl->empty[s], 1);
-        }
+    if (tid < p.stages) {
+        mbar_init(&ctrl->full[tid], 1);
+        mbar_init(&ctrl->empty[tid], 1);
+        fence_mbar_init();
+    } else if (tid == 32) {
         mbar_init(&ctrl->wbar, 1);
         mbar_init(&ctrl->xbar[0], 1);
         mbar_init(&ctrl->xbar[1], 1);
@@ -268,7 +336,6 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         fence_mbar_init();
     }
     block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
-    if (G > 1) cluster_sync_all();  // every CTA's barriers are initialised before any remote use
 
     // chunk slot q: block perm[q / cpb], sub-chunk q % cpb (empty past the row's end)
     const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) {
@@ -282,26 +349,38 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
     };
 
+    // The producer fills the ring before the cluster-wide sync, so the first copies are
+    // in flight while the cluster's CTAs meet; the rest of the part follows as stages free.
+    const uint64_t pol = policy_evict_first();
+    const auto issue = [&](int q) {
+        int64_t c0, ce;
+        chunk_at(q, c0, ce);
+        const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+        const int s = q % p.stages, use = q / p.stages;
+        if (bytes) {
+            mbar_arrive_expect_tx(&ctrl->full[s], bytes);
+            bulk_g2s(ring + static_cast<size_t>(s) * chunk_bytes, xrow + c0 * ES, bytes, &ctrl->full[s], pol);
+        } else {
+            mbar_arrive(&ctrl->full[s]);
+        }
+        ctrl->issued[s] = use + 1;
+    };
+    // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
+    // and waits only before its CTA's first access to another CTA's memory, so the
+    // cluster's CTAs meet while the first copies are in flight.
+    if (G > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+
     if (warp == kNCW) {
         // ------------------------------ producer ------------------------------------
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
             for (int q = 0; q < nq; ++q) {
-                int64_t c0, ce;
-                chunk_at(q, c0, ce);
-                const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
                 const int s = q % p.stages, use = q / p.stages;
                 if (use > 0 && !wait_bounded(&ctrl->empty[s], (use - 1) & 1, ctrl)) break;
-                if (bytes) {
-                    mbar_arrive_expect_tx(&ctrl->full[s], bytes);
-                    bulk_g2s(ring + static_cast<size_t>(s) * chunk_bytes, xrow + c0 * ES, bytes, &ctrl->full[s], pol);
-                } else {
-                    mbar_arrive(&ctrl->full[s]);
-                }
-                ctrl->issued[s] = use + 1;
+                issue(q);
             }
         }
         __syncwarp();
+        if (G > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     } else {
         // ------------------------------ consumers -----------------------------------
         bool hasT = false;
@@ -357,39 +436,40 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         chunk_at(0, c00, ce0);
         const uint32_t bytes0 = static_cast<uint32_t>(ce0 * ES) & ~15u;
         const int nvec0 = static_cast<int>(bytes0 / 16);
-        const int tail0 = static_cast<int>(ce0 - bytes0 / ES);
         const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
         if (tid == 0 && got0) ctrl->observed[0] = 1;
         {
             // group maxima: thread t owns vectors t, t + NC, ... (VT of them) and splits
-            // their elements into R groups of consecutive vectors
+            // them into R groups of consecutive vectors; a group's maximum is taken on the
+            // packed values (NaNs ignored) and keyed once
             const int R = wm / 256;
             const int VT = (p.chunk * ES / 16 + NC - 1) / NC;
             const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
             for (int b = tid; b < kBins; b += NC) hist[b] = 0u;
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
             for (int r = 0; r < R; ++r) {
-                uint32_t gmax = 0u;
+                uint32_t m = ES == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf
+                bool any = false;
                 for (int j = r * vpg; j < (r + 1) * vpg && j < VT; ++j) {
                     const int v = tid + j * NC;
                     if (got0 && v < nvec0) {
                         const uint4 x = v0[v];
-                        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (ES == 2) {
-                                gmax = max(gmax, max(key_bf16(w4[q] & 0xFFFFu), key_bf16(w4[q] >> 16)));
-                            } else {
-                                gmax = max(gmax, key_f32(w4[q]));
-                            }
+                        if (ES == 2) {
+                            m = max_bf16x2(m, max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w)));
+                        } else {
+                            m = __float_as_uint(fmaxf(__uint_as_float(m),
+                                                      fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                                            fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)))));
                         }
+                        any = true;
                     }
                 }
-                wx[crank * wm + tid * R + r] = static_cast<KeyT>(gmax);
+                wx[crank * wm + tid * R + r] = static_cast<KeyT>(any ? max_word_key<KeyT>(m) : 0u);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, NC);
             if (G > 1) {
+                asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
                 if (tid == 0) {
                     const uint32_t bytes = static_cast<uint32_t>(wm) * ES;
                     mbar_arrive_expect_tx(&ctrl->wbar, bytes * static_cast<uint32_t>(G - 1));
@@ -400,43 +480,30 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
                 }
                 wait_bounded_cluster(&ctrl->wbar, 0, ctrl);
             }
-            // histogram of the union's maxima by their top 11 key bits
+            // histogram of the union's maxima by their top 11 key bits; one warp finds the
+            // bucket of the k-th largest
             for (int j = tid; j < G * wm; j += NC) {
                 const uint32_t kk = wx[j];
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
             }
             named_bar_sync(1, NC);
-            int bstar;
-            uint32_t above, total;
-            find_pivot_bin<NC, 1>(hist, kBins, static_cast<uint32_t>(p.k), ctrl, tid, bstar, above, total);
-            uint32_t edge = 0u;  // smallest key of the pivot bucket
-            if (total >= static_cast<uint32_t>(p.k)) edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
+            if (warp == 0) {
+                int bstar;
+                uint32_t above, total;
+                warp_find_pivot(hist, kBins / 32, static_cast<uint32_t>(p.k), lane, bstar, above, total);
+                if (lane == 0) ctrl->wedge = bstar > 0 ? static_cast<uint32_t>(bstar) << (KW - kDigitBits) : 0u;
+            }
+            named_bar_sync(1, NC);
+            const uint32_t edge = ctrl->wedge;  // smallest key of the pivot bucket (0: none)
             if (edge > 0u) {
                 hasT = true;
                 T = edge - 1u;
             }
-            if (tid == 0) ctrl->wedge = edge;
-        }
-        // chunk 0's survivors: warp w filters its slice of the vectors, the last warp the tail
-        {
-            const int slice = ((nvec0 + kNCW - 1) / kNCW + 31) & ~31;
-            const int v_lo = warp * slice < nvec0 ? warp * slice : nvec0;
-            const int v_hi = v_lo + slice < nvec0 ? v_lo + slice : nvec0;
-            int pass = 0;
-            if (got0)
-                warp_chunk<KeyT>(ring + static_cast<size_t>(v_lo) * 16, v_hi - v_lo,
-                                 static_cast<uint32_t>(c00) + static_cast<uint32_t>(v_lo * EPV), xrow,
-                                 c00 + bytes0 / ES, warp == kNCW - 1 ? tail0 : 0, compare_bits<KeyT>(hasT, T), ckey,
-                                 cidx, ctrl, cap, lane, pass, tmax);
-            named_bar_sync(1, NC);
-            if (tid == 0) {
-                mbar_arrive(&ctrl->empty[0]);
-                if (hasT && (G > 1 || MC)) publish_T(T);
-            }
+            if (tid == 0 && hasT && (G > 1 || MC)) publish_T(T);
         }
 
-        // ---- every other chunk: one warp each ----
-        for (int q = 1 + warp; q < nq; q += kNCW) {
+        // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
+        for (int q = warp; q < nq; q += kNCW) {
             int req = 0;
             if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
             if (__shfl_sync(0xFFFFFFFFu, req, 0)) join_compaction();
@@ -541,9 +608,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
     const uint32_t lo_ge = max(lo_own, edge);
     const uint32_t kmax = KW == 16 ? 0xFFFFu : 0xFFFFFFFFu;
     const auto in_play = [&](uint32_t kk) { return kk >= lo_ge; };
+    // pass state (identical in every CTA): keys in [lbase, lhi] binned by (key - lbase) >> s,
+    // the last bin open-ended
     uint32_t lbase = edge, lhi = kmax;
-    int s = edge ? (ES == 2 ? 0 : 13) : (KW - kXBits);
+    int s = edge ? (ES == 2 ? 0 : 23 - kXBits) : (KW - kXBits);
     uint32_t krem = static_cast<uint32_t>(p.k);
+    uint32_t gt_all = 0u, gt_lower = 0u;      // keys above the pivot: all CTAs, CTAs of lower rank
+    uint32_t eq_lower = 0u, eq_mine = 0u;     // pivot-equal keys: CTAs of lower rank, this CTA
     uint32_t pivot = 0u;
     bool take_all = false;
     uint16_t* xr = reinterpret_cast<uint16_t*>(smem + L.xf);  // two rounds of G histograms
@@ -572,61 +643,71 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
             }
             wait_bounded_cluster(xb, (lvl >> 1) & 1, ctrl);
         }
+        // the cluster's histogram, and the part of it held by CTAs of lower rank
         const uint16_t* all = xr + static_cast<size_t>(lvl & 1) * G * kXBins;
+        uint32_t* lower = hist + kXBins;
         for (int b = tid; b < kXBins; b += NT) {
-            uint32_t t = 0u;
-            for (int c = 0; c < G; ++c) t += all[c * kXBins + b];
+            uint32_t t = 0u, lt = 0u;
+            for (int c = 0; c < G; ++c) {
+                const uint32_t v = all[c * kXBins + b];
+                t += v;
+                lt += c < static_cast<int>(crank) ? v : 0u;
+            }
             hist[b] = t;
+            lower[b] = lt;
         }
+        if (tid == 0) ctrl->cur_gt = 0u;
         __syncthreads();
         int bstar;
         uint32_t above, total;
         find_pivot_bin<NT, 0>(hist, kXBins, krem, ctrl, tid, bstar, above, total);
-        if (total < krem) {
-            take_all = true;
-            bstar = -1;
-        }
-        // every CTA's keys above the pivot bin (all of them when take_all)
-        for (int c = 0; c < G; ++c) {
-            uint32_t part_sum = 0u;
-            for (int b = bstar + 1 + tid; b < kXBins; b += NT) part_sum += all[c * kXBins + b];
-            part_sum = __reduce_add_sync(0xFFFFFFFFu, part_sum);
-            if (lane == 0 && part_sum) atomicAdd(&ctrl->sel_gt[c], part_sum);
-        }
-        if (take_all) break;
-        krem -= above;
-        const bool exact = s == 0 && bstar < kXBins - 1;
-        if (exact) {
-            pivot = lbase + static_cast<uint32_t>(bstar);
-            if (tid < G) ctrl->sel_eq[tid] = all[tid * kXBins + bstar];
-            break;
-        }
-        if (bstar < kXBins - 1) {
-            lbase += static_cast<uint32_t>(bstar) << s;
-            const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
-            lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
-            s = s > kXBits ? s - kXBits : 0;
-        } else {  // the open top bin: its keys all lie in [lbase + 1023 << s, lhi]
-            lbase += static_cast<uint32_t>(kXBins - 1) << s;
-            const int sb = bit_length(lhi - lbase) - kXBits;
-            s = sb > 0 ? sb : 0;
+        if (total < krem) bstar = -1;  // fewer than krem keys in play: keep them all
+        // keys of lower-rank CTAs above the pivot bin
+        {
+            uint32_t part = 0u;
+            for (int b = bstar + 1 + tid; b < kXBins; b += NT) part += lower[b];
+            part = __reduce_add_sync(0xFFFFFFFFu, part);
+            if (lane == 0 && part) atomicAdd(&ctrl->cur_gt, part);
         }
         __syncthreads();
-    }
-    __syncthreads();
-    // this CTA's output slots: keys above the pivot after those of lower ranks, then the
-    // pivot-equal keys by rank until the quota k - (keys above) is used up
-    uint32_t gt_before = 0u, gt_all = 0u, eq_before = 0u;
-    for (int c = 0; c < G; ++c) {
-        const uint32_t g = ctrl->sel_gt[c];
-        gt_all += g;
-        if (c < static_cast<int>(crank)) {
-            gt_before += g;
-            eq_before += ctrl->sel_eq[c];
+        gt_lower += ctrl->cur_gt;
+        int done = 0;  // 1: exact pivot, 2: keep every key in play
+        if (bstar < 0) {
+            done = 2;
+            gt_all += total;
+        } else {
+            krem -= above;
+            gt_all += above;
+            if (s == 0 && bstar < kXBins - 1) {
+                done = 1;
+                pivot = lbase + static_cast<uint32_t>(bstar);
+                eq_lower = lower[bstar];
+                eq_mine = mine[bstar];
+            } else if (bstar < kXBins - 1) {
+                lbase += static_cast<uint32_t>(bstar) << s;
+                const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
+                lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
+                s = s > kXBits ? s - kXBits : 0;
+            } else {  // the open top bin: its keys all lie in [lbase + (kXBins - 1) << s, lhi]
+                lbase += static_cast<uint32_t>(kXBins - 1) << s;
+                const int sb = bit_length(lhi - lbase) - kXBits;
+                s = sb > 0 ? sb : 0;
+            }
+        }
+        __syncthreads();  // hist, lower and ctrl->cur_gt are read before the next pass
+        if (done) {
+            take_all = done == 2;
+            break;
         }
     }
+    // Every CTA has read and pushed all it will: the cluster barrier's arrival goes now and
+    // its wait at the very end, so no CTA leaves while another may still use its memory.
+    if (G > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    // this CTA's output slots: keys above the pivot after those of lower ranks, then the
+    // pivot-equal keys by rank until the quota k - (keys above) is used up
+    const uint32_t gt_before = gt_lower, eq_before = eq_lower;
     const uint32_t quota = take_all ? 0u : static_cast<uint32_t>(p.k) - gt_all;
-    const uint32_t my_eq = take_all ? 0u : ctrl->sel_eq[crank];
+    const uint32_t my_eq = take_all ? 0u : eq_mine;
     const uint32_t eq_take = quota > eq_before ? min(quota - eq_before, my_eq) : 0u;
     const uint32_t eq_first = gt_all + min(eq_before, quota);
     OutTarget out;
@@ -642,29 +723,29 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         out.to_keys = false;
     }
     const bool write_ok = !ctrl->abort;
-    const uint32_t ltm = lanemask_lt();
-    for (int i0 = 0; i0 < n; i0 += NT) {
-        const int i = i0 + tid;
-        uint32_t kk = 0u;
-        bool gt = false, eq = false;
-        if (i < n) {
-            kk = ckey[i];
-            const bool inr = in_play(kk);
-            gt = inr && (take_all || kk > pivot);
-            eq = inr && !take_all && kk == pivot;
+    // two passes over a contiguous range per thread: count, scan, write
+    const int per_t = (n + NT - 1) / NT;
+    const int i0 = tid * per_t < n ? tid * per_t : n;
+    const int i1 = i0 + per_t < n ? i0 + per_t : n;
+    uint32_t ng = 0u, ne = 0u;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = ckey[i];
+        if (in_play(kk)) {
+            ng += (take_all || kk > pivot) ? 1u : 0u;
+            ne += (!take_all && kk == pivot) ? 1u : 0u;
         }
-        const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt), me = __ballot_sync(0xFFFFFFFFu, eq);
-        uint32_t bg = 0u, be = 0u;
-        if (lane == 0) {
-            if (mg) bg = atomicAdd(&ctrl->cur_gt, static_cast<uint32_t>(__popc(mg)));
-            if (me) be = atomicAdd(&ctrl->cur_eq, static_cast<uint32_t>(__popc(me)));
-        }
-        bg = __shfl_sync(0xFFFFFFFFu, bg, 0);
-        be = __shfl_sync(0xFFFFFFFFu, be, 0);
+    }
+    uint32_t pg, pe, tg, te;
+    team_excl_scan2<NT, 0>(ng, ne, ctrl, 0, pg, pe, tg, te, tid);
+    uint32_t g = gt_before + pg, e = pe;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = ckey[i];
+        if (!in_play(kk)) continue;
         int64_t slot = -1;
-        if (gt) slot = gt_before + bg + __popc(mg & ltm);
-        if (eq) {
-            const uint32_t t = be + __popc(me & ltm);
+        if (take_all || kk > pivot) {
+            slot = g++;
+        } else if (kk == pivot) {
+            const uint32_t t = e++;
             if (t < eq_take) slot = eq_first + t;
         }
         if (slot >= 0 && write_ok) {
@@ -682,7 +763,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
     if (take_all && !MC && tid == 0) set_status(kErrInternal);  // a whole row held fewer than k keys in play
     if (MC && crank == 0 && tid == 0)
         p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(take_all ? gt_all : static_cast<uint32_t>(p.k));
-    if (G > 1) cluster_sync_all();  // no CTA leaves while another may still read its memory
+    if (G > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace dsk
