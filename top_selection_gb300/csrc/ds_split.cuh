@@ -38,6 +38,7 @@ namespace dsk {
 constexpr int kXBits = 9;               // final-select digit width
 constexpr int kXBins = 1 << kXBits;     // final-select bins per pass (exchanged as uint16)
 constexpr int kWarmMaxBytes = 16384;    // group maxima exchanged by the warm-up, all CTAs
+constexpr int kSplitThreads = kNCW * 32;  // consumer warps only: each issues its own copies
 
 struct SplitLayout {
     size_t ring, ckey, cidx, scratch, wx, xf, perm, ctrl, total;
@@ -134,52 +135,6 @@ __device__ __forceinline__ uint32_t max_word_key(uint32_t m) {
     } else {
         return (m & 0x7FFFFFFFu) > 0x7F800000u ? 0u : key_f32(m);
     }
-}
-
-// One warp finds the bin holding the k-th largest count of h[0, nbins) (nbins = 32 * per,
-// per a power of two <= 64): on return bstar is that bin (-1 when the bins hold fewer
-// than k in all), above the count in higher bins and total the count of all bins.  Lane
-// l owns bins [l * per, (l + 1) * per).
-__device__ __forceinline__ void warp_find_pivot(const uint32_t* h, int per, uint32_t k, int lane, int& bstar,
-                                                uint32_t& above, uint32_t& total) {
-    uint32_t sum = 0u;
-    for (int j = 0; j < per; ++j) sum += h[lane * per + j];
-    uint32_t suf = sum;  // bins of lanes >= lane
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, d);
-        if (lane + d < 32) suf += t;
-    }
-    total = __shfl_sync(0xFFFFFFFFu, suf, 0);
-    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, suf >= k);
-    if (hit == 0u) {
-        bstar = -1;
-        above = 0u;
-        return;
-    }
-    const int L = 31 - __clz(hit);
-    uint32_t acc = __shfl_sync(0xFFFFFFFFu, suf - sum, L);  // bins of lanes above L
-    // lane L's bins, 32 at a time from the top
-    for (int top = per; top > 0; top -= 32) {
-        const int j = top - 32 + lane;  // this lane's bin of the group (j < 0: none)
-        const uint32_t v = j >= 0 ? h[L * per + j] : 0u;
-        uint32_t s2 = v;  // bins j' >= j of the group
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, s2, d);
-            if (lane + d < 32) s2 += t;
-        }
-        const uint32_t h2 = __ballot_sync(0xFFFFFFFFu, j >= 0 && acc + s2 >= k);
-        if (h2) {
-            const int l2 = 31 - __clz(h2);
-            bstar = L * per + top - 32 + l2;
-            above = acc + __shfl_sync(0xFFFFFFFFu, s2 - v, l2);
-            return;
-        }
-        acc += __shfl_sync(0xFFFFFFFFu, s2, 0);
-    }
-    bstar = -1;  // not reached: lane L's bins hold the k-th
-    above = 0u;
 }
 
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
@@ -285,9 +240,9 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
 }
 
 template <typename KeyT>
-__global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanParams p) {
-    constexpr int NC = kNCW * 32;
-    constexpr int NT = kScanThreads;
+__global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanParams p) {
+    constexpr int NC = kSplitThreads;
+    constexpr int NT = kSplitThreads;
     constexpr int ES = sizeof(KeyT);
     constexpr int EPV = 16 / ES;
     constexpr int KW = 8 * ES;  // key width in bits
@@ -326,7 +281,6 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
     __syncthreads();
     if (tid < p.stages) {
         mbar_init(&ctrl->full[tid], 1);
-        mbar_init(&ctrl->empty[tid], 1);
         fence_mbar_init();
     } else if (tid == 32) {
         mbar_init(&ctrl->wbar, 1);
@@ -349,8 +303,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
     };
 
-    // The producer fills the ring before the cluster-wide sync, so the first copies are
-    // in flight while the cluster's CTAs meet; the rest of the part follows as stages free.
+    // Copies: stage s belongs to warp s % 8 (the ring depth is a multiple of 8), which
+    // consumes every chunk that lands there and refills the stage itself once it is done
+    // with it, so no warp ever waits on another warp's stage.
     const uint64_t pol = policy_evict_first();
     const auto issue = [&](int q) {
         int64_t c0, ce;
@@ -365,24 +320,14 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         }
         ctrl->issued[s] = use + 1;
     };
+    // chunk 0 feeds the warm-up: it goes first, the rest of the ring once it has landed
+    if (tid == 0) issue(0);
     // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
     // and waits only before its CTA's first access to another CTA's memory, so the
     // cluster's CTAs meet while the first copies are in flight.
-    if (G > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (G > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-    if (warp == kNCW) {
-        // ------------------------------ producer ------------------------------------
-        if (lane == 0) {
-            for (int q = 0; q < nq; ++q) {
-                const int s = q % p.stages, use = q / p.stages;
-                if (use > 0 && !wait_bounded(&ctrl->empty[s], (use - 1) & 1, ctrl)) break;
-                issue(q);
-            }
-        }
-        __syncwarp();
-        if (G > 1) asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-    } else {
-        // ------------------------------ consumers -----------------------------------
+    {
         bool hasT = false;
         uint32_t T = 0u;
         uint32_t tmax = 0u;
@@ -406,9 +351,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
             hasT = true;
             if (tid == 0) publish_T(T);
         };
-        // A warp waiting for its next chunk holds no stage, so it joins any compaction
-        // requested meanwhile (the requesting warp holds a stage the producer may need
-        // before it can fill this one).  Decisions are warp-uniform.
+        // A warp waiting for its next chunk joins any compaction requested meanwhile, so
+        // the requesting warp does not wait for this chunk to land.  Decisions are
+        // warp-uniform.
         const auto wait_data = [&](uint64_t* bar, uint32_t parity) -> bool {
             if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
             const long long t0 = clock64();
@@ -436,8 +381,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
         chunk_at(0, c00, ce0);
         const uint32_t bytes0 = static_cast<uint32_t>(ce0 * ES) & ~15u;
         const int nvec0 = static_cast<int>(bytes0 / 16);
+        for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while chunk 0 lands
         const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
         if (tid == 0 && got0) ctrl->observed[0] = 1;
+        if (lane == 0)
+            for (int q = warp == 0 ? kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
         {
             // group maxima: thread t owns vectors t, t + NC, ... (VT of them) and splits
             // them into R groups of consecutive vectors; a group's maximum is taken on the
@@ -445,7 +393,6 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
             const int R = wm / 256;
             const int VT = (p.chunk * ES / 16 + NC - 1) / NC;
             const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
-            for (int b = tid; b < kBins; b += NC) hist[b] = 0u;
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
             for (int r = 0; r < R; ++r) {
                 uint32_t m = ES == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf
@@ -480,21 +427,21 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
                 }
                 wait_bounded_cluster(&ctrl->wbar, 0, ctrl);
             }
-            // histogram of the union's maxima by their top 11 key bits; one warp finds the
-            // bucket of the k-th largest
+            // histogram of the union's maxima by their top 11 key bits, and the bucket of
+            // the k-th largest
             for (int j = tid; j < G * wm; j += NC) {
                 const uint32_t kk = wx[j];
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
             }
             named_bar_sync(1, NC);
-            if (warp == 0) {
-                int bstar;
-                uint32_t above, total;
-                warp_find_pivot(hist, kBins / 32, static_cast<uint32_t>(p.k), lane, bstar, above, total);
-                if (lane == 0) ctrl->wedge = bstar > 0 ? static_cast<uint32_t>(bstar) << (KW - kDigitBits) : 0u;
-            }
-            named_bar_sync(1, NC);
-            const uint32_t edge = ctrl->wedge;  // smallest key of the pivot bucket (0: none)
+            int bstar;
+            uint32_t above, total;
+            find_pivot_bin<NC, 1>(hist, kBins, static_cast<uint32_t>(p.k), ctrl, tid, bstar, above, total);
+            // smallest key of the pivot bucket (0: none)
+            const uint32_t edge = total >= static_cast<uint32_t>(p.k) && bstar > 0
+                                      ? static_cast<uint32_t>(bstar) << (KW - kDigitBits)
+                                      : 0u;
+            if (tid == 0) ctrl->wedge = edge;
             if (edge > 0u) {
                 hasT = true;
                 T = edge - 1u;
@@ -550,8 +497,9 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
                     if (__shfl_sync(0xFFFFFFFFu, ab, 0)) break;
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->empty[s]);
+            __syncwarp();  // every lane is done with the stage: refill it with this warp's next chunk there
+            if (lane == 0 && got && q + p.stages < nq && !*reinterpret_cast<volatile int*>(&ctrl->abort))
+                issue(q + p.stages);
         }
         // A warp out of chunks still joins compactions other warps request: it reads the
         // count of finished warps before the request flag, so a request raised by the
@@ -702,7 +650,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_split_kernel(const ScanPar
     }
     // Every CTA has read and pushed all it will: the cluster barrier's arrival goes now and
     // its wait at the very end, so no CTA leaves while another may still use its memory.
-    if (G > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    if (G > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // this CTA's output slots: keys above the pivot after those of lower ranks, then the
     // pivot-equal keys by rank until the quota k - (keys above) is used up
     const uint32_t gt_before = gt_lower, eq_before = eq_lower;

@@ -1527,7 +1527,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows * P.parts), 1, 1);
-    cfg.blockDim = dim3(kScanThreads, 1, 1);
+    cfg.blockDim = dim3(P.parts == 1 ? kScanThreads : kSplitThreads, 1, 1);
     cfg.dynamicSmemBytes = P.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1613,7 +1613,7 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
     if (st != DS_OK) return st;
     plan->parts = P.parts;
     plan->cluster = P.G;
-    plan->threads = kScanThreads;
+    plan->threads = P.parts == 1 ? kScanThreads : kSplitThreads;
     plan->chunk_elems = P.chunk;
     plan->stages = P.stages;
     plan->capacity = P.cap;
