@@ -137,6 +137,103 @@ __device__ __forceinline__ uint32_t max_word_key(uint32_t m) {
     }
 }
 
+// The bin of the k-th largest count among nbins = 8 warps x 32 x R bins, for a CTA of
+// 8 warps (R <= 16).  Warp w owns bins [w * 32R, (w + 1) * 32R) in rows of 32 (lane l
+// reads bin row * 32 + l, so the reads are conflict-free); per-warp totals meet in shared
+// memory after one barrier, and the warp whose range holds the k-th largest finds the bin
+// by suffix scans over its rows from the top.  cnt(b) gives a bin's count and low(b) a
+// second count summed over the bins above the pivot (low_above).  bstar = -1 when all
+// bins together hold fewer than k.  Ends with a CTA barrier; all threads get the results.
+template <int R, typename Cnt, typename Low>
+__device__ __forceinline__ void cta_pivot(uint32_t k, Cnt&& cnt, Low&& low, Ctrl* ctrl, int tid, int& bstar,
+                                          uint32_t& above, uint32_t& total, uint32_t& low_above) {
+    const int lane = tid & 31, warp = tid >> 5;
+    const int base = warp * 32 * R;
+    uint32_t v[R], lw[R];
+    uint32_t tw = 0u, lwt = 0u;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        v[r] = cnt(base + r * 32 + lane);
+        lw[r] = low(base + r * 32 + lane);
+        tw += v[r];
+        lwt += lw[r];
+    }
+    tw = __reduce_add_sync(0xFFFFFFFFu, tw);
+    lwt = __reduce_add_sync(0xFFFFFFFFu, lwt);
+    if (lane == 0) {
+        ctrl->warp_tot[0][warp] = tw;
+        ctrl->warp_tot[0][16 + warp] = lwt;
+    }
+    if (tid == 0) ctrl->bstar = -1;
+    __syncthreads();
+    uint32_t all = 0u, hi = 0u, lhi = 0u;  // all bins; bins and low counts of higher warps
+#pragma unroll
+    for (int w = 0; w < kNCW; ++w) {
+        const uint32_t t = ctrl->warp_tot[0][w];
+        all += t;
+        if (w > warp) {
+            hi += t;
+            lhi += ctrl->warp_tot[0][16 + w];
+        }
+    }
+    total = all;
+    if (hi < k && k <= hi + ctrl->warp_tot[0][warp]) {  // this warp's range holds the k-th largest
+        // the row: row totals (independent reductions), then a walk down from the top row
+        uint32_t rt[R], rl[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            rt[r] = __reduce_add_sync(0xFFFFFFFFu, v[r]);
+            rl[r] = __reduce_add_sync(0xFFFFFFFFu, lw[r]);
+        }
+        uint32_t acc = hi, lacc = lhi, x = 0u, lx = 0u;
+        int row = 0;
+        bool found = false;
+#pragma unroll
+        for (int r = R - 1; r >= 0; --r) {
+            if (!found && acc + rt[r] >= k) {
+                found = true;
+                row = r;
+                x = v[r];
+                lx = lw[r];
+            } else if (!found) {
+                acc += rt[r];
+                lacc += rl[r];
+            }
+        }
+        // the bin within the row: suffix sums over lanes >= lane
+        uint32_t s2 = x, l2 = lx;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, s2, d);
+            const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, l2, d);
+            if (lane + d < 32) {
+                s2 += t;
+                l2 += u;
+            }
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, acc + s2 >= k);
+        const int l = hit ? 31 - __clz(hit) : 0;
+        const uint32_t ab = __shfl_sync(0xFFFFFFFFu, s2 - x, l);
+        const uint32_t lb = __shfl_sync(0xFFFFFFFFu, l2 - lx, l);
+        if (lane == 0 && hit) {
+            ctrl->bstar = base + row * 32 + l;
+            ctrl->above = acc + ab;
+            ctrl->bcount = lacc + lb;
+        }
+    }
+    __syncthreads();
+    bstar = ctrl->bstar;
+    above = ctrl->above;
+    low_above = ctrl->bcount;
+    if (bstar < 0) {  // fewer than k in all: every bin counts as above
+        above = total;
+        low_above = 0u;
+#pragma unroll
+        for (int w = 0; w < kNCW; ++w) low_above += ctrl->warp_tot[0][16 + w];
+    }
+    __syncthreads();  // the shared results are read before the next search writes them
+}
+
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
 // last tail_n elements from global memory) against the compare bits tb and appends the
 // survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
@@ -289,6 +386,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         ctrl->fail_base = 0x7FFFFFFF;
         fence_mbar_init();
     }
+    {  // this CTA's slot of the final select's first exchange round
+        uint32_t* x0 = reinterpret_cast<uint32_t*>(smem + L.xf) + static_cast<size_t>(crank) * (kXBins / 2);
+        for (int i = tid; i < kXBins / 2; i += NT) x0[i] = 0u;
+    }
     block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
 
     // chunk slot q: block perm[q / cpb], sub-chunk q % cpb (empty past the row's end)
@@ -321,6 +422,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         ctrl->issued[s] = use + 1;
     };
     // chunk 0 feeds the warm-up: it goes first, the rest of the ring once it has landed
+    // (requested together, chunk 0 of some CTAs lands late and holds their clusters up)
     if (tid == 0) issue(0);
     // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
     // and waits only before its CTA's first access to another CTA's memory, so the
@@ -433,10 +535,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 const uint32_t kk = wx[j];
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
             }
-            named_bar_sync(1, NC);
+            __syncthreads();
             int bstar;
-            uint32_t above, total;
-            find_pivot_bin<NC, 1>(hist, kBins, static_cast<uint32_t>(p.k), ctrl, tid, bstar, above, total);
+            uint32_t above, total, unused;
+            cta_pivot<kBins / (kNCW * 32)>(
+                static_cast<uint32_t>(p.k), [&](int b) { return hist[b]; }, [](int) { return 0u; }, ctrl, tid, bstar,
+                above, total, unused);
             // smallest key of the pivot bucket (0: none)
             const uint32_t edge = total >= static_cast<uint32_t>(p.k) && bstar > 0
                                       ? static_cast<uint32_t>(bstar) << (KW - kDigitBits)
@@ -544,18 +648,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
 
     // ------------------------------ final selection over the cluster ----------------
     const int n = ctrl->fin_n;
-    uint32_t lo_own = ctrl->fin_hasT ? ctrl->fin_T : 0u;
-    if (G > 1) lo_own = max(lo_own, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
-    if (MC) {
-        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_own = max(lo_own, static_cast<uint32_t>(g));
-    }
-    // Keys below lo_ge are out of play: at least k keys of the cluster's union are at or
-    // above every published threshold and above the warm-up bucket's edge.
+    // Keys below the warm-up bucket's edge are out of play: at least k keys of the
+    // cluster's union lie at or above it.
     const uint32_t edge = ctrl->wedge;  // the same in every CTA of the cluster
-    const uint32_t lo_ge = max(lo_own, edge);
     const uint32_t kmax = KW == 16 ? 0xFFFFu : 0xFFFFFFFFu;
-    const auto in_play = [&](uint32_t kk) { return kk >= lo_ge; };
+    const auto in_play = [&](uint32_t kk) { return kk >= edge; };
     // pass state (identical in every CTA): keys in [lbase, lhi] binned by (key - lbase) >> s,
     // the last bin open-ended
     uint32_t lbase = edge, lhi = kmax;
@@ -565,87 +662,73 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     uint32_t eq_lower = 0u, eq_mine = 0u;     // pivot-equal keys: CTAs of lower rank, this CTA
     uint32_t pivot = 0u;
     bool take_all = false;
-    uint16_t* xr = reinterpret_cast<uint16_t*>(smem + L.xf);  // two rounds of G histograms
+    // two rounds of G histograms of kXBins uint16 counts, as pairs in 32-bit words; this
+    // CTA's slot of round 0 was cleared at start-up
+    constexpr int XW = kXBins / 2;
+    uint32_t* xr = reinterpret_cast<uint32_t*>(smem + L.xf);
     for (int lvl = 0;; ++lvl) {
-        uint16_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * kXBins;
-        for (int b = tid; b < kXBins; b += NT) hist[b] = 0u;
-        __syncthreads();
+        uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
         for (int i = tid; i < n; i += NT) {
             const uint32_t kk = ckey[i];
             if (in_play(kk) && kk >= lbase && kk <= lhi) {
-                const uint32_t d = (kk - lbase) >> s;
-                atomicAdd(&hist[d < kXBins - 1 ? d : kXBins - 1], 1u);
+                uint32_t d = (kk - lbase) >> s;
+                d = d < kXBins - 1 ? d : kXBins - 1;
+                atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
             }
         }
-        __syncthreads();
-        for (int b = tid; b < kXBins; b += NT) mine[b] = static_cast<uint16_t>(hist[b]);
         fence_proxy_async_smem();
         __syncthreads();
         uint64_t* xb = &ctrl->xbar[lvl & 1];
         if (G > 1) {
             if (tid == 0) {
-                const uint32_t bytes = kXBins * 2u;
+                const uint32_t bytes = XW * 4u;
                 mbar_arrive_expect_tx(xb, bytes * static_cast<uint32_t>(G - 1));
                 for (int r = 0; r < G; ++r)
                     if (r != static_cast<int>(crank)) bulk_s2s_cluster(map_rank(mine, r), mine, bytes, map_rank(xb, r));
             }
             wait_bounded_cluster(xb, (lvl >> 1) & 1, ctrl);
         }
+        // this CTA's slot of the other round is free again (what it held was pushed a round
+        // ago and every peer has used it since): clear it for the next pass
+        uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
+        for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
         // the cluster's histogram, and the part of it held by CTAs of lower rank
-        const uint16_t* all = xr + static_cast<size_t>(lvl & 1) * G * kXBins;
-        uint32_t* lower = hist + kXBins;
-        for (int b = tid; b < kXBins; b += NT) {
-            uint32_t t = 0u, lt = 0u;
-            for (int c = 0; c < G; ++c) {
-                const uint32_t v = all[c * kXBins + b];
-                t += v;
-                lt += c < static_cast<int>(crank) ? v : 0u;
-            }
-            hist[b] = t;
-            lower[b] = lt;
-        }
-        if (tid == 0) ctrl->cur_gt = 0u;
-        __syncthreads();
+        const uint16_t* all = reinterpret_cast<const uint16_t*>(xr + static_cast<size_t>(lvl & 1) * G * XW);
+        const auto cnt = [&](int b) {
+            uint32_t t = 0u;
+            for (int c = 0; c < G; ++c) t += all[c * kXBins + b];
+            return t;
+        };
+        const auto low = [&](int b) {
+            uint32_t t = 0u;
+            for (int c = 0; c < static_cast<int>(crank); ++c) t += all[c * kXBins + b];
+            return t;
+        };
         int bstar;
-        uint32_t above, total;
-        find_pivot_bin<NT, 0>(hist, kXBins, krem, ctrl, tid, bstar, above, total);
-        if (total < krem) bstar = -1;  // fewer than krem keys in play: keep them all
-        // keys of lower-rank CTAs above the pivot bin
-        {
-            uint32_t part = 0u;
-            for (int b = bstar + 1 + tid; b < kXBins; b += NT) part += lower[b];
-            part = __reduce_add_sync(0xFFFFFFFFu, part);
-            if (lane == 0 && part) atomicAdd(&ctrl->cur_gt, part);
-        }
-        __syncthreads();
-        gt_lower += ctrl->cur_gt;
-        int done = 0;  // 1: exact pivot, 2: keep every key in play
-        if (bstar < 0) {
-            done = 2;
-            gt_all += total;
-        } else {
-            krem -= above;
-            gt_all += above;
-            if (s == 0 && bstar < kXBins - 1) {
-                done = 1;
-                pivot = lbase + static_cast<uint32_t>(bstar);
-                eq_lower = lower[bstar];
-                eq_mine = mine[bstar];
-            } else if (bstar < kXBins - 1) {
-                lbase += static_cast<uint32_t>(bstar) << s;
-                const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
-                lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
-                s = s > kXBits ? s - kXBits : 0;
-            } else {  // the open top bin: its keys all lie in [lbase + (kXBins - 1) << s, lhi]
-                lbase += static_cast<uint32_t>(kXBins - 1) << s;
-                const int sb = bit_length(lhi - lbase) - kXBits;
-                s = sb > 0 ? sb : 0;
-            }
-        }
-        __syncthreads();  // hist, lower and ctrl->cur_gt are read before the next pass
-        if (done) {
-            take_all = done == 2;
+        uint32_t above, total, low_above;
+        cta_pivot<kXBins / (kNCW * 32)>(krem, cnt, low, ctrl, tid, bstar, above, total, low_above);
+        gt_lower += low_above;
+        gt_all += above;
+        if (bstar < 0) {  // fewer than krem keys in play: keep them all
+            take_all = true;
             break;
+        }
+        krem -= above;
+        if (s == 0 && bstar < kXBins - 1) {
+            pivot = lbase + static_cast<uint32_t>(bstar);
+            eq_lower = low(bstar);
+            eq_mine = all[crank * kXBins + bstar];
+            break;
+        }
+        if (bstar < kXBins - 1) {
+            lbase += static_cast<uint32_t>(bstar) << s;
+            const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
+            lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
+            s = s > kXBits ? s - kXBits : 0;
+        } else {  // the open top bin: its keys all lie in [lbase + (kXBins - 1) << s, lhi]
+            lbase += static_cast<uint32_t>(kXBins - 1) << s;
+            const int sb = bit_length(lhi - lbase) - kXBits;
+            s = sb > 0 ? sb : 0;
         }
     }
     // Every CTA has read and pushed all it will: the cluster barrier's arrival goes now and
@@ -653,11 +736,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     if (G > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // this CTA's output slots: keys above the pivot after those of lower ranks, then the
     // pivot-equal keys by rank until the quota k - (keys above) is used up
-    const uint32_t gt_before = gt_lower, eq_before = eq_lower;
     const uint32_t quota = take_all ? 0u : static_cast<uint32_t>(p.k) - gt_all;
-    const uint32_t my_eq = take_all ? 0u : eq_mine;
-    const uint32_t eq_take = quota > eq_before ? min(quota - eq_before, my_eq) : 0u;
-    const uint32_t eq_first = gt_all + min(eq_before, quota);
+    const uint32_t eq_take = take_all ? 0u : (quota > eq_lower ? min(quota - eq_lower, eq_mine) : 0u);
+    const uint32_t eq_first = gt_all + min(eq_lower, quota);
     OutTarget out;
     if (MC) {
         out.vals = p.ws_key;
@@ -671,21 +752,43 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         out.to_keys = false;
     }
     const bool write_ok = !ctrl->abort;
-    // two passes over a contiguous range per thread: count, scan, write
-    const int per_t = (n + NT - 1) / NT;
-    const int i0 = tid * per_t < n ? tid * per_t : n;
-    const int i1 = i0 + per_t < n ? i0 + per_t : n;
+    // Two passes over the candidates, each thread taking a contiguous run of them (runs in
+    // thread order): count the keys above / equal to the pivot, place the runs after each
+    // other (bit-plane prefix sums in the warp, one barrier across warps), then write.
+    const int m = (n + NT - 1) / NT;
+    const int i0 = tid * m < n ? tid * m : n;
+    const int i1 = i0 + m < n ? i0 + m : n;
     uint32_t ng = 0u, ne = 0u;
+#pragma unroll 4
     for (int i = i0; i < i1; ++i) {
         const uint32_t kk = ckey[i];
-        if (in_play(kk)) {
-            ng += (take_all || kk > pivot) ? 1u : 0u;
-            ne += (!take_all && kk == pivot) ? 1u : 0u;
-        }
+        const bool inr = in_play(kk);
+        ng += (inr && (take_all || kk > pivot)) ? 1u : 0u;
+        ne += (inr && !take_all && kk == pivot) ? 1u : 0u;
     }
-    uint32_t pg, pe, tg, te;
-    team_excl_scan2<NT, 0>(ng, ne, ctrl, 0, pg, pe, tg, te, tid);
-    uint32_t g = gt_before + pg, e = pe;
+    const uint32_t ltm = lanemask_lt();
+    uint32_t pg = 0u, pe = 0u, wg = 0u, we = 0u;  // exclusive prefixes in the warp, warp totals
+#pragma unroll
+    for (int bit = 0; bit < 16; ++bit) {  // runs hold fewer than 2^16 keys
+        const uint32_t bg = __ballot_sync(0xFFFFFFFFu, (ng >> bit) & 1u);
+        const uint32_t be = __ballot_sync(0xFFFFFFFFu, (ne >> bit) & 1u);
+        pg += static_cast<uint32_t>(__popc(bg & ltm)) << bit;
+        pe += static_cast<uint32_t>(__popc(be & ltm)) << bit;
+        wg += static_cast<uint32_t>(__popc(bg)) << bit;
+        we += static_cast<uint32_t>(__popc(be)) << bit;
+        if (__all_sync(0xFFFFFFFFu, (ng >> bit) <= 1u && (ne >> bit) <= 1u)) break;  // no higher bits
+    }
+    if (lane == 0) {
+        ctrl->warp_tot[1][warp] = wg;
+        ctrl->warp_tot[1][16 + warp] = we;
+    }
+    __syncthreads();
+    uint32_t g = gt_lower + pg, e = pe;
+    for (int w = 0; w < warp; ++w) {
+        g += ctrl->warp_tot[1][w];
+        e += ctrl->warp_tot[1][16 + w];
+    }
+#pragma unroll 4
     for (int i = i0; i < i1; ++i) {
         const uint32_t kk = ckey[i];
         if (!in_play(kk)) continue;
