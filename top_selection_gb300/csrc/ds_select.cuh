@@ -29,33 +29,25 @@ __device__ __forceinline__ void set_status(uint32_t bits) { atomicOr(&g_ds_statu
 
 // shared-memory control block
 struct Ctrl {
-    uint64_t full[kMaxStages];   // ring stage filled (one producer arrival + bytes)
-    uint64_t empty[kMaxStages];  // ring stage drained (one arrival per consumer warp)
-    int issued[kMaxStages];      // copies issued per stage (producer)
-    int observed[kMaxStages];    // copies seen complete per stage (consumers)
+    uint64_t full[kMaxStages];   // ring stage filled (one arrival + bytes)
+    uint64_t empty[kMaxStages];  // ring stage drained (one-CTA rows: one arrival per consumer warp)
+    int issued[kMaxStages];      // copies issued per stage
+    int observed[kMaxStages];    // copies seen complete per stage
     int cnt;                     // append cursor of the candidate buffer
     uint32_t maxkey;             // largest key appended (reduced from the threads at each select)
-    uint32_t sharedT;            // cluster-shared threshold key (each CTA's copy), 0 = none
-    uint32_t gmax;               // cluster-wide largest key (each CTA's copy)
+    uint32_t sharedT;            // split rows: the cluster's threshold key (each CTA's copy), 0 = none
     int abort;                   // a bounded wait ran out: skip the remaining waits
     int bstar;                   // pivot search results
     uint32_t above;
-    uint32_t bcount;             // keys in the pivot bin
-    uint32_t out_gt, out_eq;     // output cursors (rank 0 of the cluster)
-    uint32_t cta_gt, cta_eq;     // this CTA's reserved output ranges
+    uint32_t bcount;             // keys in the pivot bin (or a second count above it)
     uint32_t fp_tot[32];         // pivot-search scratch
     uint32_t warp_tot[2][32];    // team-scan scratch, two rows used alternately (2 x 16 words)
     uint32_t block_cnt[2][32];   // per-warp appends of the current block, by block parity
-    int compact_req;             // split rows: a warp saw the buffer reach k + B2
-    int done_warps;              // split rows: consumer warps that have filtered all their chunks
-    uint64_t csync[6];           // consumer-only cluster syncs of the warm-up (one arrival per CTA)
-    uint32_t ticket;             // warm-up tickets of pivot-equal keys (rank 0)
+    int compact_req;             // split rows: a reservation did not fit the buffer
+    int done_warps;              // split rows: warps that have filtered all their chunks
     int fail_base;               // split rows: first slot of a reservation that did not fit
     uint64_t wbar;               // split rows: warm-up exchange of group maxima
     uint64_t xbar[2];            // split rows: final-select histogram exchange, by pass parity
-    uint32_t sel_gt[16];         // split rows: keys above the final pivot, per CTA of the cluster
-    uint32_t sel_eq[16];         // split rows: keys equal to the final pivot, per CTA
-    uint32_t cur_gt, cur_eq;     // split rows: this CTA's output cursors
     uint32_t wedge;              // split rows: smallest key of the warm-up's pivot bucket
     int fin_n;                   // consumer state handed to the whole CTA after the scan
     int fin_hasT;
@@ -172,33 +164,6 @@ __device__ __forceinline__ uint32_t group_key(const uint4& g, int e, int es) {
     return (es == 2) ? ((e & 1) ? (w >> 16) : (w & 0xFFFFu)) : w;
 }
 
-// gsum[b] = sum over the cluster's CTAs of their hist[b], b < nbins.  Threads take groups
-// of four bins and issue every CTA's 16-byte remote load before adding, so the remote
-// round trips overlap instead of serialising.  hist and gsum must hold whole groups.
-template <int NTH>
-__device__ __forceinline__ void cluster_hist_sum(const uint32_t* hist, uint32_t* gsum, int nbins, int G, int tid) {
-    const int ng = (nbins + 3) / 4;
-    for (int g = tid; g < ng; g += NTH) {
-        uint4 acc = make_uint4(0u, 0u, 0u, 0u);
-        for (int r0 = 0; r0 < G; r0 += 4) {  // four CTAs' loads in flight at a time
-            uint4 v[4];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (r0 + r < G) v[r] = ld_cluster_v4(map_rank(hist + 4 * g, r0 + r));
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                if (r0 + r < G) {
-                    acc.x += v[r].x;
-                    acc.y += v[r].y;
-                    acc.z += v[r].z;
-                    acc.w += v[r].w;
-                }
-            }
-        }
-        reinterpret_cast<uint4*>(gsum)[g] = acc;
-    }
-}
-
 // Digit shift for the key range [lo, hi].
 __device__ __forceinline__ int range_shift(uint32_t lo, uint32_t hi) {
     const int s = bit_length(hi - lo) - kDigitBits;
@@ -285,31 +250,23 @@ __device__ __forceinline__ void build_hist(const KeyT* ckey, int n, uint32_t lo,
     }
 }
 
-// The key of rank krem (1 = largest) among the keys in [lo, hi] of the team's buffer
-// (and, with CL, of the buffers of every CTA of the cluster), by radix passes over
-// adaptive digits.  On return krem is the number of pivot-equal keys to keep.  take_all
-// is set when the range holds fewer than krem keys (then every key in range is kept).
-// hist must be zero on entry; it is left dirty.
-template <typename KeyT, int NTH, int BAR, bool CL>
+// The key of rank krem (1 = largest) among the keys in [lo, hi] of the team's buffer, by
+// radix passes over adaptive digits.  On return krem is the number of pivot-equal keys
+// to keep.  take_all is set when the range holds fewer than krem keys (then every key in
+// range is kept).  hist must be zero on entry; it is left dirty.
+template <typename KeyT, int NTH, int BAR>
 __device__ uint32_t radix_pivot(const KeyT* ckey, int n, uint32_t lo, uint32_t hi, uint32_t& krem, bool& take_all,
-                                uint32_t* hist, uint32_t* ghist, int G, Ctrl* ctrl, int tid, uint32_t* eq_count = nullptr,
+                                uint32_t* hist, Ctrl* ctrl, int tid, uint32_t* eq_count = nullptr,
                                 bool all_in_range = false) {
     take_all = false;
     for (int pass = 0;; ++pass) {
         const int s = range_shift(lo, hi);
         const int nbins = static_cast<int>((hi - lo) >> s) + 1;
         build_hist<KeyT, NTH>(ckey, n, lo, hi, s, hist, tid, pass == 0 && all_in_range);
-        const uint32_t* hsum = hist;
-        if (CL) {
-            cluster_sync_all();
-            cluster_hist_sum<NTH>(hist, ghist, nbins, G, tid);
-            hsum = ghist;
-        }
         team_sync<NTH, BAR>();
         int bstar;
         uint32_t above, total;
-        find_pivot_bin<NTH, BAR>(hsum, nbins, krem, ctrl, tid, bstar, above, total);
-        if (CL) cluster_sync_all();  // every CTA is done reading this pass's histograms
+        find_pivot_bin<NTH, BAR>(hist, nbins, krem, ctrl, tid, bstar, above, total);
         if (total < krem) {
             take_all = true;
             return lo;
@@ -382,8 +339,8 @@ __device__ __noinline__ uint32_t compact(KeyT* ckey, uint32_t* cidx, uint32_t* h
     uint32_t krem = static_cast<uint32_t>(k);
     bool take_all;
     uint32_t eqn = 0;
-    const uint32_t pivot = radix_pivot<KeyT, NTH, BAR, false>(ckey, n, lo, hi, krem, take_all, hist, hist, 1, ctrl,
-                                                              tid, &eqn, all_in_range);
+    const uint32_t pivot =
+        radix_pivot<KeyT, NTH, BAR>(ckey, n, lo, hi, krem, take_all, hist, ctrl, tid, &eqn, all_in_range);
     if (take_all) set_status(kErrInternal);  // n > k keys all lie in [lo, hi]
     const uint32_t quota = krem;
     constexpr int GK = 16 / sizeof(KeyT);
@@ -521,22 +478,18 @@ struct OutTarget {
     int esize;           // bytes per raw value
 };
 
-// Final RadixSelectTopK over the union of the candidates of the cluster's CTAs (CL) or of
-// this CTA alone.  All NT threads of every CTA call it.  lo0 bounds every key that may
-// belong to the answer from below; keys below it are ignored.  Writes min(k, kept) entries
-// and returns that count (identical in every CTA of the cluster).  Each CTA reserves its
-// output ranges with one atomic on rank 0's cursors.
-template <typename KeyT, int NT, bool CL>
-__device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_t* hist, uint32_t* ghist, Ctrl* ctrl,
-                                 int n, int k, uint32_t lo0, uint32_t hi0, int G, OutTarget out, bool write_ok,
-                                 int tid) {
+// Final RadixSelectTopK over this CTA's candidates.  All NT threads call it.  lo0 bounds
+// every key that may belong to the answer from below (keys below it are ignored) and hi0
+// every key from above.  Writes min(k, kept) entries and returns that count.
+template <typename KeyT, int NT>
+__device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int n, int k,
+                                 uint32_t lo0, uint32_t hi0, OutTarget out, bool write_ok, int tid) {
     for (int b = tid; b < kBins; b += NT) hist[b] = 0u;
     __syncthreads();
     uint32_t krem = static_cast<uint32_t>(k);
     bool take_all = true;
     uint32_t pivot = 0;
-    if (hi0 >= lo0)
-        pivot = radix_pivot<KeyT, NT, 0, CL>(ckey, n, lo0, hi0, krem, take_all, hist, ghist, G, ctrl, tid);
+    if (hi0 >= lo0) pivot = radix_pivot<KeyT, NT, 0>(ckey, n, lo0, hi0, krem, take_all, hist, ctrl, tid);
     const uint32_t quota = krem;
     uint32_t gc = 0, ec = 0;
     for (int i = tid; i < n; i += NT) {
@@ -547,21 +500,8 @@ __device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_
     }
     uint32_t tot;
     const uint32_t pre = team_excl_scan<NT, 0>(gc | (ec << 16), ctrl, 0, tot, tid);
-    if (tid == 0) {
-        const uint32_t GT = tot & 0xFFFFu, EQ = tot >> 16;
-        if (CL) {
-            ctrl->cta_gt = GT ? atom_cluster_add_u32(map_rank(&ctrl->out_gt, 0), GT) : 0u;
-            ctrl->cta_eq = EQ ? atom_cluster_add_u32(map_rank(&ctrl->out_eq, 0), EQ) : 0u;
-        } else {
-            ctrl->cta_gt = 0u;
-            ctrl->cta_eq = 0u;
-        }
-    }
-    __syncthreads();
-    uint32_t g = ctrl->cta_gt + (pre & 0xFFFFu);
-    uint32_t e = ctrl->cta_eq + (pre >> 16);
-    // kept entries: all keys in range when take_all (the cluster's total of them), else k
-    uint32_t kept = static_cast<uint32_t>(k);
+    uint32_t g = pre & 0xFFFFu;
+    uint32_t e = pre >> 16;
     for (int i = tid; i < n; i += NT) {
         const uint32_t kk = ckey[i];
         const bool inr = kk >= lo0 && kk <= hi0;
@@ -588,11 +528,8 @@ __device__ uint32_t final_select(const KeyT* ckey, const uint32_t* cidx, uint32_
             }
         }
     }
-    if (CL) cluster_sync_all();
-    else __syncthreads();
-    // (with CL only rank 0's count is meaningful: its cursor saw every CTA's reservation)
-    if (take_all) kept = CL ? ctrl->out_gt : (tot & 0xFFFFu);
-    return kept;
+    __syncthreads();
+    return take_all ? (tot & 0xFFFFu) : static_cast<uint32_t>(k);
 }
 
 }  // namespace dsk

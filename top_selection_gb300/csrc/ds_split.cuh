@@ -341,7 +341,6 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     constexpr int NC = kSplitThreads;
     constexpr int NT = kSplitThreads;
     constexpr int ES = sizeof(KeyT);
-    constexpr int EPV = 16 / ES;
     constexpr int KW = 8 * ES;  // key width in bits
     extern __shared__ __align__(1024) uint8_t smem[];
     const int G = p.G;

@@ -7,23 +7,18 @@
 // RadixSelectTopK.
 //
 // GB300 mapping
-//   * One CTA scans one part of a row (a contiguous range of blocks; a part is the whole
-//     row when the row is not split).  A producer warp streams the part's blocks, in
-//     the part's Philox order, into a ring of shared-memory stages with 1-D bulk copies
-//     (cp.async.bulk, completion on mbarriers); the input is read from HBM exactly once,
-//     with an L2 evict-first hint.
-//   * Consumer warps filter each staged chunk against T with integer compares on the raw
-//     bits (16-byte vector loads from shared memory, one warp vote per vector) and append
-//     survivors with a warp prefix sum and one shared atomic per warp.
-//   * After each block the consumers agree on |C| (per-warp counts, one named barrier)
-//     and, at >= k + B2, run RadixSelectTopK in shared memory (ds_select.cuh).
-//   * Split rows ("Implementation" section of the deep-dive: one sequence over several
-//     SMs, CTA results merged): the CTAs of a row form a thread-block cluster.  They
-//     share the best threshold through distributed shared memory, and the final
-//     selection runs over the union of their candidate buffers (cluster-wide histograms),
-//     each CTA writing its own survivors straight to the output.  Rows split over more
-//     than one cluster also share T through a global per-row word, write per-cluster
-//     results to a workspace, and a small merge kernel finishes the row.
+//   * Rows processed one CTA each (ds_scan_kernel, the algorithm as written): a producer
+//     warp streams the row's blocks, in the row's Philox order, into a ring of shared-
+//     memory stages with 1-D bulk copies (cp.async.bulk, completion on mbarriers; the
+//     input is read from HBM exactly once, with an L2 evict-first hint).  Consumer warps
+//     filter each staged chunk against T with integer compares on the raw bits and
+//     append survivors in warp order after one named barrier.  After each block, at
+//     >= k + B2 entries, RadixSelectTopK runs in shared memory (ds_select.cuh).
+//   * Rows split over several CTAs (ds_split_kernel in ds_split.cuh; the deep dive's
+//     "Implementation" section has the CTAs of a thread-block cluster share T through
+//     distributed shared memory and select over the union of their candidates).  Rows
+//     split over more than one cluster also share T through a global per-row word,
+//     write per-cluster results to a workspace, and ds_merge_kernel finishes the row.
 //   * No tensor cores: nothing on this path is a dense contraction.
 //
 // Every wait on an mbarrier is bounded (about one second of SM clock); on expiry the
@@ -48,16 +43,15 @@ constexpr int kMergeThreads = kNCW * 32;
 constexpr int kChunkBytesMax = 16384;          // one bulk copy
 constexpr int kLiteralStages = 8;              // deepest ring of one-CTA rows
 constexpr int kMergeTile = 2048;               // entries per merge block
-constexpr int kPageMax = 64;                   // split rows: candidate slots a warp reserves at a time
-constexpr uint32_t kSentinelIdx = 0xFFFFFFFFu; // column of an unused slot (its key is 0)
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Shared memory of the one-CTA-per-row kernel.
 struct ScanLayout {
-    size_t ring, ckey, cidx, hist, ghist, perm, ctrl, total;
+    size_t ring, ckey, cidx, hist, perm, ctrl, total;
 };
 
-__host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages, int cap, int G, int perm_cap) {
+__host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages, int cap, int perm_cap) {
     ScanLayout L;
     size_t off = 0;
     L.ring = off;
@@ -68,8 +62,6 @@ __host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages,
     off += align_up(static_cast<size_t>(cap) * 4, 16);
     L.hist = off;
     off += kScratchWords * 4;
-    L.ghist = off;
-    if (G > 1) off += kBins * 4;
     L.perm = off;
     off += align_up(static_cast<size_t>(perm_cap) * 4, 16);
     L.ctrl = off;
@@ -350,199 +342,6 @@ __device__ __forceinline__ uint32_t filter_chunk_sync(const uint4* src, int nvec
     return total;
 }
 
-// Split rows: the filter without a consumer barrier.  Each warp appends into its own
-// page of the candidate buffer (slots [pg_cur, pg_end), reserved with one shared atomic
-// per page), so warps never wait for each other between chunks.  A page that cannot take
-// the warp's survivors is filled first and the rest goes to a new page.  When a
-// reservation reaches `trigger` (k + B2) the warp raises ctrl->compact_req; every warp
-// checks it before its next chunk.  page is the reservation size (0: exact reservations).
-template <typename KeyT, int MODE>
-__device__ __forceinline__ void filter_chunk_paged(const uint4* src, int nvec, uint32_t col0, uint32_t thr,
-                                                   const char* xrow, int64_t tail_first, int tail_n, bool have,
-                                                   uint32_t tk, uint64_t* empty_bar, KeyT* ckey, uint32_t* cidx,
-                                                   Ctrl* ctrl, int cap, int tid, uint32_t& pg_cur, uint32_t& pg_end,
-                                                   uint32_t page, uint32_t trigger, uint32_t& tmax) {
-    constexpr int NC = kNCW * 32;
-    constexpr int ES = sizeof(KeyT);
-    constexpr int VEC = 16 / ES;
-    constexpr int V = 4;
-    const int lane = tid & 31, warp = tid >> 5;
-    uint4 v[V];
-    int nv = 0;
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        const int vi = tid + j * NC;
-        v[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (vi < nvec) {
-            v[j] = src[vi];
-            ++nv;
-        }
-    }
-    uint32_t tkey = 0u;
-    bool thit = false;
-    if (warp == 0 && lane < tail_n) {
-        tkey = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane])
-                       : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane]);
-        thit = !have || tkey > tk;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_bar);  // the stage is free: everything is in registers
-    bool any = true;
-    if (MODE != 0) {
-        uint32_t r[2 * V];
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-            const uint32_t e0 = v[j].x, e1 = v[j].y, e2 = v[j].z, e3 = v[j].w;
-            uint32_t a, b;
-            if (MODE == 1) {
-                a = static_cast<uint32_t>(max(static_cast<int32_t>(e0), static_cast<int32_t>(e1)));
-                b = static_cast<uint32_t>(max(static_cast<int32_t>(e2), static_cast<int32_t>(e3)));
-                if (ES == 2) {
-                    a = static_cast<uint32_t>(max(static_cast<int32_t>(a),
-                                                  max(static_cast<int32_t>(e0 << 16), static_cast<int32_t>(e1 << 16))));
-                    b = static_cast<uint32_t>(max(static_cast<int32_t>(b),
-                                                  max(static_cast<int32_t>(e2 << 16), static_cast<int32_t>(e3 << 16))));
-                }
-                if (j >= nv) a = b = 0x80000000u;
-            } else {
-                a = min(e0, e1);
-                b = min(e2, e3);
-                if (ES == 2) {
-                    a = min(a, min(e0 << 16, e1 << 16));
-                    b = min(b, min(e2 << 16, e3 << 16));
-                }
-                if (j >= nv) a = b = 0xFFFFFFFFu;
-            }
-            r[2 * j] = a;
-            r[2 * j + 1] = b;
-        }
-#pragma unroll
-        for (int w = 1; w < 2 * V; w *= 2) {
-#pragma unroll
-            for (int i = 0; i + w < 2 * V; i += 2 * w) {
-                r[i] = (MODE == 1) ? static_cast<uint32_t>(max(static_cast<int32_t>(r[i]), static_cast<int32_t>(r[i + w])))
-                                   : min(r[i], r[i + w]);
-            }
-        }
-        any = __any_sync(0xFFFFFFFFu, (pass_bits<MODE>(r[0], thr) != 0u) || thit);
-    }
-    if (!any) return;
-    uint32_t mask = 0u;
-#pragma unroll
-    for (int j = 0; j < V; ++j) {
-        if (j < nv) {
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            uint32_t bits;
-            if (MODE == 0) {
-                bits = (1u << VEC) - 1u;
-            } else {
-                uint32_t b0 = 0u, b1 = 0u;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (ES == 4) {
-                        b0 |= pass_bits<MODE>(w[q], thr) << q;
-                    } else {
-                        b0 |= pass_bits<MODE>(w[q] << 16, thr) << (2 * q);
-                        b1 |= pass_bits<MODE>(w[q], thr) << (2 * q + 1);
-                    }
-                }
-                bits = b0 | b1;
-            }
-            mask |= bits << (j * VEC);
-        }
-    }
-    const uint32_t c = __popc(mask) + (thit ? 1u : 0u);
-    uint32_t tot;
-    const uint32_t pre = warp_prefix_small(c, tot);
-    if (tot == 0u) return;
-    // slots: the rest of the current page, then a fresh page for what does not fit
-    const uint32_t rem = pg_end - pg_cur;
-    uint32_t fresh = 0u;
-    if (tot > rem) {
-        const uint32_t need = tot - rem;
-        const uint32_t size = need > page ? need : page;
-        uint32_t b = 0u;
-        if (lane == 0) {
-            b = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->cnt), size);
-            if (b + size >= trigger) *reinterpret_cast<volatile int*>(&ctrl->compact_req) = 1;
-        }
-        fresh = __shfl_sync(0xFFFFFFFFu, b, 0);
-        if (fresh + size > static_cast<uint32_t>(cap)) {
-            set_status(kErrOverflow);
-            return;
-        }
-        pg_end = fresh + size;
-    }
-    const uint32_t cur = pg_cur;
-    pg_cur = (tot > rem) ? fresh + (tot - rem) : cur + tot;
-    uint32_t q = pre;
-    while (mask) {
-        const int b = __ffs(mask) - 1;
-        mask &= mask - 1u;
-        const int j = b / VEC, e = b % VEC;
-        uint4 vv = v[0];
-        if (j == 1) vv = v[1];
-        if (j == 2) vv = v[2];
-        if (j == 3) vv = v[3];
-        const int qq = (e * ES) >> 2;
-        uint32_t w = vv.x;
-        if (qq == 1) w = vv.y;
-        if (qq == 2) w = vv.z;
-        if (qq == 3) w = vv.w;
-        const uint32_t key = (ES == 4) ? key_f32(w) : key_bf16((e & 1) ? (w >> 16) : (w & 0xFFFFu));
-        const uint32_t pos = q < rem ? cur + q : fresh + (q - rem);
-        ckey[pos] = static_cast<KeyT>(key);
-        cidx[pos] = col0 + static_cast<uint32_t>(tid + j * NC) * VEC + e;
-        ++q;
-        tmax = max(tmax, key);
-    }
-    if (thit) {
-        const uint32_t pos = q < rem ? cur + q : fresh + (q - rem);
-        ckey[pos] = static_cast<KeyT>(tkey);
-        cidx[pos] = static_cast<uint32_t>(tail_first + lane);
-        tmax = max(tmax, tkey);
-    }
-}
-
-// Marks the unused rest of the warp's page as empty (key 0, column kSentinelIdx): below
-// every threshold, so no selection counts it.
-template <typename KeyT>
-__device__ __forceinline__ void close_page(KeyT* ckey, uint32_t* cidx, uint32_t& pg_cur, uint32_t& pg_end, int lane) {
-    for (uint32_t pos = pg_cur + lane; pos < pg_end; pos += 32) {
-        ckey[pos] = static_cast<KeyT>(0u);
-        cidx[pos] = kSentinelIdx;
-    }
-    pg_cur = pg_end = 0u;
-}
-
-// Elements of the row's last < 16 bytes, read straight from global memory (one per lane).
-template <typename KeyT>
-__device__ __forceinline__ uint32_t filter_tail(const char* xrow, int64_t c_first, int count, bool have, uint32_t tk,
-                                                KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int cap, int lane,
-                                                uint32_t& tmax) {
-    constexpr int ES = sizeof(KeyT);
-    const bool valid = lane < count;
-    uint32_t key = 0u;
-    if (valid) {
-        if (ES == 2) key = key_bf16(reinterpret_cast<const uint16_t*>(xrow)[c_first + lane]);
-        else key = key_f32(reinterpret_cast<const uint32_t*>(xrow)[c_first + lane]);
-    }
-    const bool hit = valid && (!have || key > tk);
-    const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
-    if (!hmask) return 0u;
-    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
-    if (hit) {
-        if (pos < static_cast<uint32_t>(cap)) {
-            ckey[pos] = static_cast<KeyT>(key);
-            cidx[pos] = static_cast<uint32_t>(c_first + lane);
-        } else {
-            set_status(kErrOverflow);
-        }
-        tmax = max(tmax, key);
-    }
-    return __popc(hmask);
-}
-
 __device__ __forceinline__ void threshold_mode(int es, bool have, uint32_t tk, int& mode, uint32_t& thr) {
     if (!have) {
         mode = 0;
@@ -616,286 +415,42 @@ __global__ void ds_wait_probe_kernel(long long limit) {
     }
 }
 
-// ---------------------------------------------------------------- warm-up ---------
-// Split rows start from the union of the first chunks of the cluster's CTAs: the k
-// largest keys of that union are selected directly from the staged chunks (histograms
-// summed over distributed shared memory), only they are appended, and their smallest key
-// becomes every CTA's threshold T.  This is DeepSelect's first compaction taken over a
-// window that spans the cluster (the pages' implementations likewise raise T from an
-// initial window before the steady scan): the cluster then holds exactly k keys >= T,
-// which is all the later filter and final selection rely on.
-
-// Sync among the consumer warps of every CTA of the cluster (the producer warp keeps
-// streaming): local named barrier, one remote arrival per CTA on every CTA's barrier
-// `idx`, then a bounded cluster-scope wait on the local one.
-__device__ __forceinline__ void consumer_cluster_sync(Ctrl* ctrl, int idx, int G, int tid) {
-    named_bar_sync(1, kNCW * 32);
-    if (G <= 1) return;
-    if (tid == 0) {
-        fence_acq_rel_cluster();
-        for (int r = 0; r < G; ++r) mbar_arrive_remote(map_rank(&ctrl->csync[idx], r));
-    }
-    if (mbar_try_wait_cluster(&ctrl->csync[idx], 0, 20000u)) return;
-    const long long t0 = clock64();
-    while (!mbar_try_wait_cluster(&ctrl->csync[idx], 0, 20000u)) {
-        if (*reinterpret_cast<volatile int*>(&ctrl->abort)) return;
-        if (clock64() - t0 > kSpinLimit) {
-            set_status(kErrTimeout);
-            *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
-            return;
-        }
-    }
-}
-
-// Keys of one staged chunk held by thread `tid`: vectors tid, tid + NC, ... plus, for
-// warp 0, up to 15 tail bytes read from global memory (one element per lane).
-template <typename KeyT, typename F>
-__device__ __forceinline__ void for_chunk_keys(const uint4* src, int nvec, const char* xrow, int64_t tail_first,
-                                               int tail_n, int tid, F&& f) {
-    constexpr int NC = kNCW * 32;
-    constexpr int ES = sizeof(KeyT);
-    constexpr int VEC = 16 / ES;
-    for (int vi = tid; vi < nvec; vi += NC) {
-        const uint4 v = src[vi];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (ES == 2) {
-                f(vi * VEC + 2 * q, key_bf16(w[q] & 0xFFFFu));
-                f(vi * VEC + 2 * q + 1, key_bf16(w[q] >> 16));
-            } else {
-                f(vi * VEC + q, key_f32(w[q]));
-            }
-        }
-    }
-    if (tid < tail_n) {
-        const uint32_t key = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + tid])
-                                     : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + tid]);
-        f(nvec * VEC + tid, key);
-    }
-}
-
-// Warp append of one key per lane (hit lanes only); returns the warp's count.
-template <typename KeyT>
-__device__ __forceinline__ uint32_t append_one(bool hit, uint32_t key, uint32_t col, KeyT* ckey, uint32_t* cidx,
-                                               Ctrl* ctrl, int cap, int lane, uint32_t& tmax) {
-    const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
-    if (!hmask) return 0u;
-    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
-    if (hit) {
-        if (pos < static_cast<uint32_t>(cap)) {
-            ckey[pos] = static_cast<KeyT>(key);
-            cidx[pos] = col;
-        } else {
-            set_status(kErrOverflow);
-        }
-        tmax = max(tmax, key);
-    }
-    return __popc(hmask);
-}
-
-// The warm-up selection over the first chunk of every CTA of the cluster.  Consumers
-// only.  On return hasT/T hold the new threshold (unchanged when the union holds fewer
-// than k keys, in which case every key was appended) and wcnt counts this warp's appends.
-template <typename KeyT>
-__device__ void warmup_select(const uint4* src, int nvec, const char* xrow, int64_t tail_first, int tail_n,
-                              uint32_t col0, int k, int G, uint32_t* hA, uint32_t* hB, uint32_t* gsum, KeyT* ckey,
-                              uint32_t* cidx, Ctrl* ctrl, int cap, int tid, bool& hasT, uint32_t& T, uint32_t& tmax,
-                              uint32_t& wcnt) {
-    constexpr int NC = kNCW * 32;
-    constexpr int ES = sizeof(KeyT);
-    constexpr int VEC = 16 / ES;
-    const int lane = tid & 31;
-    uint32_t lo = 0u, hi = ES == 2 ? 0xFFFFu : 0xFFFFFFFFu;
-    uint32_t krem = static_cast<uint32_t>(k);
-    bool take_all = false;
-    uint32_t pivot = 0u;
-    int level = 0;
-    for (;; ++level) {
-        const int s = range_shift(lo, hi);
-        const int nbins = static_cast<int>((hi - lo) >> s) + 1;
-        uint32_t* h = (level & 1) ? hB : hA;
-        for (int b = tid; b < ((nbins + 3) & ~3); b += NC) h[b] = 0u;
-        named_bar_sync(1, NC);
-        for_chunk_keys<KeyT>(src, nvec, xrow, tail_first, tail_n, tid, [&](int, uint32_t kk) {
-            if (kk - lo <= hi - lo) atomicAdd(&h[(kk - lo) >> s], 1u);
-        });
-        consumer_cluster_sync(ctrl, level, G, tid);
-        const uint32_t* hs = h;
-        if (G > 1) {
-            cluster_hist_sum<NC>(h, gsum, nbins, G, tid);
-            named_bar_sync(1, NC);
-            hs = gsum;
-        }
-        int bstar;
-        uint32_t above, total;
-        find_pivot_bin<NC, 1>(hs, nbins, krem, ctrl, tid, bstar, above, total);
-        if (total < krem) {  // the union holds fewer than k keys: keep them all
-            take_all = true;
-            break;
-        }
-        krem -= above;
-        lo += static_cast<uint32_t>(bstar) << s;
-        if (s == 0) {
-            pivot = lo;
-            break;
-        }
-        const uint32_t top = lo + ((1u << s) - 1u);
-        hi = top < hi ? top : hi;
-    }
-    const uint32_t quota = krem;
-    const uint32_t a_ticket = G > 1 ? map_rank(&ctrl->ticket, 0) : 0u;
-    // filter the chunk against the pivot; pivot-equal keys draw cluster-wide tickets
-    for (int vi0 = tid - lane; vi0 < nvec; vi0 += NC) {  // warp-uniform rounds, one vector per lane
-        const int vi = vi0 + lane;
-        uint32_t keys[VEC];
-        uint32_t valid = 0u;
-        if (vi < nvec) {
-            const uint4 v = src[vi];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (ES == 2) {
-                    keys[2 * q] = key_bf16(w[q] & 0xFFFFu);
-                    keys[2 * q + 1] = key_bf16(w[q] >> 16);
-                } else {
-                    keys[q] = key_f32(w[q]);
-                }
-            }
-            valid = (1u << VEC) - 1u;
-        } else {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) keys[e] = 0u;
-        }
-        uint32_t gt = 0u, eq = 0u;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-            gt |= ((take_all || keys[e] > pivot) ? 1u : 0u) << e;
-            eq |= ((!take_all && keys[e] == pivot) ? 1u : 0u) << e;
-        }
-        gt &= valid;
-        eq &= valid;
-        if (__any_sync(0xFFFFFFFFu, eq != 0u)) {
-            const uint32_t c = __popc(eq);
-            const uint32_t incl = warp_incl_scan(c, lane);
-            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t base = 0u;
-            if (lane == 0) base = G > 1 ? atom_cluster_add_u32(a_ticket, tot) : atomicAdd(&ctrl->ticket, tot);
-            base = __shfl_sync(0xFFFFFFFFu, base, 0) + incl - c;
-            uint32_t m = eq;
-            while (m) {
-                const int b = __ffs(m) - 1;
-                m &= m - 1u;
-                if (base++ < quota) gt |= 1u << b;
-            }
-        }
-        // append this lane's kept keys
-        const uint32_t c = __popc(gt);
-        if (__any_sync(0xFFFFFFFFu, c != 0u)) {
-            const uint32_t incl = warp_incl_scan(c, lane);
-            const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            uint32_t pos = warp_reserve(ctrl, tot, lane) + incl - c;
-            uint32_t m = gt;
-            while (m) {
-                const int b = __ffs(m) - 1;
-                m &= m - 1u;
-                uint32_t key = keys[0];
-#pragma unroll
-                for (int e = 1; e < VEC; ++e)
-                    if (b == e) key = keys[e];
-                if (pos < static_cast<uint32_t>(cap)) {
-                    ckey[pos] = static_cast<KeyT>(key);
-                    cidx[pos] = col0 + static_cast<uint32_t>(vi) * VEC + b;
-                } else {
-                    set_status(kErrOverflow);
-                }
-                ++pos;
-                tmax = max(tmax, key);
-            }
-            wcnt += tot;
-        }
-    }
-    // tail elements (row end, < 16 bytes): warp 0
-    if (tail_n > 0 && tid < 32) {
-        const bool valid = lane < tail_n;
-        uint32_t key = 0u;
-        if (valid)
-            key = ES == 2 ? key_bf16(reinterpret_cast<const uint16_t*>(xrow)[tail_first + lane])
-                          : key_f32(reinterpret_cast<const uint32_t*>(xrow)[tail_first + lane]);
-        bool keep = valid && (take_all || key > pivot);
-        const bool eqk = valid && !take_all && key == pivot;
-        const uint32_t em = __ballot_sync(0xFFFFFFFFu, eqk);
-        if (em) {
-            uint32_t base = 0u;
-            if (lane == 0) base = G > 1 ? atom_cluster_add_u32(a_ticket, __popc(em)) : atomicAdd(&ctrl->ticket, __popc(em));
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            if (eqk && base + __popc(em & lanemask_lt()) < quota) keep = true;
-        }
-        wcnt += append_one<KeyT>(keep, key, static_cast<uint32_t>(tail_first + lane), ckey, cidx, ctrl, cap, lane,
-                                 tmax);
-    }
-    if (!take_all) {
-        hasT = true;
-        T = pivot;
-    }
-    consumer_cluster_sync(ctrl, level + 1, G, tid);  // every remote read of this CTA is done
-}
-
 // ---------------------------------------------------------------- scan kernel -----
-template <typename KeyT, int KIND>
+// One CTA per row, the deep dive's algorithm as written: a producer warp streams the
+// row's blocks in Philox order through the copy ring; after each block the consumers
+// compact the candidate buffer with RadixSelectTopK once it holds k + B2 entries or more
+// (T becomes the k-th key), and a final RadixSelectTopK writes the k results.
+template <typename KeyT>
 __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanParams p) {
-    // KIND 0: one CTA per row; 1: rows split over CTAs without a cluster; 2: rows split
-    // over the CTAs of clusters (p.G > 1).  Each kind is its own instantiation, so a kernel
-    // carries only the code of its own path.
-    constexpr bool SPLIT = KIND != 0;
-    constexpr bool CL = KIND == 2;
-    const bool MC = SPLIT && p.C > 1;  // rows split over several clusters
     constexpr int NC = kNCW * 32;
     constexpr int NT = kScanThreads;
     constexpr int ES = sizeof(KeyT);
     extern __shared__ __align__(1024) uint8_t smem[];
-    const ScanLayout L = scan_layout(ES, p.chunk, p.stages, p.cap, p.G, p.perm_cap);
+    const ScanLayout L = scan_layout(ES, p.chunk, p.stages, p.cap, p.perm_cap);
     uint8_t* ring = smem + L.ring;
     KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
     uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
     uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
-    uint32_t* ghist = CL ? reinterpret_cast<uint32_t*>(smem + L.ghist) : hist;
     int32_t* perm = reinterpret_cast<int32_t*>(smem + L.perm);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t cta = blockIdx.x;
-    const int64_t row = cta / p.parts;
-    const int part = static_cast<int>(cta % p.parts);
-    const int cl = part / p.G;
-    const uint32_t crank = CL ? cluster_ctarank() : 0u;
-    const int64_t b0 = static_cast<int64_t>(part) * p.m / p.parts;
-    const int64_t b1 = static_cast<int64_t>(part + 1) * p.m / p.parts;
-    const int mp = static_cast<int>(b1 - b0);
+    const int64_t row = blockIdx.x;
+    const int mp = static_cast<int>(p.m);
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
-    const bool shared_T = CL || MC;
 
     {
         int* z = reinterpret_cast<int*>(ctrl);
         for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&ctrl->full[s], 1);
-            mbar_init(&ctrl->empty[s], kNCW);
-        }
-        for (int c = 0; c < 6; ++c) mbar_init(&ctrl->csync[c], p.G);
+    if (tid < p.stages) {
+        mbar_init(&ctrl->full[tid], 1);
+        mbar_init(&ctrl->empty[tid], kNCW);
         fence_mbar_init();
     }
-    block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
-    if (CL) cluster_sync_all();  // every CTA's control block is initialised
-    // The cluster's shared threshold lives in every CTA's own ctrl->sharedT: a CTA that
-    // raises it writes a max into all G copies, and readers load their local copy.
-    const auto publish_T = [&](uint32_t t) {
-        for (int r = 0; r < p.G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
-    };
+    block_order<NT>(p.seed, row, 0, mp, hist, perm, tid);
 
     if (warp == kNCW) {
         // ------------------------------ producer: bulk copies in block order ------
@@ -933,128 +488,41 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         int n = 0;
         bool hasT = false;
         uint32_t T = 0u;
-        uint32_t badd = 0u;     // appends of the current block
+        uint32_t badd = 0u;  // appends of the current block
         uint32_t tmax = 0u;
-        uint32_t sh_next = 0u;  // other clusters' threshold, loaded during the previous block
         long long sA = 0, sR = 0, sW = 0, sMax = 0;
-        // split rows: per-warp pages of the candidate buffer, compaction on request
-        uint32_t pg_cur = 0u, pg_end = 0u;
-        const uint32_t trigger = static_cast<uint32_t>(p.k + p.B2);
-        uint32_t page_size = static_cast<uint32_t>(p.B2) / (2u * kNCW);
-        if (page_size > static_cast<uint32_t>(kPageMax)) page_size = kPageMax;
-        // every consumer warp arrives here, in the loop or after its last chunk
-        const auto split_compact = [&]() {
-            close_page<KeyT>(ckey, cidx, pg_cur, pg_end, lane);
-            named_bar_sync(2, NC);
-            n = ctrl->cnt;
-            if (tid == 0) ctrl->compact_req = 0;
-            T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, hasT ? T : 0u, tmax, tid, false);
-            hasT = true;
-            n = p.k;
-            if (tid == 0 && shared_T) {
-                if (CL) publish_T(T);
-                if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
-            }
-        };
         for (int i = 0; i < mp; ++i) {
             const int64_t lo = static_cast<int64_t>(perm[i]) * p.B;
             const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
-            bool have = hasT;
-            uint32_t tk = T;
-            if (shared_T) {
-                uint32_t sh = sh_next;
-                if (CL && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
-                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
-                if (sh != 0u && (!have || sh > tk)) {
-                    tk = sh;
-                    have = true;
-                }
-                // the global load for the next block is issued now; it completes while this one runs
-                if (MC && lane == 0) {
-                    const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-                    sh_next = static_cast<uint32_t>(g >> 32) == p.epoch ? static_cast<uint32_t>(g) : 0u;
-                }
-            }
             int mode;
             uint32_t thr;
-            threshold_mode(ES, have, tk, mode, thr);
+            threshold_mode(ES, hasT, T, mode, thr);
             for (int64_t c0 = lo; c0 < hi; c0 += p.chunk) {
                 const int64_t ce = (hi - c0) < p.chunk ? (hi - c0) : p.chunk;
                 const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
                 const int s = seq % p.stages, use = seq / p.stages;
-                if (SPLIT && seq > 0) {
-                    int req = 0;
-                    if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
-                    if (__shfl_sync(0xFFFFFFFFu, req, 0)) {
-                        split_compact();
-                        threshold_mode(ES, true, T, mode, thr);
-                        have = true;
-                        tk = T;
-                    }
-                }
                 const bool got = wait_bounded(&ctrl->full[s], use & 1, ctrl);
                 if (got && tid == 0) ctrl->observed[s] = use + 1;
-                if (SPLIT && seq == 0) {
-                    // split rows: the first chunk of every CTA feeds the cluster warm-up
-                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
-                    const int tail = static_cast<int>(ce - bytes / ES);
-                    uint32_t wcnt = 0u;
-                    warmup_select<KeyT>(src, got ? static_cast<int>(bytes / 16) : 0, xrow, c0 + bytes / ES,
-                                        got ? tail : 0, static_cast<uint32_t>(c0), p.k, p.G, hist,
-                                        hist + kScratchWords / 2, ghist, ckey, cidx, ctrl, p.cap, tid, hasT, T, tmax,
-                                        wcnt);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctrl->empty[s]);
-                    // the warm-up appended through the shared cursor; its final sync makes it exact
-                    n = ctrl->cnt;
-                    badd += static_cast<uint32_t>(n);
-                    if (tid == 0 && hasT && shared_T) {
-                        if (CL) publish_T(T);
-                        if (MC)
-                            atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
-                    }
-                    if (hasT) threshold_mode(ES, true, T, mode, thr);
-                    have = have || hasT;
-                    tk = hasT ? T : tk;
-                } else if (SPLIT) {
-                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
-                    const int nvec = got ? static_cast<int>(bytes / 16) : 0;
-                    const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
-                    const uint32_t col0 = static_cast<uint32_t>(c0);
-                    const int64_t tfirst = c0 + bytes / ES;
-                    const uint32_t page = (hasT && T != 0u) ? page_size : 0u;
-                    if (mode == 0)
-                        filter_chunk_paged<KeyT, 0>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
-                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
-                    else if (mode == 1)
-                        filter_chunk_paged<KeyT, 1>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
-                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
-                    else
-                        filter_chunk_paged<KeyT, 2>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk, &ctrl->empty[s],
-                                                    ckey, cidx, ctrl, p.cap, tid, pg_cur, pg_end, page, trigger, tmax);
-                } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
-                    const int nvec = got ? static_cast<int>(bytes / 16) : 0;
-                    const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
-                    const uint32_t col0 = static_cast<uint32_t>(c0);
-                    const int64_t tfirst = c0 + bytes / ES;
-                    uint32_t add;
-                    if (mode == 0)
-                        add = filter_chunk_sync<KeyT, 0>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
-                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
-                    else if (mode == 1)
-                        add = filter_chunk_sync<KeyT, 1>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
-                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
-                    else
-                        add = filter_chunk_sync<KeyT, 2>(src, nvec, col0, thr, xrow, tfirst, tail, have, tk,
-                                                         &ctrl->empty[s], ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
-                    n += static_cast<int>(add);
-                    badd += add;
-                }
+                const uint4* src = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * chunk_bytes);
+                const int nvec = got ? static_cast<int>(bytes / 16) : 0;
+                const int tail = got ? static_cast<int>(ce - bytes / ES) : 0;
+                const uint32_t col0 = static_cast<uint32_t>(c0);
+                const int64_t tfirst = c0 + bytes / ES;
+                uint32_t add;
+                if (mode == 0)
+                    add = filter_chunk_sync<KeyT, 0>(src, nvec, col0, thr, xrow, tfirst, tail, hasT, T, &ctrl->empty[s],
+                                                     ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                else if (mode == 1)
+                    add = filter_chunk_sync<KeyT, 1>(src, nvec, col0, thr, xrow, tfirst, tail, hasT, T, &ctrl->empty[s],
+                                                     ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                else
+                    add = filter_chunk_sync<KeyT, 2>(src, nvec, col0, thr, xrow, tfirst, tail, hasT, T, &ctrl->empty[s],
+                                                     ckey, cidx, ctrl, p.cap, tid, n, seq & 1, tmax);
+                n += static_cast<int>(add);
+                badd += add;
                 ++seq;
             }
-            // end of block (one CTA per row): |C| is known in every thread; compact at >= k + B2
-            if (SPLIT) continue;
+            // end of block: |C| is known in every thread; compact at >= k + B2
             if (tid == 0) {
                 sA += badd;
                 sMax = n > sMax ? n : sMax;
@@ -1069,42 +537,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
                 T = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, lo_k, tmax, tid);
                 hasT = true;
                 n = p.k;
-                if (tid == 0 && shared_T) {
-                    if (CL) publish_T(T);
-                    if (MC)
-                        atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | T);
-                }
             }
-        }
-        if (SPLIT) {
-            // A warp out of chunks still joins any compaction another warp requested:
-            // it reads the count of finished warps before the request flag, so a request
-            // raised by the last warp before it finished is always seen.
-            close_page<KeyT>(ckey, cidx, pg_cur, pg_end, lane);
-            __threadfence_block();
-            if (lane == 0) atomicAdd(&ctrl->done_warps, 1);
-            const long long t0 = clock64();
-            while (true) {
-                int d = 0, f = 0;
-                if (lane == 0) {
-                    d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
-                    __threadfence_block();
-                    f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
-                }
-                d = __shfl_sync(0xFFFFFFFFu, d, 0);
-                f = __shfl_sync(0xFFFFFFFFu, f, 0);
-                if (f) {
-                    split_compact();
-                    continue;
-                }
-                if (d >= kNCW) break;
-                if (clock64() - t0 > kSpinLimit) {  // cannot happen; keep the CTA alive
-                    set_status(kErrTimeout);
-                    break;
-                }
-            }
-            named_bar_sync(1, NC);
-            n = ctrl->cnt;
         }
         const uint32_t wm = warp_max(tmax);
         if (lane == 0) atomicMax(&ctrl->maxkey, wm);
@@ -1112,7 +545,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
             ctrl->fin_n = n;
             ctrl->fin_hasT = hasT ? 1 : 0;
             ctrl->fin_T = T;
-            if (p.stats && p.parts == 1) {
+            if (p.stats) {
                 long long* st = p.stats + row * DS_NSTAT;
                 st[0] = sA;
                 st[1] = sR;
@@ -1131,48 +564,16 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
             if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
     }
     const int n = ctrl->fin_n;
-    const bool hasT = ctrl->fin_hasT != 0;
-    const uint32_t T = ctrl->fin_T;
 
-    // ------------------------------ final selection over the cluster --------------
-    uint32_t lo_own = hasT ? T : 0u;
-    if (MC) {
-        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_own = max(lo_own, static_cast<uint32_t>(g));
-    }
-    uint32_t lo0, hi0;
-    if (CL) {
-        if (tid < p.G) {
-            red_cluster_max_u32(map_rank(&ctrl->gmax, tid), ctrl->maxkey);
-            red_cluster_max_u32(map_rank(&ctrl->sharedT, tid), lo_own);
-        }
-        cluster_sync_all();
-        lo0 = *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT);
-        hi0 = *reinterpret_cast<volatile uint32_t*>(&ctrl->gmax);
-    } else {
-        lo0 = lo_own;
-        hi0 = ctrl->maxkey;
-    }
+    // ------------------------------ final selection --------------------------------
     OutTarget out;
-    if (MC) {
-        out.vals = p.ws_key;
-        out.idx = p.ws_idx;
-        out.base = (row * p.C + cl) * static_cast<int64_t>(p.k);
-        out.to_keys = true;
-    } else {
-        out.vals = p.out_vals;
-        out.idx = p.out_idx;
-        out.base = row * static_cast<int64_t>(p.k);
-        out.to_keys = false;
-    }
+    out.vals = p.out_vals;
+    out.idx = p.out_idx;
+    out.base = row * static_cast<int64_t>(p.k);
+    out.to_keys = false;
     out.esize = ES;
-    const bool write_ok = !ctrl->abort;
-    uint32_t kept;
-    if constexpr (CL)
-        kept = final_select<KeyT, NT, true>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, p.G, out, write_ok, tid);
-    else
-        kept = final_select<KeyT, NT, false>(ckey, cidx, hist, ghist, ctrl, n, p.k, lo0, hi0, 1, out, write_ok, tid);
-    if (MC && crank == 0 && tid == 0) p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(kept);
+    const uint32_t lo0 = ctrl->fin_hasT ? ctrl->fin_T : 0u;
+    final_select<KeyT, NT>(ckey, cidx, hist, ctrl, n, p.k, lo0, ctrl->maxkey, out, !ctrl->abort, tid);
 }
 
 }  // namespace dsk
@@ -1264,8 +665,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeP
     out.base = row * static_cast<int64_t>(p.k);
     out.to_keys = false;
     out.esize = ES;
-    final_select<KeyT, NT, false>(ckey, cidx, hist, hist, ctrl, n, p.k, hasT ? T : lo_g, ctrl->maxkey, 1, out, true,
-                                  tid);
+    final_select<KeyT, NT>(ckey, cidx, hist, ctrl, n, p.k, hasT ? T : lo_g, ctrl->maxkey, out, true, tid);
 }
 
 // ================================================================ host ============
@@ -1410,7 +810,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         if (!ok) return DS_ERR_UNSUPPORTED;
     } else {
         const auto layout_bytes = [&](int s) -> size_t {
-            return scan_layout(P.es, P.chunk, s, P.cap, G, P.perm_cap).total;
+            return scan_layout(P.es, P.chunk, s, P.cap, P.perm_cap).total;
         };
         // Ring depth: the deepest ring (3..8) that still lets two CTAs share an SM;
         // otherwise the deepest ring that fits one CTA (at least 2 stages).
@@ -1519,7 +919,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     void (*kern)(ScanParams);
     int slot = sizeof(KeyT) == 2 ? 0 : 1;
     if (P.parts == 1) {
-        kern = ds_scan_kernel<KeyT, 0>;
+        kern = ds_scan_kernel<KeyT>;
     } else {
         kern = ds_split_kernel<KeyT>;
         slot += 2;
