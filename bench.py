@@ -40,7 +40,7 @@ ROWS, N, K_TOP, B, B2 = 64, 131072, 512, 4096, 4096
 SEED = 0x5EED
 WORKLOAD = f"indexer_bf16: {ROWS} rows x {N} bf16 N(0,1), stride {N}, k={K_TOP}, B={B}, B2={B2}"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ds_scan_kernel_indexer_bf16.md")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ds_split_kernel_indexer_bf16.md")
 
 
 def _dist():
@@ -311,14 +311,15 @@ def run_gpu(args):
     ms_per_step = t_max / args.steps
     value = ws * step_bytes * args.steps / (t_max * 1e-3) / 1e9
 
-    # roofline of the scan kernel: algorithmic bytes per launch / average launch time
+    # roofline of the split-row kernel (the one kernel of a step): algorithmic bytes per
+    # launch / average launch time
     alg_bytes = step_bytes + ROWS * K_TOP * (2 + 4)
     peak, peak_kind = _peak()
     achieved = alg_bytes / (ms / args.steps * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
                 "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
-                "kernel": "ds_scan_kernel<uint16_t>"}
+                "kernel": "ds_split_kernel<uint16_t>"}
 
     # e2e through the public API with host buffers
     pinned = host.pin_memory()
