@@ -242,3 +242,58 @@ def test_graph_capture_replay():
     torch.cuda.synchronize()
     v = vals.cpu().numpy().view(np.uint16)
     check_topk(w.x, w.dtype, 512, v, idx.cpu().numpy())
+
+
+# ------------------------------------------------- consecutive calls on one stream -----
+# Calls on a stream may overlap their edges (programmatic dependent launch): a call starts
+# its scan while the previous call finishes, and writes its outputs only once the previous
+# call has completed.
+
+def test_back_to_back_calls_same_outputs():
+    """A graph of consecutive calls on different inputs into the same outputs: the outputs
+    hold the last call's result, and intermediate results (copied out between calls)
+    are each correct."""
+    import top_selection_gb300 as ds
+    ws = [synth.indexer_bf16(seed=600 + i, rows=16, N=131072) for i in range(6)]
+    xs = [to_device(w.x, w.dtype) for w in ws]
+    vals = torch.empty((16, 512), dtype=xs[0].dtype, device="cuda")
+    idx = torch.empty((16, 512), dtype=torch.int32, device="cuda")
+    keep_v = [torch.empty_like(vals) for _ in xs]
+    keep_i = [torch.empty_like(idx) for _ in xs]
+    ds.topk(xs[0], 512, 4096, 4096, seed=3, out=(vals, idx))
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i, x in enumerate(xs):
+                ds.topk(x, 512, 4096, 4096, seed=3, out=(vals, idx))
+                if i % 2 == 1:
+                    keep_v[i].copy_(vals)
+                    keep_i[i].copy_(idx)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert ds.ds_get_device_status() == 0
+    check_topk(ws[-1].x, ws[-1].dtype, 512, vals.cpu().numpy().view(np.uint16), idx.cpu().numpy())
+    for i in (1, 3):
+        check_topk(ws[i].x, ws[i].dtype, 512, keep_v[i].cpu().numpy().view(np.uint16), keep_i[i].cpu().numpy())
+
+
+def test_input_written_right_before_each_call():
+    """The input of every call is written by a copy kernel just before the call, on the same
+    stream; every result matches its own input."""
+    import top_selection_gb300 as ds
+    ws = [synth.indexer_bf16(seed=700 + i, rows=16, N=131072) for i in range(4)]
+    srcs = [to_device(w.x, w.dtype) for w in ws]
+    x = torch.empty_like(srcs[0])
+    outs = [(torch.empty((16, 512), dtype=x.dtype, device="cuda"), torch.empty((16, 512), dtype=torch.int32,
+                                                                                device="cuda")) for _ in ws]
+    for rep in range(2):
+        for i in range(len(ws)):
+            x.copy_(srcs[i])
+            ds.topk(x, 512, 4096, 4096, seed=5, out=outs[i])
+        torch.cuda.synchronize()
+        assert ds.ds_get_device_status() == 0
+        for i, w in enumerate(ws):
+            check_topk(w.x, w.dtype, 512, outs[i][0].cpu().numpy().view(np.uint16), outs[i][1].cpu().numpy())

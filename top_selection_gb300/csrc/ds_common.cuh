@@ -178,6 +178,14 @@ __device__ __forceinline__ uint32_t set_gtu_f32(uint32_t a, uint32_t b) {
     return d;
 }
 
+// Programmatic dependent launch: let the stream's next kernel start launching its CTAs
+// as this one's leave, and wait until the stream's previous kernel has completed and its
+// memory operations are visible.  Both are no-ops for kernels launched without it.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

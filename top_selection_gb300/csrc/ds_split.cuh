@@ -370,6 +370,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     const bool MC = p.C > 1;
     const uint32_t cap = static_cast<uint32_t>(p.cap);
 
+    // The next call may start as this one's CTAs leave; this call's global writes wait for
+    // the previous call to complete (at once when rows span several clusters, which share
+    // a global threshold word and a workspace between calls).
+    pdl_launch_dependents();
+    if (MC) pdl_wait();
     {
         int* z = reinterpret_cast<int*>(ctrl);
         for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
@@ -751,6 +756,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         out.to_keys = false;
     }
     const bool write_ok = !ctrl->abort;
+    pdl_wait();  // the previous call's outputs are complete before this call writes its own
     // Two passes over the candidates, each thread taking a contiguous run of them (runs in
     // thread order): count the keys above / equal to the pivot, place the runs after each
     // other (bit-plane prefix sums in the warp, one barrier across warps), then write.

@@ -440,6 +440,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
 
+    pdl_launch_dependents();  // the next call may start as this one's CTAs leave
     {
         int* z = reinterpret_cast<int*>(ctrl);
         for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
@@ -545,6 +546,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
             ctrl->fin_n = n;
             ctrl->fin_hasT = hasT ? 1 : 0;
             ctrl->fin_T = T;
+            pdl_wait();  // the previous call has completed before this call writes
             if (p.stats) {
                 long long* st = p.stats + row * DS_NSTAT;
                 st[0] = sA;
@@ -573,6 +575,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     out.to_keys = false;
     out.esize = ES;
     const uint32_t lo0 = ctrl->fin_hasT ? ctrl->fin_T : 0u;
+    pdl_wait();  // the previous call's outputs are complete before this call writes its own
     final_select<KeyT, NT>(ckey, cidx, hist, ctrl, n, p.k, lo0, ctrl->maxkey, out, !ctrl->abort, tid);
 }
 
@@ -930,8 +933,13 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     cfg.blockDim = dim3(P.parts == 1 ? kScanThreads : kSplitThreads, 1, 1);
     cfg.dynamicSmemBytes = P.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
+    // programmatic dependent launch: consecutive calls on a stream overlap their edges
+    // (each kernel waits for its predecessor before its first global write)
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (P.G > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = P.G;
