@@ -425,9 +425,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
         ctrl->issued[s] = use + 1;
     };
-    // chunk 0 feeds the warm-up: it goes first, the rest of the ring once it has landed
-    // (requested together, chunk 0 of some CTAs lands late and holds their clusters up)
+    // chunk 0 feeds the warm-up: it goes first, the rest of the ring right behind it
     if (tid == 0) issue(0);
+    if (lane == 0)
+        for (int q = warp == 0 ? kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
     // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
     // and waits only before its CTA's first access to another CTA's memory, so the
     // cluster's CTAs meet while the first copies are in flight.
@@ -490,34 +491,43 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while chunk 0 lands
         const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
         if (tid == 0 && got0) ctrl->observed[0] = 1;
-        if (lane == 0)
-            for (int q = warp == 0 ? kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
         {
             // group maxima: thread t owns vectors t, t + NC, ... (VT of them) and splits
             // them into R groups of consecutive vectors; a group's maximum is taken on the
             // packed values (NaNs ignored) and keyed once
             const int R = wm / 256;
-            const int VT = (p.chunk * ES / 16 + NC - 1) / NC;
-            const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
+            const int VT = (p.chunk * ES / 16 + NC - 1) / NC;  // at most 4 (16 KB chunks)
+            const int vpg = VT / R > 0 ? VT / R : 1;          // vectors per group
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            for (int r = 0; r < R; ++r) {
-                uint32_t m = ES == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf
-                bool any = false;
-                for (int j = r * vpg; j < (r + 1) * vpg && j < VT; ++j) {
-                    const int v = tid + j * NC;
-                    if (got0 && v < nvec0) {
-                        const uint4 x = v0[v];
-                        if (ES == 2) {
-                            m = max_bf16x2(m, max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w)));
-                        } else {
-                            m = __float_as_uint(fmaxf(__uint_as_float(m),
-                                                      fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
-                                                            fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)))));
-                        }
-                        any = true;
-                    }
+            uint32_t vm[4];  // packed maximum of each of the thread's vectors (-inf past the chunk)
+            bool vv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int v = tid + j * NC;
+                vv[j] = got0 && j < VT && v < nvec0;
+                const uint4 x = vv[j] ? v0[v] : make_uint4(0u, 0u, 0u, 0u);
+                if (ES == 2) {
+                    vm[j] = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
+                } else {
+                    vm[j] = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                                  fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
                 }
-                wx[crank * wm + tid * R + r] = static_cast<KeyT>(any ? max_word_key<KeyT>(m) : 0u);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r < R) {
+                    uint32_t m = ES == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf
+                    bool any = false;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if (j >= r * vpg && j < (r + 1) * vpg && vv[j]) {
+                            m = ES == 2 ? max_bf16x2(m, vm[j])
+                                        : __float_as_uint(fmaxf(__uint_as_float(m), __uint_as_float(vm[j])));
+                            any = true;
+                        }
+                    }
+                    wx[crank * wm + tid * R + r] = static_cast<KeyT>(any ? max_word_key<KeyT>(m) : 0u);
+                }
             }
             fence_proxy_async_smem();
             named_bar_sync(1, NC);
