@@ -682,12 +682,21 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     uint32_t* xr = reinterpret_cast<uint32_t*>(smem + L.xf);
     for (int lvl = 0;; ++lvl) {
         uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
-        for (int i = tid; i < n; i += NT) {
-            const uint32_t kk = ckey[i];
-            if (in_play(kk) && kk >= lbase && kk <= lhi) {
-                uint32_t d = (kk - lbase) >> s;
-                d = d < kXBins - 1 ? d : kXBins - 1;
-                atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
+        for (int i0 = 0; i0 < n; i0 += NT * 8) {  // batches of 8 keys per thread, loads issued together
+            uint32_t kb[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int i = i0 + tid + j * NT;
+                kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t kk = kb[j];
+                if (i0 + tid + j * NT < n && in_play(kk) && kk >= lbase && kk <= lhi) {
+                    uint32_t d = (kk - lbase) >> s;
+                    d = d < kXBins - 1 ? d : kXBins - 1;
+                    atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
+                }
             }
         }
         fence_proxy_async_smem();
@@ -710,12 +719,16 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         const uint16_t* all = reinterpret_cast<const uint16_t*>(xr + static_cast<size_t>(lvl & 1) * G * XW);
         const auto cnt = [&](int b) {
             uint32_t t = 0u;
-            for (int c = 0; c < G; ++c) t += all[c * kXBins + b];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c < G) t += all[c * kXBins + b];
             return t;
         };
         const auto low = [&](int b) {
             uint32_t t = 0u;
-            for (int c = 0; c < static_cast<int>(crank); ++c) t += all[c * kXBins + b];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c < static_cast<int>(crank)) t += all[c * kXBins + b];
             return t;
         };
         int bstar;
@@ -767,24 +780,36 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     const bool write_ok = !ctrl->abort;
     pdl_wait();  // the previous call's outputs are complete before this call writes its own
-    // Two passes over the candidates, each thread taking a contiguous run of them (runs in
-    // thread order): count the keys above / equal to the pivot, place the runs after each
-    // other (bit-plane prefix sums in the warp, one barrier across warps), then write.
-    const int m = (n + NT - 1) / NT;
-    const int i0 = tid * m < n ? tid * m : n;
-    const int i1 = i0 + m < n ? i0 + m : n;
-    uint32_t ng = 0u, ne = 0u;
-#pragma unroll 4
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = ckey[i];
+    // Two passes over the candidates in batches of 8 per thread (thread t takes t, t + NT,
+    // ...; loads issued together): count the keys above / equal to the pivot, place the
+    // threads after each other (bit-plane prefix sums in the warp, one barrier across
+    // warps), then write.  Pivot-equal keys are taken in thread order until the quota.
+    const auto classify = [&](uint32_t kk, bool& isg, bool& ise) {
         const bool inr = in_play(kk);
-        ng += (inr && (take_all || kk > pivot)) ? 1u : 0u;
-        ne += (inr && !take_all && kk == pivot) ? 1u : 0u;
+        isg = inr && (take_all || kk > pivot);
+        ise = inr && !take_all && kk == pivot;
+    };
+    uint32_t ng = 0u, ne = 0u;
+    for (int i0 = 0; i0 < n; i0 += NT * 8) {
+        uint32_t kb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + tid + j * NT;
+            kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            bool isg, ise;
+            classify(kb[j], isg, ise);
+            const bool ok = i0 + tid + j * NT < n;
+            ng += (ok && isg) ? 1u : 0u;
+            ne += (ok && ise) ? 1u : 0u;
+        }
     }
     const uint32_t ltm = lanemask_lt();
     uint32_t pg = 0u, pe = 0u, wg = 0u, we = 0u;  // exclusive prefixes in the warp, warp totals
 #pragma unroll
-    for (int bit = 0; bit < 16; ++bit) {  // runs hold fewer than 2^16 keys
+    for (int bit = 0; bit < 16; ++bit) {  // counts stay below 2^16
         const uint32_t bg = __ballot_sync(0xFFFFFFFFu, (ng >> bit) & 1u);
         const uint32_t be = __ballot_sync(0xFFFFFFFFu, (ne >> bit) & 1u);
         pg += static_cast<uint32_t>(__popc(bg & ltm)) << bit;
@@ -799,33 +824,47 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     __syncthreads();
     uint32_t g = gt_lower + pg, e = pe;
-    for (int w = 0; w < warp; ++w) {
-        g += ctrl->warp_tot[1][w];
-        e += ctrl->warp_tot[1][16 + w];
-    }
-#pragma unroll 4
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t kk = ckey[i];
-        if (!in_play(kk)) continue;
-        int64_t slot = -1;
-        if (take_all || kk > pivot) {
-            slot = g++;
-        } else if (kk == pivot) {
-            const uint32_t t = e++;
-            if (t < eq_take) slot = eq_first + t;
+#pragma unroll
+    for (int w = 0; w < kNCW; ++w) {
+        if (w < warp) {
+            g += ctrl->warp_tot[1][w];
+            e += ctrl->warp_tot[1][16 + w];
         }
-        if (slot >= 0 && write_ok) {
-            if (slot < p.k) {
+    }
+    // slots are decided without branches; only the stores are predicated
+    const uint32_t kslots = static_cast<uint32_t>(p.k);
+    uint32_t bad = 0u;
+    for (int i0 = 0; i0 < n; i0 += NT * 8) {
+        uint32_t kb[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + tid + j * NT;
+            kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = i0 + tid + j * NT;
+            const uint32_t kk = kb[j];
+            bool isg, ise;
+            classify(kk, isg, ise);
+            isg = isg && i < n;
+            ise = ise && i < n;
+            const uint32_t te = e;
+            const uint32_t slot = isg ? g : eq_first + te;
+            const bool put = isg || (ise && te < eq_take);
+            g += isg ? 1u : 0u;
+            e += ise ? 1u : 0u;
+            if (put && slot < kslots && write_ok) {
                 const int64_t o = out.base + slot;
                 if (out.to_keys) static_cast<uint32_t*>(out.vals)[o] = kk;
                 else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
                 else static_cast<uint32_t*>(out.vals)[o] = unkey_f32(kk);
                 out.idx[o] = static_cast<int32_t>(cidx[i]);
-            } else {
-                set_status(kErrInternal);
             }
+            bad |= (put && slot >= kslots) ? 1u : 0u;
         }
     }
+    if (bad) set_status(kErrInternal);
     if (take_all && !MC && tid == 0) set_status(kErrInternal);  // a whole row held fewer than k keys in play
     if (MC && crank == 0 && tid == 0)
         p.ws_cnt[row * p.C + cl] = static_cast<int32_t>(take_all ? gt_all : static_cast<uint32_t>(p.k));

@@ -747,10 +747,16 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     if (cap64 > (int64_t(1) << 20)) return DS_ERR_UNSUPPORTED;
     int parts = opt ? opt->parts : 0;
     if (parts < 0) return DS_ERR_INVALID_ARG;
+    if (parts == 0 && opt && opt->stats) parts = 1;  // the statistics describe the one-CTA schedule
     if (parts == 0) {
+        // Enough CTAs to cover the SMs: rows split in parts of at least 4 blocks.  Rows that
+        // already cover the SMs still go in halves when k is small against a chunk (the
+        // split-row kernel keeps k + one chunk of candidates and runs two CTAs per SM,
+        // where a whole row's CTA needs k + B + B2 and runs alone).
         parts = 1;
         const int64_t maxp = P.m / 4 > 1 ? P.m / 4 : 1;
         while (rows * parts < di.sms && parts * 2 <= maxp && parts < 256) parts *= 2;
+        if (parts == 1 && maxp >= 2 && static_cast<int64_t>(k) * 4 <= P.chunk) parts = 2;
         while ((P.m + parts - 1) / parts > kPermMax) parts *= 2;
         if (parts > P.m) return DS_ERR_UNSUPPORTED;
     } else {
