@@ -108,6 +108,12 @@ typedef struct {
     int64_t* stats;         /* optional device array rows*DS_NSTAT, parts == 1 only    */
     void* workspace;        /* optional caller-owned device workspace; NULL = library  */
     size_t workspace_bytes; /* its size; see ds_workspace_bytes                        */
+    int32_t input_ready;    /* 0 (default): the call reads x only after every earlier
+                               kernel on the stream has completed, so x may be written
+                               by the kernel just before it.  Nonzero: the caller states
+                               that x was complete before that kernel started, and the
+                               call starts reading x while that kernel is still running
+                               (consecutive calls on static inputs overlap their edges) */
 } ds_options;
 
 /* ds_topk with explicit options (NULL = defaults, identical to ds_topk). */

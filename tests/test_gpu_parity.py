@@ -249,10 +249,12 @@ def test_graph_capture_replay():
 # its scan while the previous call finishes, and writes its outputs only once the previous
 # call has completed.
 
-def test_back_to_back_calls_same_outputs():
+@pytest.mark.parametrize("ready", [False, True])
+def test_back_to_back_calls_same_outputs(ready):
     """A graph of consecutive calls on different inputs into the same outputs: the outputs
     hold the last call's result, and intermediate results (copied out between calls)
-    are each correct."""
+    are each correct -- also when the calls state that their inputs were complete before
+    the previous call started (and so overlap it)."""
     import top_selection_gb300 as ds
     ws = [synth.indexer_bf16(seed=600 + i, rows=16, N=131072) for i in range(6)]
     xs = [to_device(w.x, w.dtype) for w in ws]
@@ -267,7 +269,7 @@ def test_back_to_back_calls_same_outputs():
     with torch.cuda.stream(s):
         with torch.cuda.graph(g, stream=s):
             for i, x in enumerate(xs):
-                ds.topk(x, 512, 4096, 4096, seed=3, out=(vals, idx))
+                ds.topk(x, 512, 4096, 4096, seed=3, out=(vals, idx), input_ready=ready)
                 if i % 2 == 1:
                     keep_v[i].copy_(vals)
                     keep_i[i].copy_(idx)
@@ -297,3 +299,27 @@ def test_input_written_right_before_each_call():
         assert ds.ds_get_device_status() == 0
         for i, w in enumerate(ws):
             check_topk(w.x, w.dtype, 512, outs[i][0].cpu().numpy().view(np.uint16), outs[i][1].cpu().numpy())
+
+
+@pytest.mark.parametrize("parts", [0, 1])
+def test_input_is_previous_calls_output(parts):
+    """A call whose input is the output of the call just before it on the stream (which
+    lets its successor start early) reads that output only once it is complete: the top-64
+    of each row's top-512 values is the row's top-64."""
+    import top_selection_gb300 as ds
+    ws = [synth.indexer_bf16(seed=900 + i, rows=64, N=131072) for i in range(3)]
+    xs = [to_device(w.x, w.dtype) for w in ws]
+    mid = torch.empty((64, 512), dtype=xs[0].dtype, device="cuda")
+    mid_i = torch.empty((64, 512), dtype=torch.int32, device="cuda")
+    outs = [(torch.empty((64, 64), dtype=mid.dtype, device="cuda"),
+             torch.empty((64, 64), dtype=torch.int32, device="cuda")) for _ in range(20)]
+    for j in range(len(outs)):
+        mid.fill_(-1)  # every value -1.0: a stale read returns only -1.0
+        ds.topk(xs[j % 3], 512, 4096, 4096, seed=5, out=(mid, mid_i))
+        ds.topk(mid, 64, 256, 256, seed=6, out=outs[j], parts=parts)
+    torch.cuda.synchronize()
+    assert ds.ds_get_device_status() == 0
+    want = [oracle.topk_sort(bits_of(w.x, w.dtype), w.dtype, 64, threads=8)[0] for w in ws]
+    for j, (v, _) in enumerate(outs):
+        got = np.sort(v.cpu().numpy().view(np.uint16).astype(np.int64), axis=1)
+        assert np.array_equal(got, np.sort(want[j % 3].astype(np.int64), axis=1)), f"call {j}"

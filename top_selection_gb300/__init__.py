@@ -47,7 +47,7 @@ class DSError(RuntimeError):
 class ds_options(ctypes.Structure):
     _fields_ = [("parts", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("stats", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("input_ready", ctypes.c_int32)]
 
 
 class ds_plan(ctypes.Structure):
@@ -105,9 +105,9 @@ def load():
         return lib
 
 
-def _opts(parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0):
+def _opts(parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, input_ready=False):
     return ds_options(int(parts), int(cluster), int(stats) or None, int(workspace) or None,
-                      int(workspace_bytes))
+                      int(workspace_bytes), 1 if input_ready else 0)
 
 
 # ------------------------------------------------------------------ C ABI mirror ----
@@ -119,8 +119,9 @@ def ds_topk(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, st
 
 
 def ds_topk_ex(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx,
-               parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, stream=0) -> int:
-    o = _opts(parts, cluster, stats, workspace, workspace_bytes)
+               parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, input_ready=False,
+               stream=0) -> int:
+    o = _opts(parts, cluster, stats, workspace, workspace_bytes, input_ready)
     return load().ds_topk_ex(int(x) or None, dtype, rows, N, row_stride, k, B, B2, seed,
                              int(out_vals) or None, int(out_idx) or None, ctypes.byref(o),
                              int(stream) or None)
@@ -189,12 +190,15 @@ def _torch_dtype_code(t):
 
 
 def topk(x, k: int, B: int, B2: int, seed: int = 0x5EED, N: int | None = None,
-         out=None, parts: int = 0, cluster: int = 0, stats=None, workspace=None, stream=None):
+         out=None, parts: int = 0, cluster: int = 0, stats=None, workspace=None, stream=None,
+         input_ready: bool = False):
     """Row-wise DeepSelect top-k of a CUDA tensor ``x`` of shape (rows, stride).
 
     Returns (values, indices), each (rows, k), unordered within a row.  ``N`` (default:
     the row length) may be shorter than the stride.  ``stats`` is an optional int64
-    CUDA tensor (rows, DS_NSTAT) filled when each row is one part."""
+    CUDA tensor (rows, DS_NSTAT) filled when each row is one part.  ``input_ready`` states
+    that ``x`` was complete before the previous kernel on the stream started, which lets
+    the call start reading it while that kernel finishes."""
     import torch
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (there is no CPU path)")
@@ -219,7 +223,7 @@ def topk(x, k: int, B: int, B2: int, seed: int = 0x5EED, N: int | None = None,
     st = ds_topk_ex(x.data_ptr(), dtype, rows, n, stride, k, B, B2, seed, vals.data_ptr(),
                     idx.data_ptr(), parts=parts, cluster=cluster,
                     stats=0 if stats is None else stats.data_ptr(), workspace=ws_ptr,
-                    workspace_bytes=ws_bytes, stream=stream)
+                    workspace_bytes=ws_bytes, input_ready=input_ready, stream=stream)
     if st != 0:
         raise DSError(st)
     return vals, idx

@@ -370,9 +370,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     const bool MC = p.C > 1;
     const uint32_t cap = static_cast<uint32_t>(p.cap);
 
-    // The next call may start as this one's CTAs leave; this call's global writes wait for
-    // the previous call to complete (at once when rows span several clusters, which share
-    // a global threshold word and a workspace between calls).
+    // The next kernel on the stream may start as this one's CTAs leave.  This kernel may
+    // have started before the previous one completed: it waits for it before reading x
+    // (unless the caller stated that x was complete earlier) and before any global write
+    // (at once when rows span several clusters, which share a global threshold word and a
+    // workspace between calls).
     pdl_launch_dependents();
     if (MC) pdl_wait();
     {
@@ -425,6 +427,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
         ctrl->issued[s] = use + 1;
     };
+    if (!MC && !p.early) pdl_wait();
     // chunk 0 feeds the warm-up: it goes first, the rest of the ring right behind it
     if (tid == 0) issue(0);
     if (lane == 0)

@@ -100,6 +100,7 @@ struct ScanParams {
     int32_t parts, G, C;          // CTAs per row, CTAs per cluster, clusters per row
     int32_t chunk, stages, cap, perm_cap;
     int32_t wm;                   // split rows: warm-up group maxima per CTA
+    int32_t early;                // start reading x before the previous kernel completes
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
     uint32_t* ws_key;             // per (row, cluster) partial results (C > 1)
@@ -440,7 +441,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
 
-    pdl_launch_dependents();  // the next call may start as this one's CTAs leave
+    // The next kernel on the stream may start as this one's CTAs leave.  This kernel may
+    // have started before the previous one completed: it waits for it before reading x
+    // (unless the caller stated that x was complete earlier) and before writing anything.
+    pdl_launch_dependents();
     {
         int* z = reinterpret_cast<int*>(ctrl);
         for (int i = tid; i < static_cast<int>(sizeof(Ctrl) / sizeof(int)); i += NT) z[i] = 0;
@@ -452,6 +456,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         fence_mbar_init();
     }
     block_order<NT>(p.seed, row, 0, mp, hist, perm, tid);
+    if (!p.early) pdl_wait();
 
     if (warp == kNCW) {
         // ------------------------------ producer: bulk copies in block order ------
@@ -889,7 +894,7 @@ static cudaError_t set_smem(Kern kern, int slot, int dev, size_t bytes, bool non
 template <typename KeyT>
 static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
                         int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, long long* stats,
-                        char* ws, cudaStream_t stream) {
+                        char* ws, bool early, cudaStream_t stream) {
     ScanParams sp;
     sp.x = static_cast<const char*>(x);
     sp.rows = rows;
@@ -911,6 +916,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.cap = P.cap;
     sp.perm_cap = P.perm_cap;
     sp.wm = P.wm;
+    sp.early = early ? 1 : 0;
     sp.epoch = 0;
     sp.gT = nullptr;
     sp.ws_key = nullptr;
@@ -1075,9 +1081,11 @@ ds_status ds_topk_ex(const void* x, int32_t dtype, int64_t rows, int64_t N, int6
         }
     }
     long long* stats = options ? reinterpret_cast<long long*>(options->stats) : nullptr;
+    const bool early = options && options->input_ready;
     if (dtype == DS_BF16)
-        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, stream);
-    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, stream);
+        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, early,
+                                stream);
+    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, early, stream);
 }
 
 ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k, int32_t B,
@@ -1120,8 +1128,10 @@ ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N,
         ws = static_cast<char*>(g_static_ws_addr[dev]);
     }
     if (dtype == DS_BF16)
-        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, stream);
-    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, stream);
+        return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, false,
+                                stream);
+    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, false,
+                            stream);
 }
 
 size_t ds_noalloc_scratch_bytes(void) { return kStaticWorkspaceBytes; }
