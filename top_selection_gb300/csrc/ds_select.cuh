@@ -52,6 +52,8 @@ struct Ctrl {
     int fin_n;                   // consumer state handed to the whole CTA after the scan
     int fin_hasT;
     uint32_t fin_T;
+    int out_g;                   // split rows: output cursors of the final select (keys above
+    int out_e;                   // the pivot, pivot-equal keys)
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

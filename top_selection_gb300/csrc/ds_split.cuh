@@ -37,6 +37,7 @@ namespace dsk {
 
 constexpr int kXBits = 9;               // final-select digit width
 constexpr int kXBins = 1 << kXBits;     // final-select bins per pass (exchanged as uint16)
+static_assert(kXBins == 32 * 16, "warp_pivot_x gives each lane 16 bins");
 constexpr int kWarmMaxBytes = 16384;    // group maxima exchanged by the warm-up, all CTAs
 constexpr int kSplitThreads = kNCW * 32;  // consumer warps only: each issues its own copies
 
@@ -234,6 +235,85 @@ __device__ __forceinline__ void cta_pivot(uint32_t k, Cnt&& cnt, Low&& low, Ctrl
     __syncthreads();  // the shared results are read before the next search writes them
 }
 
+// The pivot of a final-select pass, found by every warp on its own (no barrier).  The
+// cluster's histogram is G rows of kXBins 16-bit counts (pairs in 32-bit words), row c
+// from the CTA of rank c; lane l owns bins [16l, 16l + 16), higher bins holding larger
+// keys.  For the bin bstar holding the krem-th largest key (-1 when all bins together
+// hold fewer): the keys in the bins above it (above), those held by CTAs of rank below
+// crank (low_above), and the bin's keys held by CTAs of rank below crank (eq_lower).
+// With bstar = -1, above and low_above count every key.
+struct XPivot {
+    int bstar;
+    uint32_t above, low_above, eq_lower;
+};
+__device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int crank, uint32_t krem, int lane) {
+    uint32_t ca[16], cl[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) ca[j] = cl[j] = 0u;
+#pragma unroll 1
+    for (int c = 0; c < G; ++c) {
+        if (c == crank) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) cl[j] = ca[j];
+        }
+        const uint4* r4 = reinterpret_cast<const uint4*>(rows + static_cast<size_t>(c) * (kXBins / 2)) + 2 * lane;
+        const uint4 a = r4[0], b = r4[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            ca[2 * j] += w[j] & 0xFFFFu;
+            ca[2 * j + 1] += w[j] >> 16;
+        }
+    }
+    uint32_t t = 0u, tl = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        t += ca[j];
+        tl += cl[j];
+    }
+    uint32_t sf = t, sl = tl;  // inclusive suffix sums over lanes >= lane
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
+        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, sl, d);
+        if (lane + d < 32) {
+            sf += u;
+            sl += v;
+        }
+    }
+    XPivot r;
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, sf >= krem);
+    if (hit == 0u) {
+        r.bstar = -1;
+        r.above = __shfl_sync(0xFFFFFFFFu, sf, 0);
+        r.low_above = __shfl_sync(0xFFFFFFFFu, sl, 0);
+        r.eq_lower = 0u;
+        return r;
+    }
+    const int L = 31 - __clz(hit);
+    uint32_t acc = sf - t, lacc = sl - tl, eql = 0u;  // keys in the lanes above
+    int jb = 0;
+    bool found = false;
+#pragma unroll
+    for (int j = 15; j >= 0; --j) {
+        if (!found) {
+            if (acc + ca[j] >= krem) {
+                found = true;
+                jb = j;
+                eql = cl[j];
+            } else {
+                acc += ca[j];
+                lacc += cl[j];
+            }
+        }
+    }
+    r.bstar = 16 * L + __shfl_sync(0xFFFFFFFFu, jb, L);
+    r.above = __shfl_sync(0xFFFFFFFFu, acc, L);
+    r.low_above = __shfl_sync(0xFFFFFFFFu, lacc, L);
+    r.eq_lower = __shfl_sync(0xFFFFFFFFu, eql, L);
+    return r;
+}
+
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
 // last tail_n elements from global memory) against the compare bits tb and appends the
 // survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
@@ -428,10 +508,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         ctrl->issued[s] = use + 1;
     };
     if (!MC && !p.early) pdl_wait();
-    // chunk 0 feeds the warm-up: it goes first, the rest of the ring right behind it
-    if (tid == 0) issue(0);
-    if (lane == 0)
-        for (int q = warp == 0 ? kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
+    // The warm-up's chunks go first; the rest of the ring follows once chunk 0 has landed,
+    // so that the sample reaches every CTA early.
+    const int ww = min(min(p.ww, nq), 4);  // the warm-up tracks at most 4 chunks
+    if (tid == 0)
+        for (int q = 0; q < ww; ++q) issue(q);
     // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
     // and waits only before its CTA's first access to another CTA's memory, so the
     // cluster's CTAs meet while the first copies are in flight.
@@ -486,28 +567,49 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             }
         };
 
-        // ---- warm-up on chunk 0 (all consumer warps) ----
-        int64_t c00, ce0;
-        chunk_at(0, c00, ce0);
-        const uint32_t bytes0 = static_cast<uint32_t>(ce0 * ES) & ~15u;
-        const int nvec0 = static_cast<int>(bytes0 / 16);
-        for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while chunk 0 lands
-        const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
+        // ---- warm-up on the first ww chunks (all consumer warps) ----
+        for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while the sample lands
+        const int cvec = chunk_bytes / 16;  // vectors per full chunk
+        int nvw[4];                         // whole vectors in each sampled chunk
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            nvw[q] = 0;
+            if (q < ww) {
+                int64_t c0, ce;
+                chunk_at(q, c0, ce);
+                nvw[q] = static_cast<int>(ce * ES / 16);
+            }
+        }
+        bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
         if (tid == 0 && got0) ctrl->observed[0] = 1;
+        if (lane == 0)
+            for (int q = warp < ww ? warp + kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
+        bool gotw = got0;
+        for (int q = 1; q < ww; ++q) {
+            const bool g = wait_bounded(&ctrl->full[q], 0, ctrl);
+            if (tid == 0 && g) ctrl->observed[q] = 1;
+            gotw = gotw && g;
+        }
         {
-            // group maxima: thread t owns vectors t, t + NC, ... (VT of them) and splits
-            // them into R groups of consecutive vectors; a group's maximum is taken on the
-            // packed values (NaNs ignored) and keyed once
+            // group maxima: thread t owns vectors t, t + NC, ... of the sample (VT of them)
+            // and splits them into R groups; a group's maximum is taken on the packed values
+            // (NaNs ignored) and keyed once
             const int R = wm / 256;
-            const int VT = (p.chunk * ES / 16 + NC - 1) / NC;  // at most 4 (16 KB chunks)
-            const int vpg = VT / R > 0 ? VT / R : 1;          // vectors per group
+            const int VT = (ww * cvec + NC - 1) / NC;  // at most 4
+            const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            uint32_t vm[4];  // packed maximum of each of the thread's vectors (-inf past the chunk)
+            uint32_t vm[4];  // packed maximum of each of the thread's vectors (-inf past the sample)
             bool vv[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int v = tid + j * NC;
-                vv[j] = got0 && j < VT && v < nvec0;
+                const int q = v / cvec;
+                const int lv = v - q * cvec;
+                int nv = nvw[0];
+#pragma unroll
+                for (int t = 1; t < 4; ++t)
+                    if (q == t) nv = nvw[t];
+                vv[j] = gotw && j < VT && q < ww && lv < nv;
                 const uint4 x = vv[j] ? v0[v] : make_uint4(0u, 0u, 0u, 0u);
                 if (ES == 2) {
                     vm[j] = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
@@ -558,11 +660,34 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             cta_pivot<kBins / (kNCW * 32)>(
                 static_cast<uint32_t>(p.k), [&](int b) { return hist[b]; }, [](int) { return 0u; }, ctrl, tid, bstar,
                 above, total, unused);
-            // smallest key of the pivot bucket (0: none)
-            const uint32_t edge = total >= static_cast<uint32_t>(p.k) && bstar > 0
-                                      ? static_cast<uint32_t>(bstar) << (KW - kDigitBits)
-                                      : 0u;
-            if (tid == 0) ctrl->wedge = edge;
+            // The edge: the smallest key of the 32nd part of the pivot bucket that holds the
+            // k-th largest maximum (every CTA holds the whole union, so this needs no
+            // exchange).  At least k maxima, each an element of the row, lie at or above it.
+            uint32_t edge = 0u;
+            if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
+                constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
+                uint32_t* sub = ctrl->block_cnt[0];     // zero since start-up
+                for (int j = tid; j < G * wm; j += NC) {
+                    const uint32_t kk = wx[j];
+                    if (kk && (kk >> (KW - kDigitBits)) == static_cast<uint32_t>(bstar))
+                        atomicAdd(&sub[(kk >> SB) & 31u], 1u);
+                }
+                __syncthreads();
+                if (warp == 0) {
+                    uint32_t sfx = sub[lane];  // maxima in parts >= lane of the bucket
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, sfx, d);
+                        if (lane + d < 32) sfx += t;
+                    }
+                    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, above + sfx >= static_cast<uint32_t>(p.k));
+                    const uint32_t l = hit ? 31u - __clz(hit) : 0u;
+                    if (lane == 0)
+                        ctrl->wedge = (static_cast<uint32_t>(bstar) << (KW - kDigitBits)) | (l << SB);
+                }
+                __syncthreads();
+                edge = ctrl->wedge;
+            }
             if (edge > 0u) {
                 hasT = true;
                 T = edge - 1u;
@@ -685,6 +810,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     uint32_t* xr = reinterpret_cast<uint32_t*>(smem + L.xf);
     for (int lvl = 0;; ++lvl) {
         uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
+        if (lvl > 0) __syncthreads();  // the slot was cleared during the previous pass
         for (int i0 = 0; i0 < n; i0 += NT * 8) {  // batches of 8 keys per thread, loads issued together
             uint32_t kb[8];
 #pragma unroll
@@ -718,36 +844,21 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // ago and every peer has used it since): clear it for the next pass
         uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
         for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
-        // the cluster's histogram, and the part of it held by CTAs of lower rank
-        const uint16_t* all = reinterpret_cast<const uint16_t*>(xr + static_cast<size_t>(lvl & 1) * G * XW);
-        const auto cnt = [&](int b) {
-            uint32_t t = 0u;
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                if (c < G) t += all[c * kXBins + b];
-            return t;
-        };
-        const auto low = [&](int b) {
-            uint32_t t = 0u;
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                if (c < static_cast<int>(crank)) t += all[c * kXBins + b];
-            return t;
-        };
-        int bstar;
-        uint32_t above, total, low_above;
-        cta_pivot<kXBins / (kNCW * 32)>(krem, cnt, low, ctrl, tid, bstar, above, total, low_above);
-        gt_lower += low_above;
-        gt_all += above;
+        // the cluster's histogram; every warp finds the pivot bin on its own
+        const uint32_t* rows = xr + static_cast<size_t>(lvl & 1) * G * XW;
+        const XPivot pv = warp_pivot_x(rows, G, static_cast<int>(crank), krem, lane);
+        const int bstar = pv.bstar;
+        gt_lower += pv.low_above;
+        gt_all += pv.above;
         if (bstar < 0) {  // fewer than krem keys in play: keep them all
             take_all = true;
             break;
         }
-        krem -= above;
+        krem -= pv.above;
         if (s == 0 && bstar < kXBins - 1) {
             pivot = lbase + static_cast<uint32_t>(bstar);
-            eq_lower = low(bstar);
-            eq_mine = all[crank * kXBins + bstar];
+            eq_lower = pv.eq_lower;
+            eq_mine = reinterpret_cast<const uint16_t*>(rows)[crank * kXBins + bstar];
             break;
         }
         if (bstar < kXBins - 1) {
@@ -783,81 +894,47 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     const bool write_ok = !ctrl->abort;
     pdl_wait();  // the previous call's outputs are complete before this call writes its own
-    // Two passes over the candidates in batches of 8 per thread (thread t takes t, t + NT,
-    // ...; loads issued together): count the keys above / equal to the pivot, place the
-    // threads after each other (bit-plane prefix sums in the warp, one barrier across
-    // warps), then write.  Pivot-equal keys are taken in thread order until the quota.
+    // One pass over the candidates: each warp takes its keys above the pivot and its
+    // pivot-equal keys from two shared cursors (one atomic each per round), so slots are
+    // this CTA's range in any order; pivot-equal keys past the quota are dropped.
     const auto classify = [&](uint32_t kk, bool& isg, bool& ise) {
         const bool inr = in_play(kk);
         isg = inr && (take_all || kk > pivot);
         ise = inr && !take_all && kk == pivot;
     };
-    uint32_t ng = 0u, ne = 0u;
-    for (int i0 = 0; i0 < n; i0 += NT * 8) {
-        uint32_t kb[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = i0 + tid + j * NT;
-            kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            bool isg, ise;
-            classify(kb[j], isg, ise);
-            const bool ok = i0 + tid + j * NT < n;
-            ng += (ok && isg) ? 1u : 0u;
-            ne += (ok && ise) ? 1u : 0u;
-        }
-    }
     const uint32_t ltm = lanemask_lt();
-    uint32_t pg = 0u, pe = 0u, wg = 0u, we = 0u;  // exclusive prefixes in the warp, warp totals
-#pragma unroll
-    for (int bit = 0; bit < 16; ++bit) {  // counts stay below 2^16
-        const uint32_t bg = __ballot_sync(0xFFFFFFFFu, (ng >> bit) & 1u);
-        const uint32_t be = __ballot_sync(0xFFFFFFFFu, (ne >> bit) & 1u);
-        pg += static_cast<uint32_t>(__popc(bg & ltm)) << bit;
-        pe += static_cast<uint32_t>(__popc(be & ltm)) << bit;
-        wg += static_cast<uint32_t>(__popc(bg)) << bit;
-        we += static_cast<uint32_t>(__popc(be)) << bit;
-        if (__all_sync(0xFFFFFFFFu, (ng >> bit) <= 1u && (ne >> bit) <= 1u)) break;  // no higher bits
-    }
-    if (lane == 0) {
-        ctrl->warp_tot[1][warp] = wg;
-        ctrl->warp_tot[1][16 + warp] = we;
-    }
-    __syncthreads();
-    uint32_t g = gt_lower + pg, e = pe;
-#pragma unroll
-    for (int w = 0; w < kNCW; ++w) {
-        if (w < warp) {
-            g += ctrl->warp_tot[1][w];
-            e += ctrl->warp_tot[1][16 + w];
-        }
-    }
-    // slots are decided without branches; only the stores are predicated
     const uint32_t kslots = static_cast<uint32_t>(p.k);
     uint32_t bad = 0u;
-    for (int i0 = 0; i0 < n; i0 += NT * 8) {
-        uint32_t kb[8];
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 2 * NT) {
+        uint32_t kb[2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const int i = i0 + tid + j * NT;
             kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const int i = i0 + tid + j * NT;
-            const uint32_t kk = kb[j];
             bool isg, ise;
-            classify(kk, isg, ise);
+            classify(kb[j], isg, ise);
             isg = isg && i < n;
             ise = ise && i < n;
-            const uint32_t te = e;
-            const uint32_t slot = isg ? g : eq_first + te;
+            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, isg);
+            const uint32_t be = __ballot_sync(0xFFFFFFFFu, ise);
+            if ((bg | be) == 0u) continue;
+            uint32_t gb = 0u, eb = 0u;
+            if (lane == 0) {
+                if (bg) gb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_g), __popc(bg));
+                if (be) eb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_e), __popc(be));
+            }
+            gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
+            eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
+            const uint32_t te = eb + static_cast<uint32_t>(__popc(be & ltm));
+            const uint32_t slot = isg ? gt_lower + gb + static_cast<uint32_t>(__popc(bg & ltm)) : eq_first + te;
             const bool put = isg || (ise && te < eq_take);
-            g += isg ? 1u : 0u;
-            e += ise ? 1u : 0u;
             if (put && slot < kslots && write_ok) {
+                const uint32_t kk = kb[j];
                 const int64_t o = out.base + slot;
                 if (out.to_keys) static_cast<uint32_t*>(out.vals)[o] = kk;
                 else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));

@@ -100,6 +100,7 @@ struct ScanParams {
     int32_t parts, G, C;          // CTAs per row, CTAs per cluster, clusters per row
     int32_t chunk, stages, cap, perm_cap;
     int32_t wm;                   // split rows: warm-up group maxima per CTA
+    int32_t ww;                   // split rows: chunks sampled by the warm-up (1, 2 or 4)
     int32_t early;                // start reading x before the previous kernel completes
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
@@ -718,7 +719,7 @@ static bool dev_info(int dev, DevInfo& out) {
 }
 
 struct Plan {
-    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm;
+    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww;
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -784,16 +785,28 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.C = parts / G;
     if (opt && opt->stats && parts != 1) return DS_ERR_INVALID_ARG;
     P.wm = 0;
+    P.ww = 1;
     if (parts > 1) {
         // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
         // of the consumer warps (every stage is then used by one warp only, and a warp
         // never waits on a stage whose previous fill belongs to another warp).  Take the
         // largest chunk (halving from 16 KB, at least 1 KB) whose layout lets two CTAs
         // share an SM, 16 stages before 8; else the largest that fits one CTA.
+        // The warm-up samples the first ww chunks of each CTA (up to 4 vectors per thread,
+        // never more chunks than the CTA with the fewest has).
+        const auto warm_chunks = [&](int chunk, int stages) {
+            const int64_t per = (static_cast<int64_t>(B) + chunk - 1) / chunk;
+            const int64_t nq_min = (P.m / parts) * per;
+            const int cvec = chunk * P.es / 16;
+            int w = 1;
+            while (w * 2 <= 4 && w * 2 <= stages && w * 2 * cvec <= 4 * kNCW * 32 && w * 2 <= nq_min) w *= 2;
+            return w;
+        };
+        int ww_try = 1;
         const auto warm_groups = [&](int chunk) {
             // R group maxima per consumer thread (groups of whole vectors), enough for
             // about 4k in the cluster's union when they fit the exchange
-            const int vt = (chunk * P.es / 16 + kNCW * 32 - 1) / (kNCW * 32);
+            const int vt = (ww_try * chunk * P.es / 16 + kNCW * 32 - 1) / (kNCW * 32);
             int R = 1;
             while (R * 2 <= vt && static_cast<int64_t>(G) * 256 * R * 2 * P.es <= kWarmMaxBytes &&
                    static_cast<int64_t>(G) * 256 * R < 4 * static_cast<int64_t>(k))
@@ -802,6 +815,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         };
         const auto fit = [&](int chunk, int stages, size_t limit) -> bool {
             const int cap = static_cast<int>(align_up(static_cast<size_t>(k) + chunk, 16 / P.es));
+            ww_try = warm_chunks(chunk, stages);
             const int wm = warm_groups(chunk);
             const size_t need = split_layout(P.es, chunk, stages, cap, G, wm, k, P.perm_cap).total;
             if (need > limit) return false;
@@ -809,6 +823,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             P.stages = stages;
             P.cap = cap;
             P.wm = wm;
+            P.ww = ww_try;
             P.smem = need;
             return true;
         };
@@ -916,6 +931,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.cap = P.cap;
     sp.perm_cap = P.perm_cap;
     sp.wm = P.wm;
+    sp.ww = P.ww;
     sp.early = early ? 1 : 0;
     sp.epoch = 0;
     sp.gT = nullptr;
