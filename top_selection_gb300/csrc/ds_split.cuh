@@ -320,6 +320,15 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
 // ...); `pass` is the first pass to run and, when a reservation does not fit the buffer,
 // the pass to resume after the compaction (the function then returns false and has
 // written nothing of that pass).
+//
+// Hit masks: a compare leaves all-ones or zero per element (per 16-bit half for bf16), and
+// one and-or per compared word keeps one bit of it, so a vector costs four compares and
+// four logic ops.  bf16: word w holds vectors 4w..4w+3; bit h*16 + 4*(i%4) + q is element
+// 2q+h of vector i.  fp32: word w holds vectors 8w..8w+7; bit 4*(i%8) + q is element q.
+// Appends go in two steps: each lane writes the chunk columns of its hits into its run of
+// the reserved index slots, then the warp walks the reserved slots together (contiguous
+// accesses) to store each hit's key and its row column.  The row's tail elements take the
+// last slots.
 template <typename KeyT>
 __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint32_t col0, const char* xrow,
                                            int64_t tail_first, int tail_n, uint32_t tb, KeyT* ckey, uint32_t* cidx,
@@ -327,8 +336,8 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
     constexpr int ES = sizeof(KeyT);
     constexpr int EPV = 16 / ES;          // elements per vector
     constexpr int MW = 16 * EPV / 32;     // mask words per pass and lane
+    constexpr int VPW = 16 / MW;          // vectors per mask word
     const uint4* vec = reinterpret_cast<const uint4*>(stage);
-    const uint32_t lt = lanemask_lt();
     const int npass = nvec > 0 ? (nvec + 511) / 512 : (tail_n > 0 ? 1 : 0);
     for (; pass < npass; ++pass) {
         const int p0 = pass * 512;
@@ -340,17 +349,21 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
             const int v = p0 + lane + 32 * i;
             if (v < nvec) {
                 const uint4 x = vec[v];
-                uint32_t bits;
+                uint32_t& mw = m[i / VPW];
+                const int sh = 4 * (i % VPW);
                 if (ES == 2) {
-                    const uint32_t r0 = set_gtu_bf16x2(x.x, tb) & 0x10001u, r1 = set_gtu_bf16x2(x.y, tb) & 0x10001u;
-                    const uint32_t r2 = set_gtu_bf16x2(x.z, tb) & 0x10001u, r3 = set_gtu_bf16x2(x.w, tb) & 0x10001u;
-                    const uint32_t y = r0 | (r1 << 2) | (r2 << 4) | (r3 << 6);  // element 2q at bit 2q, 2q+1 at 2q+16
-                    bits = (y | (y >> 15)) & 0xFFu;
+                    const uint32_t c = 0x10001u << sh;
+                    mw |= set_gtu_bf16x2(x.x, tb) & c;
+                    mw |= set_gtu_bf16x2(x.y, tb) & (c << 1);
+                    mw |= set_gtu_bf16x2(x.z, tb) & (c << 2);
+                    mw |= set_gtu_bf16x2(x.w, tb) & (c << 3);
                 } else {
-                    bits = (set_gtu_f32(x.x, tb) & 1u) | (set_gtu_f32(x.y, tb) & 2u) | (set_gtu_f32(x.z, tb) & 4u) |
-                           (set_gtu_f32(x.w, tb) & 8u);
+                    const uint32_t c = 1u << sh;
+                    mw |= set_gtu_f32(x.x, tb) & c;
+                    mw |= set_gtu_f32(x.y, tb) & (c << 1);
+                    mw |= set_gtu_f32(x.z, tb) & (c << 2);
+                    mw |= set_gtu_f32(x.w, tb) & (c << 3);
                 }
-                m[(i * EPV) / 32] |= bits << ((i * EPV) % 32);
             }
         }
         // the row's last elements (fewer than 16 bytes), one per lane, in the first pass
@@ -367,17 +380,13 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
                 tkey = key_f32(h);
             }
         }
-        uint32_t c = thit ? 1u : 0u;
+        uint32_t c = 0u;
 #pragma unroll
         for (int w = 0; w < MW; ++w) c += __popc(m[w]);
-        // warp exclusive prefix of c <= 129 from its eight bit planes
-        uint32_t pre = 0u, tot = 0u;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            const uint32_t plane = __ballot_sync(0xFFFFFFFFu, (c >> b) & 1u);
-            pre += static_cast<uint32_t>(__popc(plane & lt)) << b;
-            tot += static_cast<uint32_t>(__popc(plane)) << b;
-        }
+        const uint32_t incl = warp_incl_scan(c, lane);
+        const uint32_t nbits = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const uint32_t tmask = __ballot_sync(0xFFFFFFFFu, thit);
+        const uint32_t tot = nbits + static_cast<uint32_t>(__popc(tmask));
         if (tot == 0u) continue;
         uint32_t base = 0u;
         int fits = 1;
@@ -390,26 +399,37 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
             }
         }
         if (!__shfl_sync(0xFFFFFFFFu, fits, 0)) return false;
-        uint32_t pos = __shfl_sync(0xFFFFFFFFu, base, 0) + pre;
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        // step 1: the chunk columns of this lane's hits
+        uint32_t pos = base + incl - c;
+        const int cl = (p0 + lane) * EPV;  // column of the lane's first element in the pass
 #pragma unroll
         for (int w = 0; w < MW; ++w) {
             uint32_t mm = m[w];
             while (mm) {
-                const int b = w * 32 + __ffs(mm) - 1;
+                const int bb = __ffs(mm) - 1;
                 mm &= mm - 1u;
-                const int col = (p0 + lane + 32 * (b / EPV)) * EPV + (b % EPV);  // element of the chunk
-                const uint32_t raw = ES == 2 ? reinterpret_cast<const uint16_t*>(stage)[col]
-                                             : reinterpret_cast<const uint32_t*>(stage)[col];
-                const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
-                ckey[pos] = static_cast<KeyT>(key);
-                cidx[pos] = col0 + static_cast<uint32_t>(col);
-                ++pos;
-                tmax = max(tmax, key);
+                int col;
+                if (ES == 2) col = cl + 32 * EPV * (w * VPW + ((bb & 15) >> 2)) + 2 * (bb & 3) + (bb >> 4);
+                else col = cl + 32 * EPV * (w * VPW + (bb >> 2)) + (bb & 3);
+                cidx[pos++] = static_cast<uint32_t>(col);
             }
         }
+        __syncwarp();
+        // step 2: keys and row columns, the warp's slots in order
+        for (uint32_t j = static_cast<uint32_t>(lane); j < nbits; j += 32u) {
+            const uint32_t col = cidx[base + j];
+            const uint32_t raw = ES == 2 ? reinterpret_cast<const uint16_t*>(stage)[col]
+                                         : reinterpret_cast<const uint32_t*>(stage)[col];
+            const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+            ckey[base + j] = static_cast<KeyT>(key);
+            cidx[base + j] = col0 + col;
+            tmax = max(tmax, key);
+        }
         if (thit) {
-            ckey[pos] = static_cast<KeyT>(tkey);
-            cidx[pos] = static_cast<uint32_t>(tail_first + lane);
+            const uint32_t slot = base + nbits + static_cast<uint32_t>(__popc(tmask & lanemask_lt()));
+            ckey[slot] = static_cast<KeyT>(tkey);
+            cidx[slot] = static_cast<uint32_t>(tail_first + lane);
             tmax = max(tmax, tkey);
         }
     }
@@ -660,11 +680,17 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             cta_pivot<kBins / (kNCW * 32)>(
                 static_cast<uint32_t>(p.k), [&](int b) { return hist[b]; }, [](int) { return 0u; }, ctrl, tid, bstar,
                 above, total, unused);
-            // The edge: the smallest key of the 32nd part of the pivot bucket that holds the
-            // k-th largest maximum (every CTA holds the whole union, so this needs no
-            // exchange).  At least k maxima, each an element of the row, lie at or above it.
+            // The edge: the smallest key of the pivot bucket, or (refine) of the 32nd part of
+            // it that holds the k-th largest maximum (every CTA holds the whole union, so
+            // this needs no exchange).  At least k maxima, each an element of the row, lie
+            // at or above it.
             uint32_t edge = 0u;
-            if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
+            if (!p.refine) {
+                if (total >= static_cast<uint32_t>(p.k) && bstar > 0) {
+                    edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
+                    if (tid == 0) ctrl->wedge = edge;
+                }
+            } else if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
                 constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
                 uint32_t* sub = ctrl->block_cnt[0];     // zero since start-up
                 for (int j = tid; j < G * wm; j += NC) {

@@ -101,6 +101,7 @@ struct ScanParams {
     int32_t chunk, stages, cap, perm_cap;
     int32_t wm;                   // split rows: warm-up group maxima per CTA
     int32_t ww;                   // split rows: chunks sampled by the warm-up (1, 2 or 4)
+    int32_t refine;               // split rows: the warm-up refines its pivot bucket (same for all CTAs)
     int32_t early;                // start reading x before the previous kernel completes
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
@@ -719,7 +720,7 @@ static bool dev_info(int dev, DevInfo& out) {
 }
 
 struct Plan {
-    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww;
+    int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww, refine;
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -786,6 +787,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     if (opt && opt->stats && parts != 1) return DS_ERR_INVALID_ARG;
     P.wm = 0;
     P.ww = 1;
+    P.refine = 0;
     if (parts > 1) {
         // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
         // of the consumer warps (every stage is then used by one warp only, and a warp
@@ -824,6 +826,9 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             P.cap = cap;
             P.wm = wm;
             P.ww = ww_try;
+            // Rows streamed through the ring (more chunks per CTA than stages) gain more from
+            // a tighter warm-up threshold than its extra pass costs; rows held whole do not.
+            P.refine = (P.m / parts) * ((static_cast<int64_t>(B) + chunk - 1) / chunk) > stages ? 1 : 0;
             P.smem = need;
             return true;
         };
@@ -932,6 +937,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.perm_cap = P.perm_cap;
     sp.wm = P.wm;
     sp.ww = P.ww;
+    sp.refine = P.refine;
     sp.early = early ? 1 : 0;
     sp.epoch = 0;
     sp.gT = nullptr;
