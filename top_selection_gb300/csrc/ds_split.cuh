@@ -138,103 +138,6 @@ __device__ __forceinline__ uint32_t max_word_key(uint32_t m) {
     }
 }
 
-// The bin of the k-th largest count among nbins = 8 warps x 32 x R bins, for a CTA of
-// 8 warps (R <= 16).  Warp w owns bins [w * 32R, (w + 1) * 32R) in rows of 32 (lane l
-// reads bin row * 32 + l, so the reads are conflict-free); per-warp totals meet in shared
-// memory after one barrier, and the warp whose range holds the k-th largest finds the bin
-// by suffix scans over its rows from the top.  cnt(b) gives a bin's count and low(b) a
-// second count summed over the bins above the pivot (low_above).  bstar = -1 when all
-// bins together hold fewer than k.  Ends with a CTA barrier; all threads get the results.
-template <int R, typename Cnt, typename Low>
-__device__ __forceinline__ void cta_pivot(uint32_t k, Cnt&& cnt, Low&& low, Ctrl* ctrl, int tid, int& bstar,
-                                          uint32_t& above, uint32_t& total, uint32_t& low_above) {
-    const int lane = tid & 31, warp = tid >> 5;
-    const int base = warp * 32 * R;
-    uint32_t v[R], lw[R];
-    uint32_t tw = 0u, lwt = 0u;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        v[r] = cnt(base + r * 32 + lane);
-        lw[r] = low(base + r * 32 + lane);
-        tw += v[r];
-        lwt += lw[r];
-    }
-    tw = __reduce_add_sync(0xFFFFFFFFu, tw);
-    lwt = __reduce_add_sync(0xFFFFFFFFu, lwt);
-    if (lane == 0) {
-        ctrl->warp_tot[0][warp] = tw;
-        ctrl->warp_tot[0][16 + warp] = lwt;
-    }
-    if (tid == 0) ctrl->bstar = -1;
-    __syncthreads();
-    uint32_t all = 0u, hi = 0u, lhi = 0u;  // all bins; bins and low counts of higher warps
-#pragma unroll
-    for (int w = 0; w < kNCW; ++w) {
-        const uint32_t t = ctrl->warp_tot[0][w];
-        all += t;
-        if (w > warp) {
-            hi += t;
-            lhi += ctrl->warp_tot[0][16 + w];
-        }
-    }
-    total = all;
-    if (hi < k && k <= hi + ctrl->warp_tot[0][warp]) {  // this warp's range holds the k-th largest
-        // the row: row totals (independent reductions), then a walk down from the top row
-        uint32_t rt[R], rl[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rt[r] = __reduce_add_sync(0xFFFFFFFFu, v[r]);
-            rl[r] = __reduce_add_sync(0xFFFFFFFFu, lw[r]);
-        }
-        uint32_t acc = hi, lacc = lhi, x = 0u, lx = 0u;
-        int row = 0;
-        bool found = false;
-#pragma unroll
-        for (int r = R - 1; r >= 0; --r) {
-            if (!found && acc + rt[r] >= k) {
-                found = true;
-                row = r;
-                x = v[r];
-                lx = lw[r];
-            } else if (!found) {
-                acc += rt[r];
-                lacc += rl[r];
-            }
-        }
-        // the bin within the row: suffix sums over lanes >= lane
-        uint32_t s2 = x, l2 = lx;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, s2, d);
-            const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, l2, d);
-            if (lane + d < 32) {
-                s2 += t;
-                l2 += u;
-            }
-        }
-        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, acc + s2 >= k);
-        const int l = hit ? 31 - __clz(hit) : 0;
-        const uint32_t ab = __shfl_sync(0xFFFFFFFFu, s2 - x, l);
-        const uint32_t lb = __shfl_sync(0xFFFFFFFFu, l2 - lx, l);
-        if (lane == 0 && hit) {
-            ctrl->bstar = base + row * 32 + l;
-            ctrl->above = acc + ab;
-            ctrl->bcount = lacc + lb;
-        }
-    }
-    __syncthreads();
-    bstar = ctrl->bstar;
-    above = ctrl->above;
-    low_above = ctrl->bcount;
-    if (bstar < 0) {  // fewer than k in all: every bin counts as above
-        above = total;
-        low_above = 0u;
-#pragma unroll
-        for (int w = 0; w < kNCW; ++w) low_above += ctrl->warp_tot[0][16 + w];
-    }
-    __syncthreads();  // the shared results are read before the next search writes them
-}
-
 // The pivot of a final-select pass, found by every warp on its own (no barrier).  The
 // cluster's histogram is G rows of kXBins 16-bit counts (pairs in 32-bit words), row c
 // from the CTA of rank c; lane l owns bins [16l, 16l + 16), higher bins holding larger
@@ -616,44 +519,33 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // (NaNs ignored) and keyed once
             const int R = wm / 256;
             const int VT = (ww * cvec + NC - 1) / NC;  // at most 4
-            const int vpg = VT / R > 0 ? VT / R : 1;  // vectors per group
+            const int gsh = VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0);  // log2 of vectors per group
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            uint32_t vm[4];  // packed maximum of each of the thread's vectors (-inf past the sample)
-            bool vv[4];
+            uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int v = tid + j * NC;
-                const int q = v / cvec;
-                const int lv = v - q * cvec;
-                int nv = nvw[0];
-#pragma unroll
-                for (int t = 1; t < 4; ++t)
-                    if (q == t) nv = nvw[t];
-                vv[j] = gotw && j < VT && q < ww && lv < nv;
-                const uint4 x = vv[j] ? v0[v] : make_uint4(0u, 0u, 0u, 0u);
-                if (ES == 2) {
-                    vm[j] = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
-                } else {
-                    vm[j] = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                const int q = (v >= cvec ? 1 : 0) + (v >= 2 * cvec ? 1 : 0) + (v >= 3 * cvec ? 1 : 0);
+                const int nv = q == 0 ? nvw[0] : (q == 1 ? nvw[1] : (q == 2 ? nvw[2] : nvw[3]));
+                if (gotw && j < VT && q < ww && v - q * cvec < nv) {
+                    const uint4 x = v0[v];
+                    uint32_t m;
+                    if (ES == 2) {
+                        m = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
+                    } else {
+                        m = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
                                                   fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                if (r < R) {
-                    uint32_t m = ES == 2 ? 0xFF80FF80u : 0xFF800000u;  // -inf
-                    bool any = false;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        if (j >= r * vpg && j < (r + 1) * vpg && vv[j]) {
-                            m = ES == 2 ? max_bf16x2(m, vm[j])
-                                        : __float_as_uint(fmaxf(__uint_as_float(m), __uint_as_float(vm[j])));
-                            any = true;
-                        }
                     }
-                    wx[crank * wm + tid * R + r] = static_cast<KeyT>(any ? max_word_key<KeyT>(m) : 0u);
+                    const uint32_t kk = max_word_key<KeyT>(m);  // keys keep the value order
+                    const int g = j >> gsh;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        if (g == r) gk[r] = max(gk[r], kk);
                 }
             }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (r < R) wx[crank * wm + tid * R + r] = static_cast<KeyT>(gk[r]);
             fence_proxy_async_smem();
             named_bar_sync(1, NC);
             if (G > 1) {
@@ -675,11 +567,55 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
             }
             __syncthreads();
-            int bstar;
-            uint32_t above, total, unused;
-            cta_pivot<kBins / (kNCW * 32)>(
-                static_cast<uint32_t>(p.k), [&](int b) { return hist[b]; }, [](int) { return 0u; }, ctrl, tid, bstar,
-                above, total, unused);
+            // the bucket of the k-th largest, found by warp 0: lane l sums buckets
+            // [64l, 64l + 64), then the lanes split the chosen lane's buckets in pairs
+            if (warp == 0) {
+                const uint32_t kk = static_cast<uint32_t>(p.k);
+                const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 16 * lane;
+                uint32_t t = 0u;
+#pragma unroll 4
+                for (int j = 0; j < 16; ++j) {
+                    const uint4 x = h4[(j + lane) & 15];  // rotated: fewer bank conflicts
+                    t += x.x + x.y + x.z + x.w;
+                }
+                uint32_t sf = t;  // buckets of lanes >= lane
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
+                    if (lane + d < 32) sf += u;
+                }
+                const uint32_t tot = __shfl_sync(0xFFFFFFFFu, sf, 0);
+                const uint32_t hit = __ballot_sync(0xFFFFFFFFu, sf >= kk);
+                int bs = -1;
+                uint32_t ab = tot;
+                if (hit) {
+                    const int L = 31 - __clz(hit);
+                    const uint32_t aboveL = __shfl_sync(0xFFFFFFFFu, sf - t, L);
+                    const uint2 c2 = reinterpret_cast<const uint2*>(hist)[32 * L + lane];
+                    const uint32_t c = c2.x + c2.y;
+                    uint32_t s2 = c;
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, s2, d);
+                        if (lane + d < 32) s2 += u;
+                    }
+                    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, aboveL + s2 >= kk);
+                    const int J = 31 - __clz(hit2);
+                    const uint32_t aJ = __shfl_sync(0xFFFFFFFFu, aboveL + s2 - c, J);
+                    const uint32_t hiJ = __shfl_sync(0xFFFFFFFFu, c2.y, J);
+                    const bool top = aJ + hiJ >= kk;
+                    bs = 64 * L + 2 * J + (top ? 1 : 0);
+                    ab = top ? aJ : aJ + hiJ;
+                }
+                if (lane == 0) {
+                    ctrl->bstar = bs;
+                    ctrl->above = ab;
+                    ctrl->bcount = tot;
+                }
+            }
+            __syncthreads();
+            const int bstar = ctrl->bstar;
+            const uint32_t above = ctrl->above, total = ctrl->bcount;
             // The edge: the smallest key of the pivot bucket, or (refine) of the 32nd part of
             // it that holds the k-th largest maximum (every CTA holds the whole union, so
             // this needs no exchange).  At least k maxima, each an element of the row, lie
