@@ -217,6 +217,16 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
     return r;
 }
 
+// Counts a key in the final select's first histogram (kXBins 16-bit counts in pairs):
+// keys from `edge` up, in bins of 2^s keys, the last bin open-ended.
+__device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t edge, int s) {
+    if (key >= edge) {
+        uint32_t d = (key - edge) >> s;
+        d = d < kXBins - 1 ? d : kXBins - 1;
+        atomicAdd(&xh[d >> 1], 1u << ((d & 1u) * 16u));
+    }
+}
+
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
 // last tail_n elements from global memory) against the compare bits tb and appends the
 // survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
@@ -235,7 +245,8 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
 template <typename KeyT>
 __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint32_t col0, const char* xrow,
                                            int64_t tail_first, int tail_n, uint32_t tb, KeyT* ckey, uint32_t* cidx,
-                                           Ctrl* ctrl, uint32_t cap, int lane, int& pass, uint32_t& tmax) {
+                                           Ctrl* ctrl, uint32_t cap, int lane, int& pass, uint32_t& tmax,
+                                           uint32_t* xh, uint32_t hedge, int hs) {
     constexpr int ES = sizeof(KeyT);
     constexpr int EPV = 16 / ES;          // elements per vector
     constexpr int MW = 16 * EPV / 32;     // mask words per pass and lane
@@ -328,12 +339,14 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
             ckey[base + j] = static_cast<KeyT>(key);
             cidx[base + j] = col0 + col;
             tmax = max(tmax, key);
+            xhist_add(xh, key, hedge, hs);
         }
         if (thit) {
             const uint32_t slot = base + nbits + static_cast<uint32_t>(__popc(tmask & lanemask_lt()));
             ckey[slot] = static_cast<KeyT>(tkey);
             cidx[slot] = static_cast<uint32_t>(tail_first + lane);
             tmax = max(tmax, tkey);
+            xhist_add(xh, tkey, hedge, hs);
         }
     }
     return true;
@@ -446,6 +459,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         uint32_t T = 0u;
         uint32_t tmax = 0u;
         uint32_t gnext = 0u;  // other clusters' threshold, loaded one chunk ahead
+        // The final select's first histogram (this CTA's slot of its first exchange round)
+        // is counted as keys are appended: keys from the warm-up's edge up, in bins of
+        // 2^hs0 keys (set once the edge is known).
+        uint32_t* const xh0 = reinterpret_cast<uint32_t*>(smem + L.xf) + static_cast<size_t>(crank) * (kXBins / 2);
+        uint32_t hedge = 0u;
+        int hs0 = KW - kXBits;
         // every consumer warp calls this together (from its chunk loop or the drain)
         const auto join_compaction = [&]() {
             named_bar_sync(2, NC);
@@ -464,6 +483,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             T = hasT && T > piv ? T : piv;
             hasT = true;
             if (tid == 0) publish_T(T);
+            // the first final histogram, counted anew over the k keys kept
+            for (int i = tid; i < kXBins / 2; i += NC) xh0[i] = 0u;
+            named_bar_sync(2, NC);
+            for (int i = tid; i < p.k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
         };
         // A warp waiting for its next chunk joins any compaction requested meanwhile, so
         // the requesting warp does not wait for this chunk to land.  Decisions are
@@ -653,6 +676,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             if (edge > 0u) {
                 hasT = true;
                 T = edge - 1u;
+                hedge = edge;
+                hs0 = ES == 2 ? 0 : 23 - kXBits;
             }
             if (tid == 0 && hasT && (G > 1 || MC)) publish_T(T);
         }
@@ -694,7 +719,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 int pass = 0;
                 while (!warp_chunk<KeyT>(ring + static_cast<size_t>(s) * chunk_bytes, nvec, static_cast<uint32_t>(c0),
                                          xrow, c0 + bytes / ES, tail, compare_bits<KeyT>(have, tk), ckey, cidx, ctrl,
-                                         cap, lane, pass, tmax)) {
+                                         cap, lane, pass, tmax, xh0, hedge, hs0)) {
                     join_compaction();
                     if (!have || T > tk) {
                         tk = T;
@@ -767,23 +792,16 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     uint32_t pivot = 0u;
     bool take_all = false;
     // two rounds of G histograms of kXBins uint16 counts, as pairs in 32-bit words; this
-    // CTA's slot of round 0 was cleared at start-up
+    // CTA's slot of round 0 holds the first pass's counts, made as keys were appended
     constexpr int XW = kXBins / 2;
     uint32_t* xr = reinterpret_cast<uint32_t*>(smem + L.xf);
     for (int lvl = 0;; ++lvl) {
         uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
-        if (lvl > 0) __syncthreads();  // the slot was cleared during the previous pass
-        for (int i0 = 0; i0 < n; i0 += NT * 8) {  // batches of 8 keys per thread, loads issued together
-            uint32_t kb[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int i = i0 + tid + j * NT;
-                kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t kk = kb[j];
-                if (i0 + tid + j * NT < n && in_play(kk) && kk >= lbase && kk <= lhi) {
+        if (lvl > 0) {  // (the slot was cleared before the previous pass's last barrier)
+#pragma unroll 4
+            for (int i = tid; i < n; i += NT) {
+                const uint32_t kk = ckey[i];
+                if (in_play(kk) && kk >= lbase && kk <= lhi) {
                     uint32_t d = (kk - lbase) >> s;
                     d = d < kXBins - 1 ? d : kXBins - 1;
                     atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
@@ -806,9 +824,23 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // ago and every peer has used it since): clear it for the next pass
         uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
         for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
-        // the cluster's histogram; every warp finds the pivot bin on its own
+        // the cluster's histogram: warp 0 finds the pivot bin, the CTA reads it after a barrier
         const uint32_t* rows = xr + static_cast<size_t>(lvl & 1) * G * XW;
-        const XPivot pv = warp_pivot_x(rows, G, static_cast<int>(crank), krem, lane);
+        if (warp == 0) {
+            const XPivot w0 = warp_pivot_x(rows, G, static_cast<int>(crank), krem, lane);
+            if (lane == 0) {
+                ctrl->fp_tot[0] = static_cast<uint32_t>(w0.bstar);
+                ctrl->fp_tot[1] = w0.above;
+                ctrl->fp_tot[2] = w0.low_above;
+                ctrl->fp_tot[3] = w0.eq_lower;
+            }
+        }
+        __syncthreads();
+        XPivot pv;
+        pv.bstar = static_cast<int>(ctrl->fp_tot[0]);
+        pv.above = ctrl->fp_tot[1];
+        pv.low_above = ctrl->fp_tot[2];
+        pv.eq_lower = ctrl->fp_tot[3];
         const int bstar = pv.bstar;
         gt_lower += pv.low_above;
         gt_all += pv.above;
