@@ -153,7 +153,7 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
     uint32_t ca[16], cl[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) ca[j] = cl[j] = 0u;
-#pragma unroll 1
+#pragma unroll 4
     for (int c = 0; c < G; ++c) {
         if (c == crank) {
 #pragma unroll
@@ -888,9 +888,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     const bool write_ok = !ctrl->abort;
     pdl_wait();  // the previous call's outputs are complete before this call writes its own
-    // One pass over the candidates: each warp takes its keys above the pivot and its
-    // pivot-equal keys from two shared cursors (one atomic each per round), so slots are
-    // this CTA's range in any order; pivot-equal keys past the quota are dropped.
+    // One pass over the candidates, four per thread at a time: each warp takes slots for
+    // its keys above the pivot and its pivot-equal keys from two shared cursors (one
+    // atomic each per batch), so slots are this CTA's range in any order; pivot-equal keys
+    // past the quota are dropped.
     const auto classify = [&](uint32_t kk, bool& isg, bool& ise) {
         const bool inr = in_play(kk);
         isg = inr && (take_all || kk > pivot);
@@ -900,32 +901,38 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     const uint32_t kslots = static_cast<uint32_t>(p.k);
     uint32_t bad = 0u;
 #pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 2 * NT) {
-        uint32_t kb[2];
+    for (int i0 = 0; i0 < n; i0 += 4 * NT) {
+        uint32_t kb[4], ib[4], bg[4], be[4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 4; ++j) {
             const int i = i0 + tid + j * NT;
             kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
+            ib[j] = i < n ? cidx[i] : 0u;
         }
+        uint32_t sg = 0u, se = 0u;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int i = i0 + tid + j * NT;
+        for (int j = 0; j < 4; ++j) {
             bool isg, ise;
             classify(kb[j], isg, ise);
-            isg = isg && i < n;
-            ise = ise && i < n;
-            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, isg);
-            const uint32_t be = __ballot_sync(0xFFFFFFFFu, ise);
-            if ((bg | be) == 0u) continue;
-            uint32_t gb = 0u, eb = 0u;
-            if (lane == 0) {
-                if (bg) gb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_g), __popc(bg));
-                if (be) eb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_e), __popc(be));
-            }
-            gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
-            eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
-            const uint32_t te = eb + static_cast<uint32_t>(__popc(be & ltm));
-            const uint32_t slot = isg ? gt_lower + gb + static_cast<uint32_t>(__popc(bg & ltm)) : eq_first + te;
+            const bool ok = i0 + tid + j * NT < n;
+            bg[j] = __ballot_sync(0xFFFFFFFFu, isg && ok);
+            be[j] = __ballot_sync(0xFFFFFFFFu, ise && ok);
+            sg += static_cast<uint32_t>(__popc(bg[j]));
+            se += static_cast<uint32_t>(__popc(be[j]));
+        }
+        if ((sg | se) == 0u) continue;
+        uint32_t gb = 0u, eb = 0u;
+        if (lane == 0) {
+            if (sg) gb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_g), sg);
+            if (se) eb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_e), se);
+        }
+        gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
+        eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool isg = (bg[j] >> lane) & 1u, ise = (be[j] >> lane) & 1u;
+            const uint32_t te = eb + static_cast<uint32_t>(__popc(be[j] & ltm));
+            const uint32_t slot = isg ? gt_lower + gb + static_cast<uint32_t>(__popc(bg[j] & ltm)) : eq_first + te;
             const bool put = isg || (ise && te < eq_take);
             if (put && slot < kslots && write_ok) {
                 const uint32_t kk = kb[j];
@@ -933,9 +940,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 if (out.to_keys) static_cast<uint32_t*>(out.vals)[o] = kk;
                 else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
                 else static_cast<uint32_t*>(out.vals)[o] = unkey_f32(kk);
-                out.idx[o] = static_cast<int32_t>(cidx[i]);
+                out.idx[o] = static_cast<int32_t>(ib[j]);
             }
             bad |= (put && slot >= kslots) ? 1u : 0u;
+            gb += static_cast<uint32_t>(__popc(bg[j]));
+            eb += static_cast<uint32_t>(__popc(be[j]));
         }
     }
     if (bad) set_status(kErrInternal);
