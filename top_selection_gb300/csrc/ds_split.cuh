@@ -414,13 +414,15 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
 
-    // chunk slot q: block perm[q / cpb], sub-chunk q % cpb (empty past the row's end)
-    const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) {
-        const int64_t lo = static_cast<int64_t>(perm[q / cpb]) * p.B;
+    // chunk slot q: block perm[bi] with bi = q / cpb, sub-chunk q % cpb (empty past the
+    // row's end); the chunk loop steps (bi, sub) without dividing
+    const auto chunk_of = [&](int bi, int sub, int64_t& c0, int64_t& ce) {
+        const int64_t lo = static_cast<int64_t>(perm[bi]) * p.B;
         const int64_t hi = lo + p.B < p.N ? lo + p.B : p.N;
-        c0 = lo + static_cast<int64_t>(q % cpb) * p.chunk;
+        c0 = lo + static_cast<int64_t>(sub) * p.chunk;
         ce = c0 < hi ? ((hi - c0) < p.chunk ? (hi - c0) : p.chunk) : 0;
     };
+    const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) { chunk_of(q / cpb, q % cpb, c0, ce); };
     const auto publish_T = [&](uint32_t t) {
         for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
         if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
@@ -430,11 +432,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     // consumes every chunk that lands there and refills the stage itself once it is done
     // with it, so no warp ever waits on another warp's stage.
     const uint64_t pol = policy_evict_first();
-    const auto issue = [&](int q) {
+    const auto issue_to = [&](int s, int use, int bi, int sub) {
         int64_t c0, ce;
-        chunk_at(q, c0, ce);
+        chunk_of(bi, sub, c0, ce);
         const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
-        const int s = q % p.stages, use = q / p.stages;
         if (bytes) {
             mbar_arrive_expect_tx(&ctrl->full[s], bytes);
             bulk_g2s(ring + static_cast<size_t>(s) * chunk_bytes, xrow + c0 * ES, bytes, &ctrl->full[s], pol);
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
         ctrl->issued[s] = use + 1;
     };
+    const auto issue = [&](int q) { issue_to(q % p.stages, q / p.stages, q / cpb, q % cpb); };
     if (!MC && !p.early) pdl_wait();
     // The warm-up's chunks go first; the rest of the ring follows once chunk 0 has landed,
     // so that the sample reaches every CTA early.
@@ -683,6 +685,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
 
         // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
+        // this warp's chunk q: ring stage s = q % stages and use q / stages, block index bi
+        // and sub-chunk sub, stepped by kNCW chunks per round
+        int st = warp, use = 0, bi = warp / cpb, sub = warp % cpb;
+        const int d8 = kNCW / cpb, r8 = kNCW % cpb;            // kNCW chunks ahead
+        const int dS = p.stages / cpb, rS = p.stages % cpb;    // one ring ahead
         for (int q = warp; q < nq; q += kNCW) {
             int req = 0;
             if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
@@ -704,9 +711,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 }
             }
             int64_t c0, ce;
-            chunk_at(q, c0, ce);
+            chunk_of(bi, sub, c0, ce);
             const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
-            const int s = q % p.stages, use = q / p.stages;
+            const int s = st;
             const bool got = wait_data(&ctrl->full[s], use & 1);
             if (lane == 0 && got) ctrl->observed[s] = use + 1;
             if (hasT && (!have || T > tk)) {  // a compaction ran while the warp waited
@@ -731,8 +738,25 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 }
             }
             __syncwarp();  // every lane is done with the stage: refill it with this warp's next chunk there
-            if (lane == 0 && got && q + p.stages < nq && !*reinterpret_cast<volatile int*>(&ctrl->abort))
-                issue(q + p.stages);
+            if (lane == 0 && got && q + p.stages < nq && !*reinterpret_cast<volatile int*>(&ctrl->abort)) {
+                int bj = bi + dS, sj = sub + rS;
+                if (sj >= cpb) {
+                    sj -= cpb;
+                    ++bj;
+                }
+                issue_to(s, use + 1, bj, sj);
+            }
+            bi += d8;
+            sub += r8;
+            if (sub >= cpb) {
+                sub -= cpb;
+                ++bi;
+            }
+            st += kNCW;
+            if (st >= p.stages) {
+                st -= p.stages;
+                ++use;
+            }
         }
         // A warp out of chunks still joins compactions other warps request: it reads the
         // count of finished warps before the request flag, so a request raised by the
