@@ -371,17 +371,30 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t cta = blockIdx.x;
-    const int64_t row = cta / p.parts;
-    const int part = static_cast<int>(cta % p.parts);
+    const int cta = static_cast<int>(blockIdx.x);
+    const int rowi = cta / p.parts;
+    const int64_t row = rowi;
+    const int part = cta - rowi * p.parts;
     const int cl = part / G;
     const uint32_t crank = G > 1 ? cluster_ctarank() : 0u;
-    const int64_t b0 = static_cast<int64_t>(part) * p.m / p.parts;
-    const int64_t b1 = static_cast<int64_t>(part + 1) * p.m / p.parts;
-    const int mp = static_cast<int>(b1 - b0);
+    // this part's blocks: parts [0, mr) take mq + 1 blocks, the others mq
+    const int64_t b0 = static_cast<int64_t>(part) * p.mq + (part < p.mr ? part : p.mr);
+    const int mp = static_cast<int>(p.mq) + (part < p.mr ? 1 : 0);
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
-    const int cpb = (p.B + p.chunk - 1) / p.chunk;  // chunk slots per block
+    const int cpb = p.cpb;  // chunk slots per block
+    // q / cpb and q % cpb for small q, through the reciprocal and one correction
+    const auto qdiv = [&](int q, int& bi, int& sub) {
+        bi = __float2int_rz(static_cast<float>(q) * p.cpb_rcp);
+        sub = q - bi * cpb;
+        if (sub < 0) {
+            --bi;
+            sub += cpb;
+        } else if (sub >= cpb) {
+            ++bi;
+            sub -= cpb;
+        }
+    };
     const int nq = mp * cpb;
     const bool MC = p.C > 1;
     const uint32_t cap = static_cast<uint32_t>(p.cap);
@@ -422,7 +435,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         c0 = lo + static_cast<int64_t>(sub) * p.chunk;
         ce = c0 < hi ? ((hi - c0) < p.chunk ? (hi - c0) : p.chunk) : 0;
     };
-    const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) { chunk_of(q / cpb, q % cpb, c0, ce); };
+    const auto chunk_at = [&](int q, int64_t& c0, int64_t& ce) {
+        int bi, sub;
+        qdiv(q, bi, sub);
+        chunk_of(bi, sub, c0, ce);
+    };
     const auto publish_T = [&](uint32_t t) {
         for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
         if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
@@ -444,7 +461,11 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
         ctrl->issued[s] = use + 1;
     };
-    const auto issue = [&](int q) { issue_to(q % p.stages, q / p.stages, q / cpb, q % cpb); };
+    const auto issue = [&](int q) {
+        int bi, sub;
+        qdiv(q, bi, sub);
+        issue_to(q & (p.stages - 1), q >> p.slog, bi, sub);
+    };
     if (!MC && !p.early) pdl_wait();
     // The warm-up's chunks go first; the rest of the ring follows once chunk 0 has landed,
     // so that the sample reaches every CTA early.
@@ -687,9 +708,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
         // this warp's chunk q: ring stage s = q % stages and use q / stages, block index bi
         // and sub-chunk sub, stepped by kNCW chunks per round
-        int st = warp, use = 0, bi = warp / cpb, sub = warp % cpb;
-        const int d8 = kNCW / cpb, r8 = kNCW % cpb;            // kNCW chunks ahead
-        const int dS = p.stages / cpb, rS = p.stages % cpb;    // one ring ahead
+        int st = warp, use = 0, bi, sub, d8, r8, dS, rS;
+        qdiv(warp, bi, sub);
+        qdiv(kNCW, d8, r8);      // kNCW chunks ahead
+        qdiv(p.stages, dS, rS);  // one ring ahead
         for (int q = warp; q < nq; q += kNCW) {
             int req = 0;
             if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
@@ -961,9 +983,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             if (put && slot < kslots && write_ok) {
                 const uint32_t kk = kb[j];
                 const int64_t o = out.base + slot;
-                if (out.to_keys) static_cast<uint32_t*>(out.vals)[o] = kk;
-                else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
-                else static_cast<uint32_t*>(out.vals)[o] = unkey_f32(kk);
+                if (ES == 2 && !out.to_keys) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
+                else static_cast<uint32_t*>(out.vals)[o] = out.to_keys ? kk : unkey_f32(kk);
                 out.idx[o] = static_cast<int32_t>(ib[j]);
             }
             bad |= (put && slot >= kslots) ? 1u : 0u;

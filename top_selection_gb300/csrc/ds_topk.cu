@@ -102,6 +102,11 @@ struct ScanParams {
     int32_t wm;                   // split rows: warm-up group maxima per CTA
     int32_t ww;                   // split rows: chunks sampled by the warm-up (1, 2 or 4)
     int32_t refine;               // split rows: the warm-up refines its pivot bucket (same for all CTAs)
+    int32_t cpb;                  // split rows: chunk slots per block, ceil(B / chunk)
+    float cpb_rcp;                //   1 / cpb (with a correction step: exact quotients of small ints)
+    int32_t slog;                 //   log2 of the ring depth (8 or 16 stages)
+    int32_t mr;                   //   m % parts: parts [0, mr) get mq + 1 blocks, the rest mq
+    int64_t mq;                   //   m / parts
     int32_t early;                // start reading x before the previous kernel completes
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
@@ -938,6 +943,11 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.wm = P.wm;
     sp.ww = P.ww;
     sp.refine = P.refine;
+    sp.cpb = static_cast<int32_t>((B + P.chunk - 1) / P.chunk);
+    sp.cpb_rcp = 1.0f / static_cast<float>(sp.cpb);
+    sp.slog = P.stages >= 16 ? 4 : 3;
+    sp.mq = P.m / P.parts;
+    sp.mr = static_cast<int32_t>(P.m % P.parts);
     sp.early = early ? 1 : 0;
     sp.epoch = 0;
     sp.gT = nullptr;
