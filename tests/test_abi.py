@@ -94,3 +94,38 @@ def test_fp32_alignment_rules(lib):
     assert ds.ds_topk(P, 1, 2, 100, 102, 4, 8, 8, 0, P, P, 0) == 2
     assert ds.ds_topk(P, 1, 1, 100, 100, 4, 10, 8, 0, P, P, 0) == 3
     assert ds.ds_topk(P, 1, 0, 100, 100, 4, 8, 8, 0, P, P, 0) == 0
+
+
+_PLAN_SCRIPT = r"""
+import json, top_selection_gb300 as ds
+ds.load()
+shapes = {"indexer": (0, 64, 131072, 512, 4096, 4096), "sampler": (1, 256, 129280, 512, 8192, 4096),
+          "sampler_k4096": (1, 256, 129280, 4096, 8192, 4096), "longctx": (0, 4, 1048576, 512, 4096, 4096),
+          "row65536": (1, 1, 65536, 512, 1024, 1024), "huge": (1, 1, 268435456, 32, 8192, 4096)}
+print(json.dumps({n: ds.ds_get_plan(*a) for n, a in shapes.items()}))
+"""
+
+
+def test_plans_on_a_described_device(lib):
+    """The planner's choices for the workload shapes, on a described 152-SM part with
+    228 KB of shared memory per SM (no GPU needed): rows under 16 MB stay in one cluster
+    (no merge pass), huge rows spread over clusters, one-CTA rows where k is large."""
+    import json
+    import sys
+    env = dict(os.environ, DS_PLAN_DEVICE="152,232448,233472", CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", _PLAN_SCRIPT], env=env, cwd=ROOT, capture_output=True,
+                         text=True, check=True).stdout
+    plans = json.loads(out.strip().splitlines()[-1])
+    def pc(n):
+        return plans[n]["parts"], plans[n]["cluster"], plans[n]["merge_launch"]
+    assert pc("indexer") == (4, 4, 0)
+    assert pc("sampler") == (2, 2, 0)
+    assert pc("sampler_k4096") == (1, 1, 0)
+    assert pc("longctx") == (16, 16, 0)
+    assert pc("row65536") == (8, 8, 0)
+    assert pc("huge") == (256, 8, 1)
+    for n, p in plans.items():
+        assert p["smem_bytes"] <= 232448, n
+        if p["parts"] > 1:
+            assert p["stages"] in (8, 16), n          # warp-owned stages
+            assert p["ctas_per_sm"] == 2, n

@@ -29,6 +29,8 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "ds_common.cuh"
@@ -713,11 +715,17 @@ static bool dev_info(int dev, DevInfo& out) {
     std::lock_guard<std::mutex> lk(g_mu);
     DevInfo& d = g_dev[dev];
     if (!d.ok) {
-        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-            return false;
-        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
-            return false;
+        bool ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess;
+        if (!ok) {
+            // Planning queries without a device (host tests): DS_PLAN_DEVICE="sms,smem_optin,smem_per_sm"
+            // describes one.  Launches still need the real device.
+            const char* e = std::getenv("DS_PLAN_DEVICE");
+            if (!e || std::sscanf(e, "%d,%d,%d", &d.sms, &d.smem_optin, &d.smem_per_sm) != 3 || d.sms < 1)
+                return false;
+            cudaGetLastError();
+        }
         d.ok = true;
     }
     out = d;
@@ -760,14 +768,21 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     int parts = opt ? opt->parts : 0;
     if (parts < 0) return DS_ERR_INVALID_ARG;
     if (parts == 0 && opt && opt->stats) parts = 1;  // the statistics describe the one-CTA schedule
+    const bool spread = N * P.es >= (int64_t(16) << 20);
     if (parts == 0) {
         // Enough CTAs to cover the SMs: rows split in parts of at least 4 blocks.  Rows that
         // already cover the SMs still go in halves when k is small against a chunk (the
         // split-row kernel keeps k + one chunk of candidates and runs two CTAs per SM,
         // where a whole row's CTA needs k + B + B2 and runs alone).
+        // Rows under 16 MB stay in one cluster (at most 16 CTAs: no merge pass) and are not
+        // split so finely that a warp would get no chunk; larger rows spread over several
+        // clusters and a merge kernel.
         parts = 1;
         const int64_t maxp = P.m / 4 > 1 ? P.m / 4 : 1;
-        while (rows * parts < di.sms && parts * 2 <= maxp && parts < 256) parts *= 2;
+        const int64_t fillp = N / (static_cast<int64_t>(P.chunk) * kNCW);
+        const int64_t capp = spread ? 256 : 16;
+        while (rows * parts < di.sms && parts * 2 <= maxp && parts * 2 <= capp && (spread || parts * 2 <= fillp))
+            parts *= 2;
         if (parts == 1 && maxp >= 2 && static_cast<int64_t>(k) * 4 <= P.chunk) parts = 2;
         while ((P.m + parts - 1) / parts > kPermMax) parts *= 2;
         if (parts > P.m) return DS_ERR_UNSUPPORTED;
@@ -783,8 +798,10 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     int G = opt ? opt->cluster : 0;
     if (G < 0 || G > 16) return DS_ERR_INVALID_ARG;
     if (G == 0) {
+        // one cluster per row when a row has at most 16 parts and no more than 16 MB
         G = 1;
-        while (G * 2 <= 8 && parts % (G * 2) == 0) G *= 2;
+        const int gmax = (!spread && parts <= 16) ? 16 : 8;
+        while (G * 2 <= gmax && parts % (G * 2) == 0) G *= 2;
     }
     if (parts % G != 0) return DS_ERR_INVALID_ARG;
     P.G = G;
@@ -1059,7 +1076,11 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
     const int es = dtype == DS_BF16 ? 2 : 4;
     if (k > kMaxK || N >= (int64_t(1) << 31) || (static_cast<int64_t>(B) * es) % 16 != 0) return DS_ERR_UNSUPPORTED;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) {  // no device: only a described one (DS_PLAN_DEVICE) plans
+        cudaGetLastError();
+        if (!std::getenv("DS_PLAN_DEVICE")) return DS_ERR_CUDA;
+        dev = 0;
+    }
     Plan P;
     const ds_status st = make_plan(dev, dtype, rows, N, k, B, B2, options, P);
     if (st != DS_OK) return st;
