@@ -138,6 +138,42 @@ __device__ __forceinline__ uint32_t max_word_key(uint32_t m) {
     }
 }
 
+// Warm-up group maxima of one thread: its vectors t, t + NC, ... (VT <= NV of them) of
+// the ww sampled chunks (cvec vectors each; nvw[q] whole vectors in chunk q), in groups
+// of 2^gsh vectors; gk[g] is the key of group g's largest value (0: none).  NV is 4 or 8
+// so that small samples run the short loop.
+template <typename KeyT, int NV>
+__device__ __forceinline__ void warm_maxima(const uint4* v0, int tid, int cvec, int ww, int VT, int gsh, bool gotw,
+                                            const int (&nvw)[8], uint32_t (&gk)[4]) {
+    constexpr int ES = sizeof(KeyT);
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int v = tid + j * kSplitThreads;
+        int q = 0;
+#pragma unroll
+        for (int t = 1; t < NV; ++t) q += v >= t * cvec ? 1 : 0;
+        int nv = nvw[0];
+#pragma unroll
+        for (int t = 1; t < NV; ++t)
+            if (q == t) nv = nvw[t];
+        if (gotw && j < VT && q < ww && v - q * cvec < nv) {
+            const uint4 x = v0[v];
+            uint32_t m;
+            if (ES == 2) {
+                m = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
+            } else {
+                m = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                          fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
+            }
+            const uint32_t kk = max_word_key<KeyT>(m);  // keys keep the value order
+            const int g = j >> gsh;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (g == r) gk[r] = max(gk[r], kk);
+        }
+    }
+}
+
 // The pivot of a final-select pass, found by every warp on its own (no barrier).  The
 // cluster's histogram is G rows of kXBins 16-bit counts (pairs in 32-bit words), row c
 // from the CTA of rank c; lane l owns bins [16l, 16l + 16), higher bins holding larger
@@ -469,7 +505,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     if (!MC && !p.early) pdl_wait();
     // The warm-up's chunks go first; the rest of the ring follows once chunk 0 has landed,
     // so that the sample reaches every CTA early.
-    const int ww = min(min(p.ww, nq), 4);  // the warm-up tracks at most 4 chunks
+    const int ww = min(min(p.ww, nq), 8);  // the warm-up tracks at most 8 chunks
     if (tid == 0)
         for (int q = 0; q < ww; ++q) issue(q);
     // Cluster-wide start: every thread arrives now (its CTA's barriers are initialised)
@@ -539,9 +575,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // ---- warm-up on the first ww chunks (all consumer warps) ----
         for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while the sample lands
         const int cvec = chunk_bytes / 16;  // vectors per full chunk
-        int nvw[4];                         // whole vectors in each sampled chunk
+        int nvw[8];                         // whole vectors in each sampled chunk
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 8; ++q) {
             nvw[q] = 0;
             if (q < ww) {
                 int64_t c0, ce;
@@ -564,31 +600,13 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // and splits them into R groups; a group's maximum is taken on the packed values
             // (NaNs ignored) and keyed once
             const int R = wm / 256;
-            const int VT = (ww * cvec + NC - 1) / NC;  // at most 4
-            const int gsh = VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0);  // log2 of vectors per group
+            const int VT = (ww * cvec + NC - 1) / NC;  // at most 8
+            // log2 of vectors per group
+            const int gsh = VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
             uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int v = tid + j * NC;
-                const int q = (v >= cvec ? 1 : 0) + (v >= 2 * cvec ? 1 : 0) + (v >= 3 * cvec ? 1 : 0);
-                const int nv = q == 0 ? nvw[0] : (q == 1 ? nvw[1] : (q == 2 ? nvw[2] : nvw[3]));
-                if (gotw && j < VT && q < ww && v - q * cvec < nv) {
-                    const uint4 x = v0[v];
-                    uint32_t m;
-                    if (ES == 2) {
-                        m = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
-                    } else {
-                        m = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
-                                                  fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
-                    }
-                    const uint32_t kk = max_word_key<KeyT>(m);  // keys keep the value order
-                    const int g = j >> gsh;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r)
-                        if (g == r) gk[r] = max(gk[r], kk);
-                }
-            }
+            if (VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+            else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
                 if (r < R) wx[crank * wm + tid * R + r] = static_cast<KeyT>(gk[r]);
