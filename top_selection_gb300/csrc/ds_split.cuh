@@ -388,6 +388,70 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
     return true;
 }
 
+// The final select's output: one pass over this CTA's n candidates, four per thread at
+// a time.  Each warp takes slots for its keys above the pivot and its pivot-equal keys
+// from two shared cursors (one atomic each per batch), so slots are this CTA's range in
+// any order; pivot-equal keys past the quota are dropped.  TK: write keys (partial
+// results of rows over several clusters) instead of values.  Returns nonzero when a slot
+// fell outside the row's k.
+template <typename KeyT, bool TK>
+__device__ __forceinline__ uint32_t split_output(const KeyT* ckey, const uint32_t* cidx, int n, Ctrl* ctrl,
+                                                 uint32_t edge, uint32_t pivot, bool take_all, uint32_t gt_lower,
+                                                 uint32_t eq_first, uint32_t eq_take, const OutTarget& out,
+                                                 uint32_t kslots, bool write_ok, int lane, int tid) {
+    constexpr int ES = sizeof(KeyT);
+    constexpr int NT = kSplitThreads;
+    const uint32_t ltm = lanemask_lt();
+    uint32_t bad = 0u;
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 4 * NT) {
+        uint32_t kb[4], ib[4], bg[4], be[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + tid + j * NT;
+            kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
+            ib[j] = i < n ? cidx[i] : 0u;
+        }
+        uint32_t sg = 0u, se = 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool ok = i0 + tid + j * NT < n && kb[j] >= edge;
+            const bool isg = ok && (take_all || kb[j] > pivot);
+            const bool ise = ok && !take_all && kb[j] == pivot;
+            bg[j] = __ballot_sync(0xFFFFFFFFu, isg);
+            be[j] = __ballot_sync(0xFFFFFFFFu, ise);
+            sg += static_cast<uint32_t>(__popc(bg[j]));
+            se += static_cast<uint32_t>(__popc(be[j]));
+        }
+        if ((sg | se) == 0u) continue;
+        uint32_t gb = 0u, eb = 0u;
+        if (lane == 0) {
+            if (sg) gb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_g), sg);
+            if (se) eb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_e), se);
+        }
+        gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
+        eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const bool isg = (bg[j] >> lane) & 1u, ise = (be[j] >> lane) & 1u;
+            const uint32_t te = eb + static_cast<uint32_t>(__popc(be[j] & ltm));
+            const uint32_t slot = isg ? gt_lower + gb + static_cast<uint32_t>(__popc(bg[j] & ltm)) : eq_first + te;
+            const bool put = isg || (ise && te < eq_take);
+            if (put && slot < kslots && write_ok) {
+                const int64_t o = out.base + slot;
+                if (TK) static_cast<uint32_t*>(out.vals)[o] = kb[j];
+                else if (ES == 2) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kb[j]));
+                else static_cast<uint32_t*>(out.vals)[o] = unkey_f32(kb[j]);
+                out.idx[o] = static_cast<int32_t>(ib[j]);
+            }
+            bad |= (put && slot >= kslots) ? 1u : 0u;
+            gb += static_cast<uint32_t>(__popc(bg[j]));
+            eb += static_cast<uint32_t>(__popc(be[j]));
+        }
+    }
+    return bad;
+}
+
 template <typename KeyT>
 __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanParams p) {
     constexpr int NC = kSplitThreads;
@@ -952,64 +1016,13 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     }
     const bool write_ok = !ctrl->abort;
     pdl_wait();  // the previous call's outputs are complete before this call writes its own
-    // One pass over the candidates, four per thread at a time: each warp takes slots for
-    // its keys above the pivot and its pivot-equal keys from two shared cursors (one
-    // atomic each per batch), so slots are this CTA's range in any order; pivot-equal keys
-    // past the quota are dropped.
-    const auto classify = [&](uint32_t kk, bool& isg, bool& ise) {
-        const bool inr = in_play(kk);
-        isg = inr && (take_all || kk > pivot);
-        ise = inr && !take_all && kk == pivot;
-    };
-    const uint32_t ltm = lanemask_lt();
-    const uint32_t kslots = static_cast<uint32_t>(p.k);
-    uint32_t bad = 0u;
-#pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 4 * NT) {
-        uint32_t kb[4], ib[4], bg[4], be[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = i0 + tid + j * NT;
-            kb[j] = i < n ? static_cast<uint32_t>(ckey[i]) : 0u;
-            ib[j] = i < n ? cidx[i] : 0u;
-        }
-        uint32_t sg = 0u, se = 0u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            bool isg, ise;
-            classify(kb[j], isg, ise);
-            const bool ok = i0 + tid + j * NT < n;
-            bg[j] = __ballot_sync(0xFFFFFFFFu, isg && ok);
-            be[j] = __ballot_sync(0xFFFFFFFFu, ise && ok);
-            sg += static_cast<uint32_t>(__popc(bg[j]));
-            se += static_cast<uint32_t>(__popc(be[j]));
-        }
-        if ((sg | se) == 0u) continue;
-        uint32_t gb = 0u, eb = 0u;
-        if (lane == 0) {
-            if (sg) gb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_g), sg);
-            if (se) eb = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->out_e), se);
-        }
-        gb = __shfl_sync(0xFFFFFFFFu, gb, 0);
-        eb = __shfl_sync(0xFFFFFFFFu, eb, 0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const bool isg = (bg[j] >> lane) & 1u, ise = (be[j] >> lane) & 1u;
-            const uint32_t te = eb + static_cast<uint32_t>(__popc(be[j] & ltm));
-            const uint32_t slot = isg ? gt_lower + gb + static_cast<uint32_t>(__popc(bg[j] & ltm)) : eq_first + te;
-            const bool put = isg || (ise && te < eq_take);
-            if (put && slot < kslots && write_ok) {
-                const uint32_t kk = kb[j];
-                const int64_t o = out.base + slot;
-                if (ES == 2 && !out.to_keys) static_cast<uint16_t*>(out.vals)[o] = static_cast<uint16_t>(unkey_bf16(kk));
-                else static_cast<uint32_t*>(out.vals)[o] = out.to_keys ? kk : unkey_f32(kk);
-                out.idx[o] = static_cast<int32_t>(ib[j]);
-            }
-            bad |= (put && slot >= kslots) ? 1u : 0u;
-            gb += static_cast<uint32_t>(__popc(bg[j]));
-            eb += static_cast<uint32_t>(__popc(be[j]));
-        }
-    }
+    // One pass over the candidates (split_output); partial results of rows over several
+    // clusters go out as keys
+    const uint32_t bad =
+        out.to_keys ? split_output<KeyT, true>(ckey, cidx, n, ctrl, edge, pivot, take_all, gt_lower, eq_first, eq_take,
+                                               out, static_cast<uint32_t>(p.k), write_ok, lane, tid)
+                    : split_output<KeyT, false>(ckey, cidx, n, ctrl, edge, pivot, take_all, gt_lower, eq_first,
+                                                eq_take, out, static_cast<uint32_t>(p.k), write_ok, lane, tid);
     if (bad) set_status(kErrInternal);
     if (take_all && !MC && tid == 0) set_status(kErrInternal);  // a whole row held fewer than k keys in play
     if (MC && crank == 0 && tid == 0)
