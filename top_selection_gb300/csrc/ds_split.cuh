@@ -388,6 +388,44 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
     return true;
 }
 
+// A compaction that every consumer thread of a split-row CTA joins: the buffer's slots
+// [0, min(first failed reservation, count)) are cut to the k largest keys, the threshold
+// becomes max(T, the k-th key) and is pushed to every CTA of the cluster (and to the
+// row's global word gT, tagged with the call's epoch, when the row spans clusters), and
+// the final select's first histogram is counted anew over the kept keys.  Returns the
+// new threshold.  Out of line: it runs rarely, and its code then stays out of the chunk
+// loop's instruction stream.
+template <typename KeyT>
+__device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int cap,
+                                                  int k, uint32_t tmax, int tid, bool hasT, uint32_t T, uint32_t* xh0,
+                                                  uint32_t hedge, int hs0, int G, unsigned long long* gT,
+                                                  uint32_t epoch) {
+    constexpr int NC = kSplitThreads;
+    named_bar_sync(2, NC);
+    const int fb = *reinterpret_cast<volatile int*>(&ctrl->fail_base);
+    const int cn = *reinterpret_cast<volatile int*>(&ctrl->cnt);
+    int n = fb < cn ? fb : cn;
+    n = n < cap ? n : cap;  // (a bound only: reservations never pass cap)
+    named_bar_sync(2, NC);
+    if (tid == 0) {
+        ctrl->compact_req = 0;
+        ctrl->fail_base = 0x7FFFFFFF;
+    }
+    // The threshold bounds the cluster's union, not this buffer alone, so the compaction
+    // ranks every key of the buffer.
+    const uint32_t piv = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, k, 0u, tmax, tid, true);
+    const uint32_t nt = hasT && T > piv ? T : piv;
+    if (tid == 0) {
+        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), nt);
+        if (gT) atomicMax(gT, (static_cast<unsigned long long>(epoch) << 32) | nt);
+    }
+    // the first final histogram, counted anew over the k keys kept
+    for (int i = tid; i < kXBins / 2; i += NC) xh0[i] = 0u;
+    named_bar_sync(2, NC);
+    for (int i = tid; i < k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
+    return nt;
+}
+
 // The final select's output: one pass over this CTA's n candidates, four per thread at
 // a time.  Each warp takes slots for its keys above the pivot and its pivot-equal keys
 // from two shared cursors (one atomic each per batch), so slots are this CTA's range in
@@ -589,27 +627,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         uint32_t hedge = 0u;
         int hs0 = KW - kXBits;
         // every consumer warp calls this together (from its chunk loop or the drain)
+        // every consumer warp calls this together (from its chunk loop or the drain); the
+        // work is out of line, away from the chunk loop's code
         const auto join_compaction = [&]() {
-            named_bar_sync(2, NC);
-            const int fb = *reinterpret_cast<volatile int*>(&ctrl->fail_base);
-            const int cn = *reinterpret_cast<volatile int*>(&ctrl->cnt);
-            int n = fb < cn ? fb : cn;
-            n = n < p.cap ? n : p.cap;  // (a bound only: reservations never pass cap)
-            named_bar_sync(2, NC);
-            if (tid == 0) {
-                ctrl->compact_req = 0;
-                ctrl->fail_base = 0x7FFFFFFF;
-            }
-            // The threshold bounds the cluster's union, not this buffer alone, so the
-            // compaction ranks every key of the buffer.
-            const uint32_t piv = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, p.k, 0u, tmax, tid, true);
-            T = hasT && T > piv ? T : piv;
+            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.k, tmax, tid, hasT, T, xh0, hedge, hs0, G,
+                                       MC ? p.gT + row : nullptr, p.epoch);
             hasT = true;
-            if (tid == 0) publish_T(T);
-            // the first final histogram, counted anew over the k keys kept
-            for (int i = tid; i < kXBins / 2; i += NC) xh0[i] = 0u;
-            named_bar_sync(2, NC);
-            for (int i = tid; i < p.k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
         };
         // A warp waiting for its next chunk joins any compaction requested meanwhile, so
         // the requesting warp does not wait for this chunk to land.  Decisions are
