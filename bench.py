@@ -20,6 +20,10 @@ step's input from pinned host memory, runs ds_topk, and reads the results back.
 
 --impl reference: the oracle (the CPU transcription of the method, oracle/) timed on
 this host's cores on a bounded sample of the same workload.
+
+--workload {indexer,sampler,longctx,row65536} and --k run the same measurement on the
+method's other workload shapes (sampler: 256 x 129280 fp32 logits; longctx: 4 x 1M bf16;
+row65536: one fp32 row); the default, and the headline, is the indexer shape at k=512.
 """
 from __future__ import annotations
 
@@ -40,6 +44,39 @@ if ROOT not in sys.path:
 
 METRIC = "effective input HBM GB/s (rows·N·bytes/time) at k=512; % of GB300 HBM peak"
 ROWS, N, K_TOP, B, B2 = 64, 131072, 512, 4096, 4096
+# --workload: the headline shape (indexer, the default) and the other shapes of the
+# method's workloads, each with its rows per GPU, default k and data seed
+SHAPES = {
+    "indexer": ("indexer_bf16", 64, 512, 2001),
+    "sampler": ("sampler_f32", 256, 512, 3001),
+    "longctx": ("longctx_bf16", 4, 512, 4001),
+    "row65536": ("row65536_f32", 1, 512, 1001),
+}
+
+
+class Shape:
+    """One workload of the bench: the synthetic rows, k, and the names the JSON line uses."""
+
+    def __init__(self, name: str, k: int | None, rank: int = 0):
+        import synth
+        fn, rows, k0, seed = SHAPES[name]
+        self.name = name
+        self.k = k or k0
+        self.w = getattr(synth, fn)(seed=seed + rank, rows=rows)
+        w = self.w
+        self.rows, self.N, self.stride, self.B, self.B2 = w.rows, w.N, w.stride, w.B, w.B2
+        self.bf16 = w.dtype == synth.BF16
+        self.dtype = w.dtype
+        self.es = 2 if self.bf16 else 4
+        self.dname = "bf16" if self.bf16 else "fp32"
+        self.step_bytes = self.rows * self.N * self.es
+        self.desc = (f"{fn}: {self.rows} rows x {self.N} {self.dname} ({w.desc}), stride {self.stride}, "
+                     f"k={self.k}, B={self.B}, B2={self.B2}")
+        if name == "indexer" and self.k == K_TOP:
+            self.desc = WORKLOAD
+
+    def host_array(self):
+        return self.w.x.view(np.int16) if self.bf16 else self.w.x
 SEED = 0x5EED
 WORKLOAD = f"indexer_bf16: {ROWS} rows x {N} bf16 N(0,1), stride {N}, k={K_TOP}, B={B}, B2={B2}"
 FALLBACK_HBM_GBS = 6800.0
@@ -74,11 +111,18 @@ def _source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile():
-    """dram bytes per launch recorded by the last ncu capture of this kernel, if the
-    kernel sources have not changed since."""
+def _traffic_from_profile(sh=None):
+    """dram bytes per launch recorded by the last ncu capture of this kernel on this
+    workload, if the kernel sources have not changed since."""
+    path = PROFILE_TRAFFIC
+    if sh is not None and sh.name != "indexer":
+        path = os.path.join(ROOT, "profiles", f"ds_split_kernel_{sh.name}_{sh.dname}.md")
+        if sh.k != SHAPES[sh.name][2]:
+            return None
+    elif sh is not None and sh.k != K_TOP:
+        return None
     try:
-        with open(PROFILE_TRAFFIC) as f:
+        with open(path) as f:
             text = f.read()
     except OSError:
         return None
@@ -149,26 +193,25 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def _cpu_oracle(seconds: float, threads: int | None = None):
+def _cpu_oracle(seconds: float, sh: "Shape", threads: int | None = None):
     """The oracle's DeepSelect transcription over the workload's rows on this host's
     cores, repeated for about `seconds`."""
     import oracle
-    import synth
-    w = synth.indexer_bf16()
+    w = sh.w
     th = threads or oracle.max_threads()
-    oracle.deepselect(w.x[:4], w.dtype, K_TOP, B, B2, SEED, threads=th)   # build / warm
+    oracle.deepselect(w.x[:4], w.dtype, sh.k, sh.B, sh.B2, SEED, N=w.N, threads=th)   # build / warm
     t0 = time.perf_counter()
     runs = 0
     while True:
-        oracle.deepselect(w.x, w.dtype, K_TOP, B, B2, SEED + runs, threads=th)
+        oracle.deepselect(w.x, w.dtype, sh.k, sh.B, sh.B2, SEED + runs, N=w.N, threads=th)
         runs += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
     gbs = runs * w.input_bytes / el / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": th, "kind": "oracle",
-            "sample": f"oracle DeepSelect transcription (C, OpenMP over rows) on the full {ROWS}x{N} bf16 "
-                      f"batch, {runs} runs in {el:.1f} s"}
+            "sample": f"oracle DeepSelect transcription (C, OpenMP over rows) on the full {sh.rows}x{sh.N} "
+                      f"{sh.dname} batch, {runs} runs in {el:.1f} s"}
 
 
 def run_reference(args):
@@ -179,35 +222,39 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    import synth
-    w = synth.indexer_bf16()
+    sh = Shape(args.workload, args.k)
+    w = sh.w
+    ROWS_, N_ = sh.rows, sh.N
     th = oracle.max_threads()
     steps = max(1, args.steps)
+    x = np.ascontiguousarray(w.x[:, :N_])
     t0 = time.perf_counter()
-    oracle.deepselect(w.x, w.dtype, K_TOP, B, B2, SEED, threads=th)
+    oracle.deepselect(x, w.dtype, sh.k, sh.B, sh.B2, SEED, threads=th)
     t_full = time.perf_counter() - t0
     budget = 120.0
-    rows_ps, n_ps = ROWS, N
+    rows_ps, n_ps = ROWS_, N_
     if steps * t_full > budget:
-        rows_ps = max(1, int(ROWS * budget / (steps * t_full)))
+        rows_ps = max(1, int(ROWS_ * budget / (steps * t_full)))
         if rows_ps == 1:
-            t_row = t_full * th / ROWS
-            n_ps = int(min(N, max(2 * B, N * budget / (steps * max(t_row, 1e-9)))))
-    sample = np.ascontiguousarray(w.x[:rows_ps, :n_ps])
+            t_row = t_full * th / ROWS_
+            n_ps = int(min(N_, max(2 * sh.B, N_ * budget / (steps * max(t_row, 1e-9)))))
+    sample = np.ascontiguousarray(x[:rows_ps, :n_ps])
+    k_ps = min(sh.k, n_ps)
     use_th = min(th, rows_ps)
     for i in range(args.warmup):
-        oracle.deepselect(sample, w.dtype, K_TOP, B, B2, SEED + i, threads=use_th)
+        oracle.deepselect(sample, w.dtype, k_ps, sh.B, sh.B2, SEED + i, threads=use_th)
     t0 = time.perf_counter()
     for i in range(steps):
-        oracle.deepselect(sample, w.dtype, K_TOP, B, B2, SEED + i, threads=use_th)
+        oracle.deepselect(sample, w.dtype, k_ps, sh.B, sh.B2, SEED + i, threads=use_th)
     el = time.perf_counter() - t0
-    gbs = steps * rows_ps * n_ps * 2 / el / 1e9
-    desc = f"{rows_ps} row(s) x {n_ps} of the {ROWS}x{N} bf16 batch per step, oracle DeepSelect transcription"
+    gbs = steps * rows_ps * n_ps * sh.es / el / 1e9
+    desc = (f"{rows_ps} row(s) x {n_ps} of the {ROWS_}x{N_} {sh.dname} batch per step, oracle DeepSelect "
+            f"transcription")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": ws,
         "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample_per_step": desc},
+        "scaling": "weak", "vs_baseline": None, "dtype": sh.dname, "data": "synthetic",
+        "config": {"workload": sh.desc, "sample_per_step": desc},
         "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": use_th, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -238,30 +285,31 @@ def run_gpu(args):
 
     # weak scaling: rank r owns global rows [lo, hi) of a ROWS*ws batch (its own copy of
     # the workload shape, drawn with its own seed); no data-path collective
-    lo, hi = row_range(ROWS * ws, ws, rank)
-    w = synth.indexer_bf16(seed=2001 + rank, rows=hi - lo)
-    host = torch.from_numpy(w.x.view(np.int16))
+    sh = Shape(args.workload, args.k, rank)
+    ROWS, N, K_TOP, B, B2, STRIDE, DT = sh.rows, sh.N, sh.k, sh.B, sh.B2, sh.stride, sh.dtype
+    vdt = torch.int16 if sh.bf16 else torch.float32
+    host = torch.from_numpy(sh.host_array())
     x0 = host.to(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 132 * 1024 * 1024) or 132 * 1024 * 1024
-    step_bytes = ROWS * N * 2
+    step_bytes = sh.step_bytes
     R = max(8, -(-4 * l2 // step_bytes))
     xs = [x0.clone() for _ in range(R)]
-    outs = [(torch.empty((ROWS, K_TOP), dtype=torch.int16, device=dev),
+    outs = [(torch.empty((ROWS, K_TOP), dtype=vdt, device=dev),
              torch.empty((ROWS, K_TOP), dtype=torch.int32, device=dev)) for _ in range(R)]
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
-    plan = ds.ds_get_plan(ds.DS_BF16, ROWS, N, K_TOP, B, B2)
+    plan = ds.ds_get_plan(DT, ROWS, N, K_TOP, B, B2)
     launches_per_step = 2 if plan["merge_launch"] else 1
 
     def call(i, ready=False):
         x = xs[i % R]
         v, ix = outs[i % R]
         if ready:
-            st = ds.ds_topk_ex(x.data_ptr(), ds.DS_BF16, ROWS, N, N, K_TOP, B, B2, SEED, v.data_ptr(),
+            st = ds.ds_topk_ex(x.data_ptr(), DT, ROWS, N, STRIDE, K_TOP, B, B2, SEED, v.data_ptr(),
                                ix.data_ptr(), input_ready=True, stream=sptr)
         else:
-            st = ds.ds_topk(x.data_ptr(), ds.DS_BF16, ROWS, N, N, K_TOP, B, B2, SEED, v.data_ptr(),
+            st = ds.ds_topk(x.data_ptr(), DT, ROWS, N, STRIDE, K_TOP, B, B2, SEED, v.data_ptr(),
                             ix.data_ptr(), sptr)
         if st != 0:
             raise ds.DSError(st)
@@ -333,26 +381,29 @@ def run_gpu(args):
 
     # roofline of the split-row kernel (the one kernel of a step): algorithmic bytes per
     # launch / average launch time
-    alg_bytes = step_bytes + ROWS * K_TOP * (2 + 4)
+    alg_bytes = step_bytes + ROWS * K_TOP * (sh.es + 4)
     peak, peak_kind = _peak()
     achieved = alg_bytes / (ms / args.steps * 1e-3) / 1e9
+    kname = ("ds_scan_kernel" if plan["parts"] == 1 else "ds_split_kernel") + \
+        ("<uint16_t>" if sh.bf16 else "<uint32_t>")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(),
-                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)",
-                "kernel": "ds_split_kernel<uint16_t>"}
+                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(sh),
+                "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)", "kernel": kname}
+    if plan["merge_launch"]:
+        roofline["note"] = "each step also runs ds_merge_kernel (rows over several clusters)"
 
     # e2e through the public API with host buffers
     pinned = host.pin_memory()
     xe = torch.empty_like(x0)
-    ve = torch.empty((ROWS, K_TOP), dtype=torch.int16, device=dev)
+    ve = torch.empty((ROWS, K_TOP), dtype=vdt, device=dev)
     ie = torch.empty((ROWS, K_TOP), dtype=torch.int32, device=dev)
-    hv = torch.empty((ROWS, K_TOP), dtype=torch.int16).pin_memory()
+    hv = torch.empty((ROWS, K_TOP), dtype=vdt).pin_memory()
     hi = torch.empty((ROWS, K_TOP), dtype=torch.int32).pin_memory()
     e_steps = args.e2e_steps
 
     def e2e_step():
         xe.copy_(pinned, non_blocking=True)
-        ds.topk(xe, K_TOP, B, B2, seed=SEED, out=(ve, ie), stream=sptr)
+        ds.topk(xe, K_TOP, B, B2, seed=SEED, N=N, out=(ve, ie), stream=sptr)
         hv.copy_(ve, non_blocking=True)
         hi.copy_(ie, non_blocking=True)
 
@@ -372,19 +423,19 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
     e2e = {"value": round(ws * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": step_bytes, "d2h_bytes_per_step": ROWS * K_TOP * (2 + 4),
+           "h2d_bytes_per_step": ROWS * STRIDE * sh.es, "d2h_bytes_per_step": ROWS * K_TOP * (sh.es + 4),
            "steps": e_steps}
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
-    cpu = _cpu_oracle(args.cpu_seconds) if (ws == 1 and args.cpu_seconds > 0) else None
+    cpu = _cpu_oracle(args.cpu_seconds, sh) if (ws == 1 and args.cpu_seconds > 0) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "global_batch_rows": ROWS * ws, "parallelism": f"rows replicated x{ws}",
+        "vs_baseline": None, "dtype": sh.dname, "data": "synthetic",
+        "config": {"workload": sh.desc, "global_batch_rows": ROWS * ws, "parallelism": f"rows replicated x{ws}",
                    "l2": f"inputs rotated over {R} device copies ({R * step_bytes / 1e6:.0f} MB > 4x L2 "
                          f"{l2 / 1e6:.0f} MB)",
                    "timing": f"CUDA graphs of {G} calls, CUDA events on the launching stream",
@@ -413,6 +464,9 @@ def main(argv=None):
     ap.add_argument("--graph-len", type=int, default=2000)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", choices=sorted(SHAPES), default="indexer",
+                    help="the indexer shape is the headline; the others are the method's other workloads")
+    ap.add_argument("--k", type=int, default=0, help="k (default: the workload's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
