@@ -119,13 +119,13 @@ def test_plans_on_a_described_device(lib):
     def pc(n):
         return plans[n]["parts"], plans[n]["cluster"], plans[n]["merge_launch"]
     assert pc("indexer") == (4, 4, 0)
-    assert pc("sampler") == (2, 2, 0)
-    assert pc("sampler_k4096") == (1, 1, 0)
+    assert pc("sampler") == (1, 1, 0) and plans["sampler"]["threads"] == 256        # split-row kernel
+    assert pc("sampler_k4096") == (1, 1, 0) and plans["sampler_k4096"]["threads"] == 288  # one-CTA rows
     assert pc("longctx") == (16, 16, 0)
     assert pc("row65536") == (8, 8, 0)
     assert pc("huge") == (256, 8, 1)
     for n, p in plans.items():
         assert p["smem_bytes"] <= 232448, n
-        if p["parts"] > 1:
+        if p["threads"] == 256:
             assert p["stages"] in (8, 16), n          # warp-owned stages
             assert p["ctas_per_sm"] == 2, n

@@ -323,3 +323,22 @@ def test_input_is_previous_calls_output(parts):
     for j, (v, _) in enumerate(outs):
         got = np.sort(v.cpu().numpy().view(np.uint16).astype(np.int64), axis=1)
         assert np.array_equal(got, np.sort(want[j % 3].astype(np.int64), axis=1)), f"call {j}"
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_many_rows_one_part_each(dtype):
+    """Rows that already cover the SMs run one per CTA in the split-row kernel when k is
+    small against a chunk (no cluster, k + one chunk of candidates); a ragged row length
+    leaves a tail in the last block."""
+    import top_selection_gb300 as ds
+    rng = np.random.default_rng(31 + dtype)
+    rows, N = 200, 19997
+    x = rng.standard_normal((rows, N)).astype(np.float32)
+    if dtype == synth.BF16:
+        x = synth.f32_to_bf16_bits(x)
+    xp, n = pad_rows(x, dtype)
+    plan = ds.ds_get_plan(dtype, rows, n, 64, 1024, 1024)
+    assert plan["parts"] == 1 and plan["threads"] == 256
+    for k in (1, 64, 256):
+        v, i, _ = run_gpu(xp, dtype, k, 1024, 1024, 17, N=n)
+        check_topk(x, dtype, k, v, i)

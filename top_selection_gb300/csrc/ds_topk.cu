@@ -734,6 +734,7 @@ static bool dev_info(int dev, DevInfo& out) {
 
 struct Plan {
     int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww, refine;
+    bool split;  // the split-row kernel (also for one part per row), else the one-CTA-per-row kernel
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -769,21 +770,22 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     if (parts < 0) return DS_ERR_INVALID_ARG;
     if (parts == 0 && opt && opt->stats) parts = 1;  // the statistics describe the one-CTA schedule
     const bool spread = N * P.es >= (int64_t(16) << 20);
+    bool split1 = false;
     if (parts == 0) {
-        // Enough CTAs to cover the SMs: rows split in parts of at least 4 blocks.  Rows that
-        // already cover the SMs still go in halves when k is small against a chunk (the
-        // split-row kernel keeps k + one chunk of candidates and runs two CTAs per SM,
-        // where a whole row's CTA needs k + B + B2 and runs alone).
-        // Rows under 16 MB stay in one cluster (at most 16 CTAs: no merge pass) and are not
-        // split so finely that a warp would get no chunk; larger rows spread over several
-        // clusters and a merge kernel.
+        // Enough CTAs to cover the SMs: rows split in parts of at least 4 blocks.  Rows under
+        // 16 MB stay in one cluster (at most 16 CTAs: no merge pass) and are not split so
+        // finely that a warp would get no chunk; larger rows spread over several clusters
+        // and a merge kernel.
         parts = 1;
         const int64_t maxp = P.m / 4 > 1 ? P.m / 4 : 1;
         const int64_t fillp = N / (static_cast<int64_t>(P.chunk) * kNCW);
         const int64_t capp = spread ? 256 : 16;
         while (rows * parts < di.sms && parts * 2 <= maxp && parts * 2 <= capp && (spread || parts * 2 <= fillp))
             parts *= 2;
-        if (parts == 1 && maxp >= 2 && static_cast<int64_t>(k) * 4 <= P.chunk) parts = 2;
+        // Rows that already cover the SMs run one per CTA in the split-row kernel when k is
+        // small against a chunk: it keeps k + one chunk of candidates and runs two CTAs per
+        // SM, where the one-CTA-per-row kernel needs k + B + B2 and runs alone.
+        split1 = parts == 1 && maxp >= 2 && static_cast<int64_t>(k) * 4 <= P.chunk;
         while ((P.m + parts - 1) / parts > kPermMax) parts *= 2;
         if (parts > P.m) return DS_ERR_UNSUPPORTED;
     } else {
@@ -810,7 +812,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.wm = 0;
     P.ww = 1;
     P.refine = 0;
-    if (parts > 1) {
+    P.split = parts > 1 || split1;
+    if (P.split) {
         // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
         // of the consumer warps (every stage is then used by one warp only, and a warp
         // never waits on a stage whose previous fill belongs to another warp).  Take the
@@ -985,7 +988,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     }
     void (*kern)(ScanParams);
     int slot = sizeof(KeyT) == 2 ? 0 : 1;
-    if (P.parts == 1) {
+    if (!P.split) {
         kern = ds_scan_kernel<KeyT>;
     } else {
         kern = ds_split_kernel<KeyT>;
@@ -994,7 +997,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows * P.parts), 1, 1);
-    cfg.blockDim = dim3(P.parts == 1 ? kScanThreads : kSplitThreads, 1, 1);
+    cfg.blockDim = dim3(P.split ? kSplitThreads : kScanThreads, 1, 1);
     cfg.dynamicSmemBytes = P.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1089,7 +1092,7 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
     if (st != DS_OK) return st;
     plan->parts = P.parts;
     plan->cluster = P.G;
-    plan->threads = P.parts == 1 ? kScanThreads : kSplitThreads;
+    plan->threads = P.split ? kSplitThreads : kScanThreads;
     plan->chunk_elems = P.chunk;
     plan->stages = P.stages;
     plan->capacity = P.cap;
