@@ -844,11 +844,21 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             return 256 * R;
         };
         const auto fit = [&](int chunk, int stages, size_t limit) -> bool {
-            const int cap = static_cast<int>(align_up(static_cast<size_t>(k) + chunk, 16 / P.es));
+            int cap = static_cast<int>(align_up(static_cast<size_t>(k) + chunk, 16 / P.es));
             ww_try = warm_chunks(chunk, stages);
             const int wm = warm_groups(chunk);
-            const size_t need = split_layout(P.es, chunk, stages, cap, G, wm, k, P.perm_cap).total;
+            size_t need = split_layout(P.es, chunk, stages, cap, G, wm, k, P.perm_cap).total;
             if (need > limit) return false;
+            // the shared memory left over widens the candidate buffer (fewer compactions)
+            const int unit_c = 16 / P.es * 16;  // keeps the buffer's arrays 16-byte aligned
+            const int extra = static_cast<int>((limit - need) / (P.es + 4)) / unit_c * unit_c;
+            if (extra > 0 && static_cast<int64_t>(cap) + extra <= (int64_t(1) << 20)) {
+                const size_t need2 = split_layout(P.es, chunk, stages, cap + extra, G, wm, k, P.perm_cap).total;
+                if (need2 <= limit) {
+                    cap += extra;
+                    need = need2;
+                }
+            }
             P.chunk = chunk;
             P.stages = stages;
             P.cap = cap;
