@@ -120,7 +120,7 @@ def test_plans_on_a_described_device(lib):
         return plans[n]["parts"], plans[n]["cluster"], plans[n]["merge_launch"]
     assert pc("indexer") == (4, 4, 0)
     assert pc("sampler") == (1, 1, 0) and plans["sampler"]["threads"] == 256        # split-row kernel
-    assert pc("sampler_k4096") == (1, 1, 0) and plans["sampler_k4096"]["threads"] == 288  # one-CTA rows
+    assert pc("sampler_k4096") == (1, 1, 0) and plans["sampler_k4096"]["threads"] == 256
     assert pc("longctx") == (16, 16, 0)
     assert pc("row65536") == (8, 8, 0)
     assert pc("huge") == (256, 8, 1)

@@ -782,10 +782,11 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         const int64_t capp = spread ? 256 : 16;
         while (rows * parts < di.sms && parts * 2 <= maxp && parts * 2 <= capp && (spread || parts * 2 <= fillp))
             parts *= 2;
-        // Rows that already cover the SMs run one per CTA in the split-row kernel when k is
-        // small against a chunk: it keeps k + one chunk of candidates and runs two CTAs per
-        // SM, where the one-CTA-per-row kernel needs k + B + B2 and runs alone.
-        split1 = parts == 1 && maxp >= 2 && static_cast<int64_t>(k) * 4 <= P.chunk;
+        // Rows that already cover the SMs run one per CTA in the split-row kernel (its
+        // warm-up threshold, k + at least one chunk of candidates, two CTAs per SM where
+        // they fit); the one-CTA-per-row kernel of the pages' schedule keeps the
+        // statistics, explicit parts = 1 and rows of fewer than 8 blocks.
+        split1 = parts == 1 && maxp >= 2;
         while ((P.m + parts - 1) / parts > kPermMax) parts *= 2;
         if (parts > P.m) return DS_ERR_UNSUPPORTED;
     } else {
