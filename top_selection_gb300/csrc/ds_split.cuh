@@ -174,6 +174,43 @@ __device__ __forceinline__ void warm_maxima(const uint4* v0, int tid, int cvec, 
     }
 }
 
+// The same for samples of 9..16 vectors per thread (rows streamed through the ring): up
+// to 8 chunks, groups of 2^gsh consecutive vectors of the thread, each group's key stored
+// straight to out[g] for g < R (no register array of groups).
+template <typename KeyT>
+__device__ __forceinline__ void warm_maxima16(const uint4* v0, int tid, int cvec, int ww, int VT, int gsh, int R,
+                                              bool gotw, const int (&nvw)[8], KeyT* out) {
+    constexpr int ES = sizeof(KeyT);
+    uint32_t cur = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int v = tid + j * kSplitThreads;
+        int q = 0;
+#pragma unroll
+        for (int t = 1; t < 8; ++t) q += v >= t * cvec ? 1 : 0;
+        int nv = nvw[0];
+#pragma unroll
+        for (int t = 1; t < 8; ++t)
+            if (q == t) nv = nvw[t];
+        if (gotw && j < VT && q < ww && v - q * cvec < nv) {
+            const uint4 x = v0[v];
+            uint32_t m;
+            if (ES == 2) {
+                m = max_bf16x2(max_bf16x2(x.x, x.y), max_bf16x2(x.z, x.w));
+            } else {
+                m = __float_as_uint(fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)),
+                                          fmaxf(__uint_as_float(x.z), __uint_as_float(x.w))));
+            }
+            cur = max(cur, max_word_key<KeyT>(m));
+        }
+        if (((j + 1) & ((1 << gsh) - 1)) == 0) {
+            const int g = j >> gsh;
+            if (g < R) out[g] = static_cast<KeyT>(cur);
+            cur = 0u;
+        }
+    }
+}
+
 // The pivot of a final-select pass, found by every warp on its own (no barrier).  The
 // cluster's histogram is G rows of kXBins 16-bit counts (pairs in 32-bit words), row c
 // from the CTA of rank c; lane l owns bins [16l, 16l + 16), higher bins holding larger
@@ -687,16 +724,20 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // and splits them into R groups; a group's maximum is taken on the packed values
             // (NaNs ignored) and keyed once
             const int R = wm / 256;
-            const int VT = (ww * cvec + NC - 1) / NC;  // at most 8
+            const int VT = (ww * cvec + NC - 1) / NC;  // at most 16
             // log2 of vectors per group
-            const int gsh = VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0));
+            const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
-            if (VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
-            else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+            if (VT <= 8) {
+                uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
+                if (VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+                else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                if (r < R) wx[crank * wm + tid * R + r] = static_cast<KeyT>(gk[r]);
+                for (int r = 0; r < 4; ++r)
+                    if (r < R) wx[crank * wm + tid * R + r] = static_cast<KeyT>(gk[r]);
+            } else {
+                warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * wm + tid * R);
+            }
             fence_proxy_async_smem();
             named_bar_sync(1, NC);
             if (G > 1) {

@@ -830,7 +830,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             // rows streamed through the ring sample up to 8 chunks (8 vectors per thread),
             // rows held whole 2: their filter waits for the sample's threshold
             const int wmax = nq_min > stages ? 8 : 2;
-            while (w * 2 <= wmax && w * 2 <= stages && w * 2 * cvec <= 8 * kNCW * 32 && w * 2 <= nq_min) w *= 2;
+            while (w * 2 <= wmax && w * 2 <= stages && w * 2 * cvec <= 16 * kNCW * 32 && w * 2 <= nq_min) w *= 2;
             return w;
         };
         int ww_try = 1;
@@ -839,8 +839,12 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             // about 4k in the cluster's union when they fit the exchange
             const int vt = (ww_try * chunk * P.es / 16 + kNCW * 32 - 1) / (kNCW * 32);
             int R = 1;
-            while (R * 2 <= vt && R * 2 <= 4 && static_cast<int64_t>(G) * 256 * R * 2 * P.es <= kWarmMaxBytes &&
-                   static_cast<int64_t>(G) * 256 * R < 4 * static_cast<int64_t>(k))
+            // (up to 4 groups per thread for samples of up to 8 vectors, 8 for larger ones;
+            // a CTA without a cluster exchanges nothing and takes twice as many)
+            const int rmax = vt > 8 ? 8 : 4;
+            const int64_t umax = (G == 1 ? 8 : 4) * static_cast<int64_t>(k);
+            while (R * 2 <= vt && R * 2 <= rmax && static_cast<int64_t>(G) * 256 * R * 2 * P.es <= kWarmMaxBytes &&
+                   static_cast<int64_t>(G) * 256 * R < umax)
                 R *= 2;
             return 256 * R;
         };
