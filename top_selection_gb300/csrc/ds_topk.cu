@@ -827,9 +827,10 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             const int64_t nq_min = (P.m / parts) * per;
             const int cvec = chunk * P.es / 16;
             int w = 1;
-            // rows streamed through the ring sample up to 8 chunks (8 vectors per thread),
-            // rows held whole 2: their filter waits for the sample's threshold
-            const int wmax = nq_min > stages ? 8 : 2;
+            // rows streamed through the ring sample up to 8 chunks when a CTA has the row to
+            // itself, 4 in a cluster (whose union of maxima is larger already); rows held
+            // whole 2: their filter waits for the sample's threshold
+            const int wmax = nq_min > stages ? (G == 1 ? 8 : 4) : 2;
             while (w * 2 <= wmax && w * 2 <= stages && w * 2 * cvec <= 16 * kNCW * 32 && w * 2 <= nq_min) w *= 2;
             return w;
         };
