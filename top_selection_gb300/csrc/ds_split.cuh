@@ -1,31 +1,36 @@
 // ds_split.cuh -- DeepSelect on rows split over several CTAs (a thread-block cluster per
-// group of G parts, and optionally C clusters per row).
+// group of G parts, and optionally C clusters per row), and on rows that have a CTA to
+// themselves but many neighbours (G = 1).
 //
 // DeepSelect-deep-dive.md, "Implementation", has the CTAs of a cluster scan parts of one
 // row, share the threshold T through distributed shared memory and merge their
 // candidates.  This kernel keeps that structure and arranges the work for short critical
 // paths on sm_103a:
 //
-//   * A producer warp issues every chunk of the part into a ring of bulk-copy stages at
-//     once (the whole part when it fits), in the part's Philox block order.
-//   * Warm-up: the first chunk of every CTA is reduced to group maxima (the largest key
-//     of each group of g consecutive elements).  The CTAs exchange them with bulk copies
-//     into each other's shared memory, and every CTA derives the same threshold from the
-//     union: T sits just below the 2048-bin top-digit bucket that holds the k-th largest
-//     group maximum.  At least k groups have a maximum at or above that bucket, so at
-//     least k elements of the cluster are kept above T: every element at or below T is
+//   * Copies: 8 warps, no producer.  Stage s of an 8- or 16-stage ring of 1-D bulk copies
+//     belongs to warp s mod 8, which filters every chunk landing there (chunk q, in the
+//     part's Philox block order, goes to warp q mod 8) and issues the stage's next copy
+//     itself.  The warm-up's chunks are requested first, the rest once chunk 0 landed.
+//   * Warm-up (init window): the first ww chunks of every CTA are reduced to group
+//     maxima (the largest key of each group of consecutive vectors).  The CTAs exchange
+//     them with bulk copies into each other's shared memory, and every CTA derives the
+//     same threshold from the union: T sits just below the 2048-bin top-digit bucket
+//     (narrowed by 5 more bits for rows streamed through the ring) that holds the k-th
+//     largest group maximum.  At least k groups have a maximum at or above it, so at
+//     least k elements of the row are kept above T: every element at or below T is
 //     outside the top k (the threshold invariant of the deep dive's proof).
-//   * Filter: each consumer warp owns whole chunks (chunk q goes to warp (q - 1) mod 8),
-//     so chunks are filtered in parallel.  Lanes read 16-byte vectors, compare packed
-//     values against T with one instruction per word, count survivors, reserve their
-//     slots with one shared atomic per warp and write them.  A reservation that does not
-//     fit makes every warp join a RadixSelectTopK compaction of the CTA's buffer to k
-//     (which raises T); the warp then resumes where it stopped.
+//   * Filter: each warp filters its 8 KB chunks: lanes read 16-byte vectors and compare
+//     packed values against T with one instruction per word, a shuffle scan places the
+//     lanes' survivors, one shared atomic per warp reserves their slots, and the warp
+//     writes them in two steps (columns per lane, then keys and columns for the warp's
+//     slots in order), counting each key into the final select's first histogram.  A
+//     reservation that does not fit makes every warp join a RadixSelectTopK compaction
+//     of the CTA's buffer to k (which raises T); the warp then resumes where it stopped.
 //   * Final: the cluster selects the k largest keys of the union of its buffers by
-//     most-significant-digit radix passes over 1024 bins.  Each pass, every CTA pushes
-//     its histogram to every other CTA; all CTAs then hold the same sums, find the same
-//     pivot bin, and know every CTA's count above the pivot, so each writes its share of
-//     the output at offsets it computes itself.
+//     most-significant-digit radix passes over 512 bins.  Each pass, every CTA pushes
+//     its histogram to every other CTA; warp 0 of every CTA then finds the same pivot bin
+//     and every CTA's count above it, so each CTA writes its share of the output at
+//     offsets it computes itself, in one pass with two shared slot cursors.
 //
 // The packed compare is "greater or unordered" against a float threshold chosen so that
 // every element whose key exceeds T passes (NaNs always pass, and -0 passes a -0

@@ -820,7 +820,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         // never waits on a stage whose previous fill belongs to another warp).  Take the
         // largest chunk (halving from 16 KB, at least 1 KB) whose layout lets two CTAs
         // share an SM, 16 stages before 8; else the largest that fits one CTA.
-        // The warm-up samples the first ww chunks of each CTA (up to 4 vectors per thread,
+        // The warm-up samples the first ww chunks of each CTA (up to 16 vectors per thread,
         // never more chunks than the CTA with the fewest has).
         const auto warm_chunks = [&](int chunk, int stages) {
             const int64_t per = (static_cast<int64_t>(B) + chunk - 1) / chunk;
