@@ -342,3 +342,20 @@ def test_many_rows_one_part_each(dtype):
     for k in (1, 64, 256):
         v, i, _ = run_gpu(xp, dtype, k, 1024, 1024, 17, N=n)
         check_topk(x, dtype, k, v, i)
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+@pytest.mark.parametrize("k", [1, 1000, 2048])
+def test_many_short_rows_k_up_to_n(dtype, k):
+    """One CTA per row in the split-row kernel with k up to the row length: 8 blocks per
+    row (the fewest the plan splits this way), ties from rounding."""
+    import top_selection_gb300 as ds
+    rng = np.random.default_rng(77 + k + dtype)
+    rows, N, B = 160, 2048, 256
+    x = np.round(rng.standard_normal((rows, N)) * 8).astype(np.float32) / 8
+    if dtype == synth.BF16:
+        x = synth.f32_to_bf16_bits(x)
+    plan = ds.ds_get_plan(dtype, rows, N, k, B, B)
+    assert plan["parts"] == 1 and plan["threads"] == 256
+    v, i, _ = run_gpu(x, dtype, k, B, B, 23)
+    check_topk(x, dtype, k, v, i)
