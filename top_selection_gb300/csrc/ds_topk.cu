@@ -41,10 +41,9 @@ namespace dsk {
 
 constexpr int kNCW = 8;                        // consumer warps per CTA
 constexpr int kScanThreads = (kNCW + 1) * 32;
-constexpr int kMergeThreads = kNCW * 32;
+constexpr int kMergeThreads = 512;              // one CTA per row over several clusters
 constexpr int kChunkBytesMax = 16384;          // one bulk copy
 constexpr int kLiteralStages = 8;              // deepest ring of one-CTA rows
-constexpr int kMergeTile = 2048;               // entries per merge block
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -66,25 +65,6 @@ __host__ __device__ inline ScanLayout scan_layout(int es, int chunk, int stages,
     off += kScratchWords * 4;
     L.perm = off;
     off += align_up(static_cast<size_t>(perm_cap) * 4, 16);
-    L.ctrl = off;
-    off += align_up(sizeof(Ctrl), 16);
-    L.total = off;
-    return L;
-}
-
-struct MergeLayout {
-    size_t ckey, cidx, hist, ctrl, total;
-};
-
-__host__ __device__ inline MergeLayout merge_layout(int es, int cap) {
-    MergeLayout L;
-    size_t off = 0;
-    L.ckey = off;
-    off += align_up(static_cast<size_t>(cap) * es, 16);
-    L.cidx = off;
-    off += align_up(static_cast<size_t>(cap) * 4, 16);
-    L.hist = off;
-    off += kScratchWords * 4;
     L.ctrl = off;
     off += align_up(sizeof(Ctrl), 16);
     L.total = off;
@@ -600,89 +580,157 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
 namespace dsk {
 
 // ---------------------------------------------------------------- merge kernel ----
-// Finishes rows split over C clusters: DeepSelect over the C partial results of the row
-// (each at most k (key, column) pairs), filtered against the row's shared threshold,
-// which every kept partial entry meets or exceeds.
+// The bucket of the kk-th largest count among 2048 (one warp): lane l sums buckets
+// [64l, 64l + 64), a suffix scan over the lanes picks the lane, then the lanes split its
+// buckets in pairs.  bstar = -1 when all buckets together hold fewer than kk; above =
+// the count in buckets above bstar (all of them when bstar = -1), total = all.
+__device__ __forceinline__ void warp_bucket_2048(const uint32_t* hist, uint32_t kk, int lane, int& bstar,
+                                                 uint32_t& above, uint32_t& total) {
+    const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 16 * lane;
+    uint32_t t = 0u;
+#pragma unroll 4
+    for (int j = 0; j < 16; ++j) {
+        const uint4 x = h4[(j + lane) & 15];  // rotated: fewer bank conflicts
+        t += x.x + x.y + x.z + x.w;
+    }
+    uint32_t sf = t;  // buckets of lanes >= lane
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
+        if (lane + d < 32) sf += u;
+    }
+    total = __shfl_sync(0xFFFFFFFFu, sf, 0);
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, sf >= kk);
+    bstar = -1;
+    above = total;
+    if (!hit) return;
+    const int L = 31 - __clz(hit);
+    const uint32_t aboveL = __shfl_sync(0xFFFFFFFFu, sf - t, L);
+    const uint2 c2 = reinterpret_cast<const uint2*>(hist)[32 * L + lane];
+    const uint32_t c = c2.x + c2.y;
+    uint32_t s2 = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, s2, d);
+        if (lane + d < 32) s2 += u;
+    }
+    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, aboveL + s2 >= kk);
+    const int J = 31 - __clz(hit2);
+    const uint32_t aJ = __shfl_sync(0xFFFFFFFFu, aboveL + s2 - c, J);
+    const uint32_t hiJ = __shfl_sync(0xFFFFFFFFu, c2.y, J);
+    const bool top = aJ + hiJ >= kk;
+    bstar = 64 * L + 2 * J + (top ? 1 : 0);
+    above = top ? aJ : aJ + hiJ;
+}
+
+// Finishes rows split over C clusters.  Each cluster left its share of its union's top k
+// (at most k (key, column) pairs) in the workspace; the row's top k are the k largest of
+// these.  They stay in global memory (L2): radix passes of 2048 buckets over the key
+// range still in play, [lo, hi], narrow it to the k-th largest key, starting from the
+// row's shared threshold (the largest the clusters published: one cluster alone holds k
+// pairs at or above it); then one output pass takes the keys above the pivot and the
+// quota of pivot-equal keys, slots from two shared cursors.
 template <typename KeyT>
 __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeParams p) {
     constexpr int NT = kMergeThreads;
     constexpr int ES = sizeof(KeyT);
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const MergeLayout L = merge_layout(ES, p.cap);
-    KeyT* ckey = reinterpret_cast<KeyT*>(smem + L.ckey);
-    uint32_t* cidx = reinterpret_cast<uint32_t*>(smem + L.cidx);
-    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + L.hist);
-    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.ctrl);
+    __shared__ __align__(16) uint32_t hist[kBins];
+    __shared__ int sh_b;
+    __shared__ uint32_t sh_above, sh_total;
+    __shared__ unsigned int cur_g, cur_e;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row = blockIdx.x;
-    if (tid == 0) {
-        int* z = reinterpret_cast<int*>(ctrl);
-        for (size_t i = 0; i < sizeof(Ctrl) / sizeof(int); ++i) z[i] = 0;
-    }
-    uint32_t lo_g = 0u;
+    const int64_t seg0 = row * p.C;
+    uint32_t lo = 0u;
     {
         const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo_g = static_cast<uint32_t>(g);
+        if (static_cast<uint32_t>(g >> 32) == p.epoch) lo = static_cast<uint32_t>(g);
     }
-    __syncthreads();
-    int n = 0, blk = 0;
-    bool hasT = false;
-    uint32_t T = 0u, wcnt = 0u, tmax = 0u;
-    for (int c = 0; c < p.C; ++c) {
-        const int64_t seg = row * p.C + c;
-        const int cnt = p.ws_cnt[seg];
-        const uint32_t* sk = p.ws_key + seg * p.k;
-        const int32_t* si = p.ws_idx + seg * p.k;
-        for (int t0 = 0; t0 < cnt; t0 += kMergeTile) {
-            const int te = (cnt - t0) < kMergeTile ? (cnt - t0) : kMergeTile;
-            for (int base = warp * 32; base < te; base += NT) {
-                const int j = base + lane;
-                const bool valid = j < te;
-                const uint32_t key = valid ? sk[t0 + j] : 0u;
-                const bool hit = valid && key >= lo_g && (!hasT || key > T);
-                const uint32_t hmask = __ballot_sync(0xFFFFFFFFu, hit);
-                if (hmask) {
-                    const uint32_t pos = warp_reserve(ctrl, __popc(hmask), lane) + __popc(hmask & lanemask_lt());
-                    if (hit) {
-                        if (pos < static_cast<uint32_t>(p.cap)) {
-                            ckey[pos] = static_cast<KeyT>(key);
-                            cidx[pos] = static_cast<uint32_t>(si[t0 + j]);
-                        } else {
-                            set_status(kErrOverflow);
-                        }
-                        tmax = max(tmax, key);
-                    }
-                    wcnt += __popc(hmask);
-                }
+    const uint32_t lo0 = lo;
+    uint32_t hi = ES == 2 ? 0xFFFFu : 0xFFFFFFFFu;
+    uint32_t krem = static_cast<uint32_t>(p.k), pivot = 0u, total0 = 0u;
+    bool take_all = false;
+    if (tid == 0) {
+        cur_g = 0u;
+        cur_e = 0u;
+    }
+    for (int pass = 0;; ++pass) {
+        const int sb = bit_length(hi - lo) - kDigitBits;
+        const int s = sb > 0 ? sb : 0;
+        for (int b = tid; b < kBins; b += NT) hist[b] = 0u;
+        __syncthreads();
+        for (int c = 0; c < p.C; ++c) {
+            const int cnt = p.ws_cnt[seg0 + c];
+            const uint32_t* sk = p.ws_key + (seg0 + c) * p.k;
+            for (int j = tid; j < cnt; j += NT) {
+                const uint32_t key = sk[j];
+                if (key >= lo && key <= hi) atomicAdd(&hist[(key - lo) >> s], 1u);
             }
-            if (lane == 0) ctrl->block_cnt[blk & 1][warp] = wcnt;
-            wcnt = 0u;
-            __syncthreads();
-            uint32_t add = 0u;
-#pragma unroll
-            for (int w = 0; w < NT / 32; ++w) add += ctrl->block_cnt[blk & 1][w];
-            n += static_cast<int>(add);
-            ++blk;
-            if (n >= p.k + p.B2) {
-                const uint32_t lo_k = hasT ? T : lo_g;
-                T = compact<KeyT, NT, 0>(ckey, cidx, hist, ctrl, n, p.k, lo_k, tmax, tid);
-                hasT = true;
-                n = p.k;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            int b;
+            uint32_t above, total;
+            warp_bucket_2048(hist, krem, lane, b, above, total);
+            if (lane == 0) {
+                sh_b = b;
+                sh_above = above;
+                sh_total = total;
+            }
+        }
+        __syncthreads();
+        const int b = sh_b;
+        const uint32_t above = sh_above;
+        if (pass == 0) total0 = sh_total;
+        __syncthreads();  // sh_* are read before the next pass writes them
+        if (b < 0) {  // fewer than krem keys in play: keep them all
+            take_all = true;
+            break;
+        }
+        krem -= above;
+        lo += static_cast<uint32_t>(b) << s;
+        if (s == 0) {
+            pivot = lo;
+            break;
+        }
+        hi = lo + ((1u << s) - 1u);
+    }
+    if (take_all && tid == 0 && total0 < static_cast<uint32_t>(p.k)) set_status(kErrInternal);
+    // keys above the pivot take slots [0, k - krem), pivot-equal keys the next krem
+    const uint32_t ngt = static_cast<uint32_t>(p.k) - krem;
+    const uint32_t ltm = lanemask_lt();
+    const int64_t obase = row * static_cast<int64_t>(p.k);
+    for (int c = 0; c < p.C; ++c) {
+        const int cnt = p.ws_cnt[seg0 + c];
+        const uint32_t* sk = p.ws_key + (seg0 + c) * p.k;
+        const int32_t* si = p.ws_idx + (seg0 + c) * p.k;
+        for (int j0 = 0; j0 < cnt; j0 += NT) {
+            const int j = j0 + tid;
+            const uint32_t key = j < cnt ? sk[j] : 0u;
+            const bool ok = j < cnt && key >= lo0;
+            const bool isg = ok && (take_all || key > pivot);
+            const bool ise = ok && !take_all && key == pivot;
+            const uint32_t bg = __ballot_sync(0xFFFFFFFFu, isg);
+            const uint32_t be = __ballot_sync(0xFFFFFFFFu, ise);
+            if ((bg | be) == 0u) continue;
+            uint32_t gb = 0u, eb = 0u;
+            if (lane == 0) {
+                if (bg) gb = atomicAdd(&cur_g, static_cast<unsigned int>(__popc(bg)));
+                if (be) eb = atomicAdd(&cur_e, static_cast<unsigned int>(__popc(be)));
+            }
+            gb = __shfl_sync(0xFFFFFFFFu, gb, 0) + static_cast<uint32_t>(__popc(bg & ltm));
+            eb = __shfl_sync(0xFFFFFFFFu, eb, 0) + static_cast<uint32_t>(__popc(be & ltm));
+            const uint32_t slot = isg ? gb : ngt + eb;
+            const bool put = isg || (ise && eb < krem);
+            if (put && slot < static_cast<uint32_t>(p.k)) {
+                if (ES == 2) static_cast<uint16_t*>(p.out_vals)[obase + slot] = static_cast<uint16_t>(unkey_bf16(key));
+                else static_cast<uint32_t*>(p.out_vals)[obase + slot] = unkey_f32(key);
+                p.out_idx[obase + slot] = si[j];
+            } else if (put) {
+                set_status(kErrInternal);
             }
         }
     }
-    {
-        const uint32_t wm = warp_max(tmax);
-        if (lane == 0) atomicMax(&ctrl->maxkey, wm);
-    }
-    __syncthreads();
-    OutTarget out;
-    out.vals = p.out_vals;
-    out.idx = p.out_idx;
-    out.base = row * static_cast<int64_t>(p.k);
-    out.to_keys = false;
-    out.esize = ES;
-    final_select<KeyT, NT>(ckey, cidx, hist, ctrl, n, p.k, hasT ? T : lo_g, ctrl->maxkey, out, true, tid);
 }
 
 // ================================================================ host ============
@@ -916,9 +964,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.merge_smem = 0;
     P.merge_cap = 0;
     if (P.C > 1) {
-        P.merge_cap = k + kMergeTile + B2;
-        P.merge_smem = merge_layout(P.es, P.merge_cap).total;
-        if (P.merge_smem > static_cast<size_t>(di.smem_optin)) return DS_ERR_UNSUPPORTED;
+        P.merge_cap = k;
+        P.merge_smem = 0;  // the merge kernel's shared memory is static
         size_t off = 0;
         P.off_gT = off;
         off = align_up(off + rows * 8, 256);
