@@ -90,10 +90,16 @@ typedef enum {
  *   out_vals    device, rows*k elements of dtype; 16-byte aligned.  Caller-owned.
  *   out_idx     device, rows*k int32; 16-byte aligned.  Caller-owned.
  *   stream      CUDA stream (0 = legacy default stream).
- * The library chooses how many CTAs share a row.  When a row is split over more than
- * one thread-block cluster it uses a library-owned per-device workspace, grown with
- * cudaMalloc on a call that is not being stream-captured (a call under capture that
- * would need to grow it returns DS_ERR_WORKSPACE).
+ * The library chooses how many CTAs share a row: rows split over a cluster, or rows
+ * that already fill the GPU one per CTA, run the split-row kernel (warm-up threshold
+ * from a sample of the row, compaction when a chunk's survivors do not fit); only
+ * ds_topk_ex with parts = 1 runs the pages' one-CTA schedule exactly.  When a row is
+ * split over more than one thread-block cluster it uses a library-owned per-device
+ * workspace, grown with cudaMalloc on a call that is not being stream-captured (a call
+ * under capture that would need to grow it returns DS_ERR_WORKSPACE).  Launches let the
+ * next kernel on the stream start as this one's CTAs leave (programmatic dependent
+ * launch); a call reads x only once the kernel before it has completed (see
+ * ds_options.input_ready).
  */
 ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride,
                   int32_t k, int32_t B, int32_t B2, uint64_t seed, void* out_vals,
