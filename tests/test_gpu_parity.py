@@ -359,3 +359,32 @@ def test_many_short_rows_k_up_to_n(dtype, k):
     assert plan["parts"] == 1 and plan["threads"] == 256
     v, i, _ = run_gpu(x, dtype, k, B, B, 23)
     check_topk(x, dtype, k, v, i)
+
+
+def test_many_rows_special_values_and_input_ready():
+    """One CTA per row in the split-row kernel on rows full of signed zeros, infinities,
+    NaNs of both signs and denormals; the same calls stating their inputs were ready
+    before the previous call started give the same results."""
+    import top_selection_gb300 as ds
+    specials = np.array([0x00000000, 0x80000000, 0x7FC00000, 0xFFC00000, 0x7F800000, 0xFF800000,
+                         0x00000001, 0x80000001, 0x3F800000, 0xBF800000, 0x40000000, 0xC0000000],
+                        dtype=np.uint32)
+    rng = np.random.default_rng(91)
+    rows, N, k, B = 160, 8192, 300, 512
+    x = specials[rng.integers(0, len(specials), size=(rows, N))].view(np.float32)
+    x[:, ::7] = rng.standard_normal((rows, len(range(0, N, 7)))).astype(np.float32)
+    plan = ds.ds_get_plan(synth.FP32, rows, N, k, B, B)
+    assert plan["parts"] == 1 and plan["threads"] == 256
+    xt = to_device(x, synth.FP32)
+    outs = []
+    for ready in (False, True):
+        vals = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+        idx = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        ds.topk(xt, k, B, B, seed=4, out=(vals, idx), input_ready=ready)
+        ds.topk(xt, k, B, B, seed=4, out=(vals, idx), input_ready=ready)
+        torch.cuda.synchronize()
+        assert ds.ds_get_device_status() == 0
+        v, i = vals.cpu().numpy().view(np.uint32), idx.cpu().numpy()
+        check_topk(x, synth.FP32, k, v, i)
+        outs.append(np.sort(v, axis=1))
+    assert np.array_equal(outs[0], outs[1])
