@@ -54,6 +54,8 @@ struct Ctrl {
     uint32_t fin_T;
     int out_g;                   // split rows: output cursors of the final select (keys above
     int out_e;                   // the pivot, pivot-equal keys)
+    uint32_t raise_mark;         // split rows: buffer count at which a warp next raises T from
+                                 //   the appended keys' histogram (0 = the first mark)
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

@@ -452,6 +452,7 @@ __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, ui
     if (tid == 0) {
         ctrl->compact_req = 0;
         ctrl->fail_base = 0x7FFFFFFF;
+        ctrl->raise_mark = 0u;
     }
     // The threshold bounds the cluster's union, not this buffer alone, so the compaction
     // ranks every key of the buffer.
@@ -466,6 +467,20 @@ __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, ui
     named_bar_sync(2, NC);
     for (int i = tid; i < k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
     return nt;
+}
+
+// A threshold raise by one warp, from the first final histogram of the keys appended so
+// far (bins of 2^hs keys from `edge` up): the smallest key of the bin that holds the k-th
+// largest appended key, less one, is at most the row's k-th largest key.  Returns it, or 0
+// when the histogram holds fewer than k keys or the bin is the lowest.  Counts read while
+// other warps append are never above the final ones, so the bound holds.  Out of line, as
+// it runs a few times per call.
+template <typename KeyT>
+__device__ __noinline__ uint32_t split_raise(const uint32_t* xh0, int k, uint32_t edge, int hs, int lane) {
+    const XPivot r = warp_pivot_x(xh0, 1, 0, static_cast<uint32_t>(k), lane);
+    if (r.bstar <= 0) return 0u;
+    const uint64_t lo = static_cast<uint64_t>(edge) + (static_cast<uint64_t>(r.bstar) << hs);
+    return lo - 1u <= (sizeof(KeyT) == 2 ? 0xFFFFull : 0xFFFFFFFFull) ? static_cast<uint32_t>(lo - 1u) : 0u;
 }
 
 // The final select's output: one pass over this CTA's n candidates, four per thread at
@@ -668,7 +683,6 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         uint32_t* const xh0 = reinterpret_cast<uint32_t*>(smem + L.xf) + static_cast<size_t>(crank) * (kXBins / 2);
         uint32_t hedge = 0u;
         int hs0 = KW - kXBits;
-        // every consumer warp calls this together (from its chunk loop or the drain)
         // every consumer warp calls this together (from its chunk loop or the drain); the
         // work is out of line, away from the chunk loop's code
         const auto join_compaction = [&]() {
@@ -872,7 +886,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             bool have = hasT;
             {
                 uint32_t sh = gnext;
-                if (G > 1 && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+                if ((G > 1 || p.rstep) && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
                 sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
                 if (sh != 0u && (!have || sh > tk)) {
                     tk = sh;
@@ -918,6 +932,22 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     ++bj;
                 }
                 issue_to(s, use + 1, bj, sj);
+            }
+            if (p.rstep) {  // one warp raises the threshold each time the buffer passes the mark
+                int due = 0;
+                if (lane == 0) {
+                    const uint32_t c = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&ctrl->cnt));
+                    const uint32_t mk = *reinterpret_cast<volatile uint32_t*>(&ctrl->raise_mark);
+                    if (c >= (mk ? mk : static_cast<uint32_t>(p.rmark)))
+                        due = atomicCAS(&ctrl->raise_mark, mk, c + static_cast<uint32_t>(p.rstep)) == mk;
+                }
+                if (__shfl_sync(0xFFFFFFFFu, due, 0)) {
+                    const uint32_t t = split_raise<KeyT>(xh0, p.k, hedge, hs0, lane);
+                    if (lane == 0 && t != 0u) {
+                        if (G > 1 || MC) publish_T(t);
+                        else atomicMax(&ctrl->sharedT, t);
+                    }
+                }
             }
             bi += d8;
             sub += r8;

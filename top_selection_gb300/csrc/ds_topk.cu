@@ -90,6 +90,8 @@ struct ScanParams {
     int32_t mr;                   //   m % parts: parts [0, mr) get mq + 1 blocks, the rest mq
     int64_t mq;                   //   m / parts
     int32_t early;                // start reading x before the previous kernel completes
+    int32_t rmark, rstep;         // split rows: raise T from the appended keys' histogram when the
+                                  //   buffer holds rmark keys, then every rstep more (0 = never)
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
     uint32_t* ws_key;             // per (row, cluster) partial results (C > 1)
@@ -1035,6 +1037,10 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     sp.mq = P.m / P.parts;
     sp.mr = static_cast<int32_t>(P.m % P.parts);
     sp.early = early ? 1 : 0;
+    // Streamed rows raise their threshold from the appended keys' histogram: first when
+    // the buffer holds k keys plus a step (or half of its room past k), then every step.
+    sp.rstep = P.split && P.refine ? (k > 256 ? k : 256) : 0;
+    sp.rmark = sp.rstep ? k + (sp.rstep < (P.cap - k) / 2 ? sp.rstep : (P.cap - k) / 2) : 0;
     sp.epoch = 0;
     sp.gT = nullptr;
     sp.ws_key = nullptr;
