@@ -199,6 +199,16 @@ def test_workload_longctx_bf16(kind, k):
     _auto(synth.longctx_bf16(kind), k)
 
 
+@pytest.mark.parametrize("seed", [1, 2, 3, 4])
+def test_longctx_ascending_compactions_make_progress(seed):
+    # On ascending rows every element passes the threshold, so compactions follow one
+    # another and each must leave room for a whole pass; the block order decides which
+    # keys the cuts meet.
+    w = synth.longctx_bf16("ascending")
+    v, i, _ = run_gpu(w.x, w.dtype, 2048, w.B, w.B2, seed, N=w.N)
+    check_topk(w.x, w.dtype, 2048, v, i, N=w.N, threads=16)
+
+
 @pytest.mark.parametrize("k", [32, 4096])
 def test_workload_huge_f32(k):
     w = synth.huge_f32()

@@ -56,6 +56,9 @@ struct Ctrl {
     int out_e;                   // the pivot, pivot-equal keys)
     uint32_t raise_mark;         // split rows: buffer count at which a warp next raises T from
                                  //   the appended keys' histogram (0 = the first mark)
+    int cut_bin;                 // split rows: a compaction's cut from that histogram (bin,
+    uint32_t cut_keep;           //   keys kept)
+    int last_kept;               // split rows: the buffer's count after the last compaction
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

@@ -430,42 +430,126 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
     return true;
 }
 
-// A compaction that every consumer thread of a split-row CTA joins: the buffer's slots
-// [0, min(first failed reservation, count)) are cut to the k largest keys, the threshold
-// becomes max(T, the k-th key) and is pushed to every CTA of the cluster (and to the
-// row's global word gT, tagged with the call's epoch, when the row spans clusters), and
-// the final select's first histogram is counted anew over the kept keys.  Returns the
-// new threshold.  Out of line: it runs rarely, and its code then stays out of the chunk
-// loop's instruction stream.
+// A compaction that every consumer thread of a split-row CTA joins.  The buffer's slots
+// [0, min(first failed reservation, count)) are cut down, the threshold rises and is pushed
+// to every CTA of the cluster (and to the row's global word gT, tagged with the call's
+// epoch, when the row spans clusters).  Returns the new threshold.
+//   The first final histogram counts every key of those slots (bins of 2^hs0 keys from
+// hedge up).  Its bin b* holding the k-th largest key gives a cut: the keys of bins b*
+// and above, at least k of them, stay (in slot order, moved down one tile at a time) and
+// the threshold becomes the bin's smallest key less one.  When that keeps too many keys
+// (a wide or crowded bin) or b* is the lowest bin, the buffer is cut to exactly the k
+// largest keys instead (a radix select) and the histogram is counted anew.  Either way at
+// least `room` slots (one chunk, the most one pass reserves) are free afterwards, so the
+// pass that failed to reserve, retried, fits unless other warps' passes took the room
+// first: every compaction is followed by at least one appended pass.  Out of line: it
+// runs rarely, and its code then stays out of the chunk loop's instruction stream.
 template <typename KeyT>
 __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int cap,
-                                                  int k, uint32_t tmax, int tid, bool hasT, uint32_t T, uint32_t* xh0,
+                                                  int room, int k, uint32_t tmax, int tid, bool hasT, uint32_t T,
+                                                  uint32_t* xh0,
                                                   uint32_t hedge, int hs0, int G, unsigned long long* gT,
                                                   uint32_t epoch) {
     constexpr int NC = kSplitThreads;
+    const int lane = tid & 31;
     named_bar_sync(2, NC);
     const int fb = *reinterpret_cast<volatile int*>(&ctrl->fail_base);
     const int cn = *reinterpret_cast<volatile int*>(&ctrl->cnt);
     int n = fb < cn ? fb : cn;
     n = n < cap ? n : cap;  // (a bound only: reservations never pass cap)
+    // No pass appended since the last compaction: another would change nothing.  This
+    // cannot happen (see above); if it did, the CTA reports it and stops instead of looping.
+    const bool stuck = n == ctrl->last_kept;
+    if (tid < 32 && !stuck) {
+        const XPivot r = warp_pivot_x(xh0, 1, 0, static_cast<uint32_t>(k), lane);
+        if (lane == 0) {
+            int cb = -1;
+            uint32_t keep = 0u;
+            if (r.bstar > 0) {
+                const uint64_t lo = static_cast<uint64_t>(hedge) + (static_cast<uint64_t>(r.bstar) << hs0);
+                if (lo - 1u <= (sizeof(KeyT) == 2 ? 0xFFFFull : 0xFFFFFFFFull)) {
+                    cb = r.bstar;
+                    keep = r.above + reinterpret_cast<const uint16_t*>(xh0)[r.bstar];
+                }
+            }
+            ctrl->cut_bin = cb;
+            ctrl->cut_keep = keep;
+        }
+    }
     named_bar_sync(2, NC);
     if (tid == 0) {
         ctrl->compact_req = 0;
         ctrl->fail_base = 0x7FFFFFFF;
         ctrl->raise_mark = 0u;
     }
-    // The threshold bounds the cluster's union, not this buffer alone, so the compaction
-    // ranks every key of the buffer.
-    const uint32_t piv = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, k, 0u, tmax, tid, true);
-    const uint32_t nt = hasT && T > piv ? T : piv;
+    if (stuck) {
+        if (tid == 0) {
+            set_status(kErrInternal);
+            *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+        }
+        named_bar_sync(2, NC);
+        return T;
+    }
+    const int cb = ctrl->cut_bin;
+    const uint32_t keep = ctrl->cut_keep;
+    uint32_t nt;
+    if (cb > 0 && keep <= static_cast<uint32_t>(k + (cap - k) / 2) && keep + static_cast<uint32_t>(room) <= static_cast<uint32_t>(cap)) {
+        const uint32_t lo = hedge + (static_cast<uint32_t>(cb) << hs0);
+        constexpr int PER = 4;
+        uint32_t off = 0u;
+        for (int t0 = 0, it = 0; t0 < n; t0 += NC * PER, ++it) {
+            KeyT kk[PER];
+            uint32_t ii[PER];
+            uint32_t c = 0u, f = 0u;
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                const int i = t0 + tid + NC * j;
+                kk[j] = 0;
+                ii[j] = 0u;
+                if (i < n) {
+                    kk[j] = ckey[i];
+                    ii[j] = cidx[i];
+                    if (static_cast<uint32_t>(kk[j]) >= lo) {
+                        f |= 1u << j;
+                        ++c;
+                    }
+                }
+            }
+            uint32_t total;
+            // the scan's barrier also orders every read of this tile before its writes
+            uint32_t d = off + team_excl_scan<NC, 2>(c, ctrl, it & 1, total, tid);
+#pragma unroll
+            for (int j = 0; j < PER; ++j) {
+                if (f & (1u << j)) {
+                    ckey[d] = kk[j];
+                    cidx[d] = ii[j];
+                    ++d;
+                }
+            }
+            off += total;
+        }
+        if (off != keep) set_status(kErrInternal);
+        // the bins below the cut are empty now
+        for (int i = tid; i < (cb >> 1); i += NC) xh0[i] = 0u;
+        if ((cb & 1) && tid == 0) xh0[cb >> 1] &= 0xFFFF0000u;
+        if (tid == 0) ctrl->cnt = static_cast<int>(off);
+        nt = hasT && T > lo - 1u ? T : lo - 1u;
+    } else {
+        // The threshold bounds the cluster's union, not this buffer alone, so the
+        // compaction ranks every key of the buffer.
+        const uint32_t piv = compact<KeyT, NC, 1>(ckey, cidx, hist, ctrl, n, k, 0u, tmax, tid, true);
+        nt = hasT && T > piv ? T : piv;
+        // the first final histogram, counted anew over the k keys kept
+        for (int i = tid; i < kXBins / 2; i += NC) xh0[i] = 0u;
+        named_bar_sync(2, NC);
+        for (int i = tid; i < k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
+    }
     if (tid == 0) {
         for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), nt);
         if (gT) atomicMax(gT, (static_cast<unsigned long long>(epoch) << 32) | nt);
+        ctrl->last_kept = ctrl->cnt;
     }
-    // the first final histogram, counted anew over the k keys kept
-    for (int i = tid; i < kXBins / 2; i += NC) xh0[i] = 0u;
-    named_bar_sync(2, NC);
-    for (int i = tid; i < k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
+    named_bar_sync(2, NC);  // the buffer, its count and the histogram are settled
     return nt;
 }
 
@@ -686,7 +770,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // every consumer warp calls this together (from its chunk loop or the drain); the
         // work is out of line, away from the chunk loop's code
         const auto join_compaction = [&]() {
-            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.k, tmax, tid, hasT, T, xh0, hedge, hs0, G,
+            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.chunk, p.k, tmax, tid, hasT, T, xh0, hedge, hs0, G,
                                        MC ? p.gT + row : nullptr, p.epoch);
             hasT = true;
         };
