@@ -23,9 +23,13 @@
 //     packed values against T with one instruction per word, a shuffle scan places the
 //     lanes' survivors, one shared atomic per warp reserves their slots, and the warp
 //     writes them in two steps (columns per lane, then keys and columns for the warp's
-//     slots in order), counting each key into the final select's first histogram.  A
-//     reservation that does not fit makes every warp join a RadixSelectTopK compaction
-//     of the CTA's buffer to k (which raises T); the warp then resumes where it stopped.
+//     slots in order), counting each key into the final select's first histogram.  On
+//     rows streamed through the ring, a warp raises T from that histogram each time the
+//     buffer passes a mark (just below the bin of the k-th largest appended key).  A
+//     reservation that does not fit makes every warp join a compaction of the CTA's
+//     buffer: a cut at the histogram bin of the k-th largest key where that frees
+//     enough room, else a RadixSelectTopK to exactly k; either raises T, and the warp
+//     then resumes where it stopped.
 //   * Final: the cluster selects the k largest keys of the union of its buffers by
 //     most-significant-digit radix passes over 512 bins.  Each pass, every CTA pushes
 //     its histogram to every other CTA; warp 0 of every CTA then finds the same pivot bin
