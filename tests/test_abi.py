@@ -129,3 +129,44 @@ def test_plans_on_a_described_device(lib):
         if p["threads"] == 256:
             assert p["stages"] in (8, 16), n          # warp-owned stages
             assert p["ctas_per_sm"] == 2, n
+
+
+_PLAN_SWEEP = """
+import json, top_selection_gb300 as ds
+ds.load()
+out = []
+for dtype in (0, 1):
+    for rows in (1, 3, 64, 256, 2048):
+        for N in (1000, 4097, 65536, 131072, 1048576, 16777216):
+            for k in (1, 64, 512, 2048, 4096):
+                for B, B2 in ((1024, 1024), (4096, 4096), (8192, 4096)):
+                    if k > N:
+                        continue
+                    try:
+                        p = ds.ds_get_plan(dtype, rows, N, k, B, B2)
+                    except Exception:
+                        continue
+                    out.append([dtype, rows, N, k, B, B2, p])
+print(json.dumps(out))
+"""
+
+
+def test_split_plans_leave_a_chunk_of_room():
+    """Every split-row plan over a sweep of shapes (no GPU needed) keeps a candidate buffer
+    of at least k + one chunk: after a compaction to k a whole pass (at most one chunk of
+    survivors) fits, which the compaction's progress rests on; the buffer also stays
+    below 2^16 entries, the range of the final select's 16-bit bin counts."""
+    import json
+    import sys
+    env = dict(os.environ, DS_PLAN_DEVICE="152,232448,233472", CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", _PLAN_SWEEP], env=env, cwd=ROOT, capture_output=True,
+                         text=True, check=True).stdout
+    plans = json.loads(out.strip().splitlines()[-1])
+    split = [r for r in plans if r[6]["threads"] == 256]
+    assert len(split) > 100
+    for dtype, rows, N, k, B, B2, p in split:
+        es = 2 if dtype == 0 else 4
+        assert p["capacity"] >= k + p["chunk_elems"], (dtype, rows, N, k, B, B2, p)
+        assert p["capacity"] < 1 << 16, (dtype, rows, N, k, B, B2, p)
+        assert (p["chunk_elems"] * es) % 16 == 0, (dtype, rows, N, k, B, B2, p)
+        assert p["stages"] in (8, 16), (dtype, rows, N, k, B, B2, p)
