@@ -134,13 +134,19 @@ typedef struct {
     int32_t threads;        /* threads per CTA                                         */
     int32_t chunk_elems;    /* elements per bulk copy                                  */
     int32_t stages;         /* depth of the copy ring                                  */
-    int32_t capacity;       /* candidate-buffer entries (k + B + B2)                   */
+    int32_t capacity;       /* candidate-buffer entries: k + B + B2 for rows of one CTA;
+                               at least k + one chunk for split rows, widened into the
+                               shared memory the layout leaves over                    */
     int64_t smem_bytes;     /* dynamic shared memory per CTA                           */
     int64_t workspace_bytes;/* device workspace needed (0 unless split over clusters)  */
     int32_t ctas_per_sm;    /* resident CTAs per SM for this configuration             */
     int32_t merge_launch;   /* 1 when a second (merge) kernel runs                      */
 } ds_plan;
 
+/* Errors as ds_topk's host checks (DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED), and
+   DS_ERR_CUDA when no device can be queried.  Without a device, the environment variable
+   DS_PLAN_DEVICE="sms,smem_optin,smem_per_sm" (SM count and the two shared-memory limits
+   in bytes) describes one, for planning only; launches still need the real device. */
 ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t B, int32_t B2,
                       const ds_options* options, ds_plan* plan);
 
