@@ -386,7 +386,9 @@ def run_gpu(args):
     alg_bytes = step_bytes + ROWS * K_TOP * (sh.es + 4)
     peak, peak_kind = _peak()
     achieved = alg_bytes / (ms / args.steps * 1e-3) / 1e9
-    kname = ("ds_scan_kernel" if plan["parts"] == 1 else "ds_split_kernel") + \
+    # the split-row kernel runs 256 threads per CTA (also for one part per row), the
+    # one-CTA-per-row kernel 288
+    kname = ("ds_split_kernel" if plan["threads"] == 256 else "ds_scan_kernel") + \
         ("<uint16_t>" if sh.bf16 else "<uint32_t>")
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(sh),
