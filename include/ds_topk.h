@@ -94,9 +94,13 @@ typedef enum {
  * that already fill the GPU one per CTA, run the split-row kernel (warm-up threshold
  * from a sample of the row, compaction when a chunk's survivors do not fit); only
  * ds_topk_ex with parts = 1 runs the pages' one-CTA schedule exactly.  When a row is
- * split over more than one thread-block cluster it uses a library-owned per-device
- * workspace, grown with cudaMalloc on a call that is not being stream-captured (a call
- * under capture that would need to grow it returns DS_ERR_WORKSPACE).  Launches let the
+ * split over more than one thread-block cluster it uses a library-owned workspace, one
+ * per (device, stream) -- per thread as well for cudaStreamPerThread -- so calls on
+ * different streams may run concurrently.  It is grown with cudaMalloc (and cleared with
+ * cudaMemsetAsync on `stream`) on a call that is not being stream-captured; a call under
+ * capture that would need to grow it returns DS_ERR_WORKSPACE.  An outgrown workspace is
+ * kept, not freed, until the process exits (launches already enqueued may still use it),
+ * so growing never synchronises the device.  Launches let the
  * next kernel on the stream start as this one's CTAs leave (programmatic dependent
  * launch); a call reads x only once the kernel before it has completed (see
  * ds_options.input_ready).

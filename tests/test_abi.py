@@ -170,3 +170,28 @@ def test_split_plans_leave_a_chunk_of_room():
         assert p["capacity"] < 1 << 16, (dtype, rows, N, k, B, B2, p)
         assert (p["chunk_elems"] * es) % 16 == 0, (dtype, rows, N, k, B, B2, p)
         assert p["stages"] in (8, 16), (dtype, rows, N, k, B, B2, p)
+
+
+def test_build_tracks_every_source_file():
+    """Every CUDA source or header under csrc/ and every public header is a build input,
+    so editing any of them makes the in-tree library out of date."""
+    from top_selection_gb300 import build
+    deps = set(build.deps())
+    for d, exts in ((build.CSRC, (".cu", ".cuh", ".h")), (build.INCLUDE, (".h",))):
+        for f in os.listdir(d):
+            if f.endswith(exts):
+                assert os.path.join(d, f) in deps, f
+
+
+def test_touching_a_kernel_header_marks_the_library_stale(lib):
+    from top_selection_gb300 import build
+    assert build.up_to_date()
+    split = os.path.join(build.CSRC, "ds_split.cuh")
+    st = os.stat(split)
+    try:
+        t = os.path.getmtime(build.LIB) + 10
+        os.utime(split, (t, t))
+        assert not build.up_to_date()
+    finally:
+        os.utime(split, ns=(st.st_atime_ns, st.st_mtime_ns))
+    assert build.up_to_date()

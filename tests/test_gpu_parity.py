@@ -398,3 +398,37 @@ def test_many_rows_special_values_and_input_ready():
         check_topk(x, synth.FP32, k, v, i)
         outs.append(np.sort(v, axis=1))
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_concurrent_streams_multi_cluster_rows():
+    """Rows split over several clusters use a library workspace; calls on two streams at
+    the same time (no ordering between them) each get their own, so both results are
+    right.  A larger call on one stream then grows that stream's workspace while work
+    enqueued earlier may still use the old one."""
+    import top_selection_gb300 as ds
+    rng = np.random.default_rng(404)
+    xa = rng.standard_normal((3, 400000)).astype(np.float32)
+    xb = rng.standard_normal((3, 400000)).astype(np.float32)
+    ta, tb = to_device(xa, synth.FP32), to_device(xb, synth.FP32)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = {}
+    torch.cuda.synchronize()
+    for rep in range(4):
+        for name, t, s in (("a", ta, sa), ("b", tb, sb)):
+            with torch.cuda.stream(s):
+                v = torch.empty((3, 512), dtype=torch.float32, device="cuda")
+                i = torch.empty((3, 512), dtype=torch.int32, device="cuda")
+                ds.topk(t, 512, 4096, 4096, seed=rep, out=(v, i), parts=16, cluster=4, stream=s.cuda_stream)
+                outs[(name, rep)] = (v, i)
+    with torch.cuda.stream(sa):   # more rows: stream a's workspace grows
+        xc = rng.standard_normal((9, 400000)).astype(np.float32)
+        tc = to_device(xc, synth.FP32)
+        vc = torch.empty((9, 512), dtype=torch.float32, device="cuda")
+        ic = torch.empty((9, 512), dtype=torch.int32, device="cuda")
+        ds.topk(tc, 512, 4096, 4096, seed=9, out=(vc, ic), parts=16, cluster=4, stream=sa.cuda_stream)
+    torch.cuda.synchronize()
+    assert ds.ds_get_device_status() == 0
+    for (name, rep), (v, i) in outs.items():
+        x = xa if name == "a" else xb
+        check_topk(x, synth.FP32, 512, v.cpu().numpy().view(np.uint32), i.cpu().numpy())
+    check_topk(xc, synth.FP32, 512, vc.cpu().numpy().view(np.uint32), ic.cpu().numpy())

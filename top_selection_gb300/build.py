@@ -11,8 +11,15 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libds_topk.so")
 SOURCES = [os.path.join(CSRC, "ds_topk.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ds_common.cuh", "ds_select.cuh")] + [
-    os.path.join(INCLUDE, "ds_topk.h")]
+
+
+def deps() -> list:
+    """Every file the library is built from: the CUDA sources and headers under csrc/ and
+    the public headers (globbed, so a new or edited header always triggers a rebuild)."""
+    out = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".cu", ".cuh", ".h"))]
+    out += [os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h")]
+    out.append(os.path.abspath(__file__))
+    return out
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-shared", "-Xcompiler", "-fPIC", "-I" + INCLUDE]
@@ -29,7 +36,7 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(d) <= t for d in DEPS)
+    return all(os.path.getmtime(d) <= t for d in deps())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

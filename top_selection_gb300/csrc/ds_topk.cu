@@ -32,6 +32,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <thread>
+#include <unordered_map>
+#include <vector>
 
 #include "ds_common.cuh"
 #include "ds_select.cuh"
@@ -748,11 +751,31 @@ static std::mutex g_mu;
 static DevInfo g_dev[64];
 static std::atomic<uint32_t> g_epoch{0};
 
+// Library-owned workspaces (rows split over several clusters), one per (device, stream):
+// calls on one stream are ordered, so they may share a workspace; calls on different
+// streams never do.  The per-thread default stream is a different stream in every thread,
+// so it is keyed by thread as well.  A workspace that is outgrown is retired, not freed:
+// a launch already enqueued (on this or an earlier call) may still use it, and freeing it
+// safely would need a device-wide synchronisation.  Growth is geometric, so the retired
+// buffers hold less than the live one.
 struct Workspace {
     void* ptr = nullptr;
     size_t bytes = 0;
 };
-static Workspace g_ws[64];
+struct WsKey {
+    int dev;
+    cudaStream_t stream;
+    std::thread::id thread;
+    bool operator==(const WsKey& o) const { return dev == o.dev && stream == o.stream && thread == o.thread; }
+};
+struct WsKeyHash {
+    size_t operator()(const WsKey& k) const {
+        return std::hash<const void*>()(k.stream) ^ (std::hash<std::thread::id>()(k.thread) << 1) ^
+               static_cast<size_t>(k.dev) * 0x9E3779B97F4A7C15ull;
+    }
+};
+static std::unordered_map<WsKey, Workspace, WsKeyHash> g_ws;
+static std::vector<void*> g_ws_retired;
 
 // Scratch for ds_topk_noalloc: a fixed array in the library's device image.  Every device
 // that loads the library holds it until the process exits; calls share it.
@@ -1109,8 +1132,10 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
 }
 
 static ds_status library_workspace(int dev, size_t bytes, cudaStream_t stream, void** out) {
+    const bool per_thread = stream == cudaStreamPerThread;
+    const WsKey key{dev, stream, per_thread ? std::this_thread::get_id() : std::thread::id()};
     std::lock_guard<std::mutex> lk(g_mu);
-    Workspace& w = g_ws[dev];
+    Workspace& w = g_ws[key];
     if (w.bytes >= bytes) {
         *out = w.ptr;
         return DS_OK;
@@ -1118,19 +1143,16 @@ static ds_status library_workspace(int dev, size_t bytes, cudaStream_t stream, v
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DS_ERR_CUDA;
     if (cs != cudaStreamCaptureStatusNone) return DS_ERR_WORKSPACE;
-    if (w.ptr) {
-        if (cudaDeviceSynchronize() != cudaSuccess) return DS_ERR_CUDA;
-        cudaFree(w.ptr);
-        w.ptr = nullptr;
-        w.bytes = 0;
-    }
     void* p = nullptr;
     const size_t grow = bytes + bytes / 4;
     if (cudaMalloc(&p, grow) != cudaSuccess) return DS_ERR_CUDA;
-    if (cudaMemset(p, 0, grow) != cudaSuccess) {
+    // zeroed on the caller's stream, so the clear is ordered before this call's launches
+    // (the per-row threshold words carry a call number; zero is never a live one)
+    if (cudaMemsetAsync(p, 0, grow, stream) != cudaSuccess) {
         cudaFree(p);
         return DS_ERR_CUDA;
     }
+    if (w.ptr) g_ws_retired.push_back(w.ptr);
     w.ptr = p;
     w.bytes = grow;
     *out = p;
