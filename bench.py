@@ -82,7 +82,6 @@ class Shape:
 SEED = 0x5EED
 WORKLOAD = f"indexer_bf16: {ROWS} rows x {N} bf16 N(0,1), stride {N}, k={K_TOP}, B={B}, B2={B2}"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ds_split_kernel_indexer_bf16.md")
 
 
 def _dist():
@@ -113,33 +112,24 @@ def _source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_from_profile(sh=None):
-    """dram bytes per launch recorded by the last ncu capture of this kernel on this
-    workload, if the kernel sources have not changed since."""
-    path = PROFILE_TRAFFIC
-    if sh is not None and sh.name != "indexer":
-        path = os.path.join(ROOT, "profiles", f"ds_split_kernel_{sh.name}_{sh.dname}.md")
-        if sh.k != SHAPES[sh.name][2]:
-            return None
-    elif sh is not None and sh.k != K_TOP:
-        return None
+def _profile(label: str, sh) -> dict | None:
+    """The ncu capture written by capture_profile.py for this kernel, workload and k, if
+    one exists (profiles/<kernel>_<workload>_k<k>.json)."""
+    path = os.path.join(ROOT, "profiles", f"{label}_{sh.name}_k{sh.k}.json")
     try:
         with open(path) as f:
-            text = f.read()
-    except OSError:
+            return json.load(f)
+    except (OSError, ValueError):
         return None
-    vals = {}
-    for line in text.splitlines():
-        line = line.strip().strip("`")
-        if ":" in line and line.split(":", 1)[0].strip() in ("traffic_bytes_per_launch", "source_digest"):
-            k, v = line.split(":", 1)
-            vals[k.strip()] = v.strip()
-    if vals.get("source_digest") != _source_digest():
+
+
+def _traffic_from_profile(label: str, sh):
+    """DRAM bytes per launch from the last capture of this kernel on this workload, if the
+    kernel sources have not changed since (else None)."""
+    prof = _profile(label, sh)
+    if not prof or prof.get("source_digest") != _source_digest():
         return None
-    try:
-        return int(vals["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return prof.get("traffic_bytes_per_launch")
 
 
 class ClockSampler:
@@ -214,6 +204,115 @@ def _cpu_oracle(seconds: float, sh: "Shape", threads: int | None = None):
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": th, "kind": "oracle",
             "sample": f"oracle DeepSelect transcription (C, OpenMP over rows) on the full {sh.rows}x{sh.N} "
                       f"{sh.dname} batch, {runs} runs in {el:.1f} s"}
+
+
+
+# The method's other workload shapes, timed in the same run (each its own inputs, rotated
+# over device copies totalling more than 4x the L2): (label, synth generator, kwargs, k).
+OTHER_SHAPES = [
+    ("sampler_f32 256x129280", "sampler_f32", {}, k) for k in (1, 64, 512, 4096)
+] + [
+    (f"longctx_bf16 4x1048576 {kind}", "longctx_bf16", {"kind": kind}, k)
+    for kind in ("iid", "ascending", "levels") for k in (512, 2048)
+] + [
+    ("row65536_f32 1x65536", "row65536_f32", {}, 512),
+    ("huge_f32 1x268435456", "huge_f32", {}, 32),
+    ("huge_f32 1x268435456", "huge_f32", {}, 4096),
+]
+
+
+def time_shapes(dev, ds, l2, peak, regions=7, budget_ms=3.0):
+    """us per call and effective input GB/s of default ds_topk calls on every other
+    workload shape: CUDA graphs of back-to-back calls on one stream, CUDA events around
+    each replay, the median of `regions` replays."""
+    import torch
+    import synth
+    out = []
+    cache = {}
+    stream = torch.cuda.Stream(dev)
+    for label, fn, kw, k in OTHER_SHAPES:
+        key = (fn, tuple(sorted(kw.items())))
+        if key not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            w = getattr(synth, fn)(**kw)
+            host = torch.from_numpy(w.x.view(np.int16) if w.dtype == synth.BF16 else w.x)
+            nbytes = w.rows * w.stride * host.element_size()
+            R = max(1, -(-4 * l2 // nbytes))
+            x0 = host.to(dev)
+            cache[key] = (w, [x0] + [x0.clone() for _ in range(R - 1)])
+        w, xs = cache[key]
+        R = len(xs)
+        es = 2 if w.dtype == synth.BF16 else 4
+        vals = torch.empty((w.rows, k), dtype=xs[0].dtype, device=dev)
+        idx = torch.empty((w.rows, k), dtype=torch.int32, device=dev)
+        plan = ds.ds_get_plan(w.dtype, w.rows, w.N, k, w.B, w.B2)
+        step_bytes = w.rows * w.N * es
+
+        def call(i):
+            st = ds.ds_topk(xs[i % R].data_ptr(), w.dtype, w.rows, w.N, w.stride, k, w.B, w.B2, SEED,
+                            vals.data_ptr(), idx.data_ptr(), stream.cuda_stream)
+            if st != 0:
+                raise ds.DSError(st)
+
+        with torch.cuda.stream(stream):
+            call(0)
+        stream.synchronize()
+        est_us = max(step_bytes / (peak * 1e3) * 2.0, 5.0)
+        G = max(R, min(4000, int(budget_ms * 1e3 / est_us)), 2)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(G):
+                    call(i)
+            g.replay()
+        stream.synchronize()
+        ts = []
+        for _ in range(regions):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / G)
+        status = ds.ds_get_device_status(stream.cuda_stream)
+        us = statistics.median(ts)
+        gbs = step_bytes / (us * 1e-6) / 1e9
+        out.append({"workload": label, "k": k, "B": w.B, "B2": w.B2, "us_per_call": round(us, 3),
+                    "us_min": round(min(ts), 3), "us_max": round(max(ts), 3), "value": round(gbs, 1),
+                    "unit": "GB/s", "hbm_frac_of_peak": round(gbs / peak, 4),
+                    "plan": {"parts": plan["parts"], "cluster": plan["cluster"],
+                             "merge_launch": plan["merge_launch"]},
+                    "calls_per_graph": G, "input_copies": R, "device_status": status})
+        del g
+    cache.clear()
+    torch.cuda.empty_cache()
+    return out
+
+def _cpu_sort(seconds: float, sh: "Shape", threads: int | None = None):
+    """The oracle's full stable sort (the definition of the result) over the workload's
+    rows on this host's cores, repeated for about `seconds`."""
+    import oracle
+    w = sh.w
+    th = threads or oracle.max_threads()
+    bits = w.x.view(np.uint16) if sh.bf16 else w.x.view(np.uint32)
+    rows = max(1, min(w.rows, 2 * th))
+    sample = np.ascontiguousarray(bits[:rows, :w.N])
+    oracle.topk_sort(sample[:1], w.dtype, sh.k, threads=1)   # build / warm
+    t0 = time.perf_counter()
+    runs = 0
+    while True:
+        oracle.topk_sort(sample, w.dtype, sh.k, threads=th)
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = runs * rows * w.N * sh.es / el / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": th, "kind": "oracle",
+            "sample": f"oracle full stable sort per row (C, OpenMP over rows) on {rows} of the {sh.rows} rows x "
+                      f"{sh.N} {sh.dname}, {runs} runs in {el:.1f} s"}
 
 
 def run_reference(args):
@@ -335,7 +434,9 @@ def run_gpu(args):
         return g
 
     def timed_ms(ready):
-        """W warm-up calls, then exactly K calls timed on the stream (barrier + sync around)."""
+        """W warm-up calls, then the timed region -- exactly K calls on the stream, CUDA
+        events around it, barrier + synchronize on both sides -- repeated `regions` times.
+        Returns the per-region times (ms); the median is reported, with the spread."""
         g_full = make_graph(G, ready)
         rem = args.steps % G
         g_rem = make_graph(rem, ready) if rem else None
@@ -343,31 +444,35 @@ def run_gpu(args):
         with torch.cuda.stream(stream):
             g_warm.replay()
         stream.synchronize()
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps // G):
-                g_full.replay()
-            if g_rem is not None:
-                g_rem.replay()
-            ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-        return ev0.elapsed_time(ev1)
+        out = []
+        for _ in range(args.regions):
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            if dist:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.stream(stream):
+                ev0.record(stream)
+                for _ in range(args.steps // G):
+                    g_full.replay()
+                if g_rem is not None:
+                    g_rem.replay()
+                ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            if dist:
+                dist.barrier()
+            out.append(ev0.elapsed_time(ev1))
+        return out
 
     sampler = ClockSampler(local if ws > 1 else (dev.index or 0))
     sampler.start()
     # the public call as is: each call reads its input only after the previous kernel
     # on the stream has completed (the input may be that kernel's output)
-    ms = timed_ms(False)
+    ms_regions = timed_ms(False)
+    ms = statistics.median(ms_regions)
     # the same calls stating that their inputs were complete before the previous call
     # started (true here: the inputs are written once, before any timed call)
-    ms_ready = timed_ms(True)
+    ms_ready = statistics.median(timed_ms(True))
     clocks = sampler.stop()
     status = ds.ds_get_device_status(sptr)
     if status != 0:
@@ -388,11 +493,21 @@ def run_gpu(args):
     achieved = alg_bytes / (ms / args.steps * 1e-3) / 1e9
     # the split-row kernel runs 256 threads per CTA (also for one part per row), the
     # one-CTA-per-row kernel 288
-    kname = ("ds_split_kernel" if plan["threads"] == 256 else "ds_scan_kernel") + \
-        ("<uint16_t>" if sh.bf16 else "<uint32_t>")
+    kbase = "ds_split_kernel" if plan["threads"] == 256 else "ds_scan_kernel"
+    kname = kbase + ("<uint16_t>" if sh.bf16 else "<uint32_t>")
+    klabel = kbase + ("_u16" if sh.bf16 else "_u32")
+    traffic = _traffic_from_profile(klabel, sh)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": _traffic_from_profile(sh),
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "traffic_over_algorithmic": round(traffic / alg_bytes, 4) if traffic else None,
                 "peak_source": f"{peak_kind} hbm_gbs (copy bandwidth)", "kernel": kname}
+    prof = _profile(klabel, sh)
+    if prof and prof.get("per_launch"):
+        durs = sorted(p["duration_us"] for p in prof["per_launch"] if p.get("duration_us"))
+        roofline["ncu_launch_us"] = durs[len(durs) // 2] if durs else None
+        roofline["ncu_capture_current"] = prof.get("source_digest") == _source_digest()
+        roofline["ncu_note"] = ("ncu times one launch alone with caches flushed; back to back on a stream a "
+                                "call's prologue overlaps the previous call, so ms_per_step is shorter")
     if plan["merge_launch"]:
         roofline["note"] = "each step also runs ds_merge_kernel (rows over several clusters)"
 
@@ -438,7 +553,20 @@ def run_gpu(args):
         e1.record(stream)           # after the last read-back
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
+    # the box's raw pinned host-to-device copy rate for one step's input, alone on the copy
+    # stream: the bound of the e2e number above
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(copy_s):
+        xe[0].copy_(pinned, non_blocking=True)
+        h0.record(copy_s)
+        for _ in range(10):
+            xe[0].copy_(pinned, non_blocking=True)
+        h1.record(copy_s)
+    torch.cuda.synchronize(dev)
+    h2d_gbs = 10 * pinned.numel() * pinned.element_size() / (h0.elapsed_time(h1) * 1e-3) / 1e9
     e2e = {"value": round(ws * step_bytes * e_steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_pinned_copy_gbs": round(h2d_gbs, 1),
            "h2d_bytes_per_step": ROWS * STRIDE * sh.es, "d2h_bytes_per_step": ROWS * K_TOP * (sh.es + 4),
            "steps": e_steps}
 
@@ -446,7 +574,9 @@ def run_gpu(args):
         if dist:
             dist.destroy_process_group()
         return 0
+    shapes = time_shapes(dev, ds, l2, peak, regions=args.regions // 2 + 1) if (ws == 1 and args.shapes) else None
     cpu = _cpu_oracle(args.cpu_seconds, sh) if (ws == 1 and args.cpu_seconds > 0) else None
+    cpu_sort = _cpu_sort(args.cpu_seconds, sh) if (ws == 1 and args.cpu_seconds > 0) else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -454,13 +584,20 @@ def run_gpu(args):
         "config": {"workload": sh.desc, "global_batch_rows": ROWS * ws, "parallelism": f"rows replicated x{ws}",
                    "l2": f"inputs rotated over {R} device copies ({R * step_bytes / 1e6:.0f} MB > 4x L2 "
                          f"{l2 / 1e6:.0f} MB)",
-                   "timing": f"CUDA graphs of {G} calls, CUDA events on the launching stream",
+                   "timing": f"CUDA graphs of {G} calls, CUDA events on the launching stream; the "
+                             f"{args.steps}-call timed region is run {args.regions} times, median reported",
                    "plan": plan},
+        "timing_spread": {"regions": len(ms_regions), "region_ms_median": ms,
+                          "region_ms_min": min(ms_regions), "region_ms_max": max(ms_regions),
+                          "us_per_step_x_sm_ghz": (round(ms / args.steps * 1e3 * clocks["sm_mhz"] / 1e3, 4)
+                                                   if clocks.get("sm_mhz") else None)},
         "hbm_frac_of_peak": round(value / ws / peak, 4),
         "roofline": roofline,
         "input_ready": input_ready,
         "cpu_baseline": cpu,
+        "cpu_baseline_full_sort": cpu_sort,
         "e2e": e2e,
+        "shapes": shapes,
         "clocks": clocks,
         "gpu_launches": args.steps * launches_per_step,
         "device": torch.cuda.get_device_name(dev),
@@ -474,7 +611,9 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--regions", type=int, default=15,
+                    help="the K-step timed region is repeated this many times; the median is reported")
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--graph-len", type=int, default=2000)
@@ -483,6 +622,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(SHAPES), default="indexer",
                     help="the indexer shape is the headline; the others are the method's other workloads")
     ap.add_argument("--k", type=int, default=0, help="k (default: the workload's)")
+    ap.add_argument("--no-shapes", dest="shapes", action="store_false",
+                    help="skip timing the other workload shapes (reported under 'shapes')")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

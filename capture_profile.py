@@ -1,0 +1,173 @@
+"""Captures, on a GB300, the ncu figures that bench.py's roofline reports, and writes
+them to profiles/<kernel>_<workload>_k<k>.json.
+
+    python capture_profile.py --workload indexer [--k 512]
+
+Three steps, each on the same small bench command (`bench.py --workload W --k K
+--steps 200 --warmup 3 --regions 1 --cpu-seconds 0 --e2e-steps 5 --no-shapes
+--graph-len 100`), all under `--clock-control none`:
+  1. the command alone, which must exit 0 before ncu runs it;
+  2. the launch list: gpu__time_duration.sum for launches 40..99 (one pass each; the
+     launches are cold-cache and serialised, so only their shares are comparable with
+     the bench's back-to-back timing);
+  3. the SpeedOfLight, MemoryWorkloadAnalysis, WarpStateStats, LaunchStats and
+     Occupancy sections for two warm launches (-s 40 -c 2) of the kernel that takes the
+     largest share in step 2.
+The JSON records the commands, the source digest of the CUDA sources (bench.py reports
+`traffic` only while the sources still match it), the launch list, and per launch the
+duration, DRAM bytes read and written, issue and warp activity and the top stall
+reasons.  Raw reports stay in gpurun_out/.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+NCU = os.environ.get("NCU", "ncu")
+
+
+def _bench_cmd(workload: str, k: int) -> list:
+    return [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", workload, "--k", str(k), "--steps", "200",
+            "--warmup", "3", "--regions", "1", "--cpu-seconds", "0", "--e2e-steps", "5", "--no-shapes",
+            "--graph-len", "100"]
+
+
+def _rows(text: str) -> list:
+    start = text.find('"ID"')
+    return list(csv.reader(io.StringIO(text[start:]))) if start >= 0 else []
+
+
+def kernel_label(name: str) -> str:
+    """ds_split_kernel<unsigned short>(...) -> ds_split_kernel_u16."""
+    base = name.split("<")[0].split("(")[0].strip()
+    if base.startswith("void "):
+        base = base[5:]
+    if "unsigned short" in name or "uint16" in name:
+        return base + "_u16"
+    if "unsigned int" in name or "uint32" in name:
+        return base + "_u32"
+    return base
+
+
+def main(argv=None) -> int:
+    import bench
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--workload", default="indexer", choices=sorted(bench.SHAPES))
+    ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
+    args = ap.parse_args(argv)
+    k = args.k or bench.SHAPES[args.workload][2]
+    os.makedirs(args.out_dir, exist_ok=True)
+    cmd = _bench_cmd(args.workload, k)
+    plain = subprocess.run(cmd, capture_output=True, text=True)
+    if plain.returncode != 0:
+        print(plain.stdout[-2000:], plain.stderr[-2000:])
+        return plain.returncode
+    # 2. launch list
+    lcsv = os.path.join(args.out_dir, f"launches_{args.workload}_k{k}.csv")
+    lcmd = [NCU, "--metrics", "gpu__time_duration.sum", "--clock-control", "none", "-s", "40", "-c", "60", "--csv",
+            "--log-file", lcsv] + cmd
+    r = subprocess.run(lcmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        print(r.stdout[-2000:], r.stderr[-2000:])
+        return r.returncode
+    per = {}
+    for row in _rows(open(lcsv).read())[1:]:
+        if len(row) < 15 or row[-3] != "gpu__time_duration.sum":
+            continue
+        name = row[4]
+        v = float(row[-1].replace(",", ""))
+        unit = row[-2]
+        us = v / 1e3 if unit in ("ns", "nsecond") else (v if unit in ("us", "usecond") else v * 1e3)
+        d = per.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += us
+    total = sum(t for _, t in per.values()) or 1.0
+    launch_list = sorted(({"kernel": n, "launches": c, "total_us": round(t, 2), "share": round(t / total, 4)}
+                          for n, (c, t) in per.items()), key=lambda e: -e["total_us"])
+    top = launch_list[0]["kernel"]
+    label = kernel_label(top)
+    regex = label.rsplit("_u", 1)[0] if label.endswith(("_u16", "_u32")) else label
+    # 3. sections on two warm launches of the top kernel
+    rep = os.path.join(args.out_dir, f"prof_{label}_{args.workload}_k{k}")
+    mcmd = [NCU, "--section", "SpeedOfLight", "--section", "MemoryWorkloadAnalysis", "--section", "WarpStateStats",
+            "--section", "LaunchStats", "--section", "Occupancy", "--metrics",
+            "dram__bytes_read.sum,dram__bytes_write.sum,smsp__issue_active.avg.pct_of_peak_sustained_active,"
+            "sm__icc_request_hit_rate.pct", "--clock-control", "none", "-k", f"regex:{regex}",
+            "-s", "40", "-c", "2", "-f", "-o", rep] + cmd
+    r = subprocess.run(mcmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        print(r.stdout[-2000:], r.stderr[-2000:])
+        return r.returncode
+    raw = subprocess.run([NCU, "-i", rep + ".ncu-rep", "--page", "raw", "--csv"], capture_output=True, text=True,
+                         check=True).stdout
+    rows = _rows(raw)
+    hdr, units, launches = rows[0], rows[1], rows[2:]
+
+    def val(r, name):
+        for i, h in enumerate(hdr):
+            if h == name:
+                x = r[i].replace(",", "")
+                try:
+                    f = float(x)
+                except ValueError:
+                    return None
+                u = units[i]
+                scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1e-3, "ns": 1e-3,
+                         "usecond": 1, "us": 1, "msecond": 1e3, "ms": 1e3, "KB": 1e3, "MB": 1e6, "GB": 1e9,
+                         "B": 1}.get(u, 1)
+                return f * scale
+        return None
+
+    per_launch = []
+    for r in launches:
+        stalls = {h.replace("smsp__average_warps_issue_stalled_", "").replace("_per_issue_active.ratio", ""):
+                  float(r[i].replace(",", "") or 0)
+                  for i, h in enumerate(hdr) if h.startswith("smsp__average_warps_issue_stalled_")
+                  and h.endswith("_per_issue_active.ratio") and r[i]}
+        top_st = dict(sorted(stalls.items(), key=lambda kv: -kv[1])[:8])
+        rd, wr = val(r, "dram__bytes_read.sum"), val(r, "dram__bytes_write.sum")
+        per_launch.append({
+            "duration_us": val(r, "gpu__time_duration.sum"),
+            "dram_read_bytes": rd, "dram_write_bytes": wr,
+            "traffic_bytes": (rd or 0) + (wr or 0),
+            "issue_active_pct": val(r, "smsp__issue_active.avg.pct_of_peak_sustained_active"),
+            "warps_active_pct": val(r, "sm__warps_active.avg.pct_of_peak_sustained_active"),
+            "icc_hit_pct": val(r, "sm__icc_request_hit_rate.pct"),
+            "registers_per_thread": val(r, "launch__registers_per_thread"),
+            "shared_mem_per_block": val(r, "launch__shared_mem_per_block_dynamic"),
+            "grid_size": val(r, "launch__grid_size"),
+            "warp_stalls_per_issue": top_st,
+        })
+    traffic = [p["traffic_bytes"] for p in per_launch if p["traffic_bytes"]]
+    out = {
+        "kernel": top, "label": label, "workload": args.workload, "k": k,
+        "source_digest": bench._source_digest(),
+        "command_plain": " ".join(os.path.relpath(c, ROOT) if c.startswith(ROOT) else c for c in cmd),
+        "command_launches": "ncu --metrics gpu__time_duration.sum --clock-control none -s 40 -c 60 --csv <plain>",
+        "command_sections": f"ncu --section SpeedOfLight --section MemoryWorkloadAnalysis --section WarpStateStats "
+                            f"--section LaunchStats --section Occupancy --metrics dram__bytes_read.sum,dram__bytes_write.sum,"
+                            f"smsp__issue_active.avg.pct_of_peak_sustained_active,sm__icc_request_hit_rate.pct "
+                            f"--clock-control none -k regex:{regex} "
+                            f"-s 40 -c 2 <plain>",
+        "launch_list": launch_list,
+        "per_launch": per_launch,
+        "traffic_bytes_per_launch": int(sum(traffic) / len(traffic)) if traffic else None,
+    }
+    for d in (os.path.join(ROOT, "profiles"), args.out_dir):  # (the second is a copy the GPU machine hands back)
+        path = os.path.join(d, f"{label}_{args.workload}_k{k}.json")
+        with open(path, "w") as f:
+            json.dump(out, f, indent=1)
+        print(path)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
