@@ -23,7 +23,8 @@
  * blocks in the order of the same draws.
  *
  * Results.  out_vals[r*k + j] / out_idx[r*k + j], j < k, hold the k largest values of
- * row r (bit copies of the input) and their columns, in no particular order.  Among
+ * row r (bit copies of the input) and their columns, in no particular order (in order of
+ * value descending, equal values by column ascending, with ds_options.sorted).  Among
  * values equal to the k-th largest, which columns are returned is unspecified; the
  * value multiset is always exact.
  *
@@ -53,7 +54,7 @@ typedef enum {
 
 typedef enum {
     DS_OK = 0,
-    DS_ERR_INVALID_ARG = 1, /* null pointer, rows < 0, N < 1, k < 1, k > N, B < 1, B2 < 1,
+    DS_ERR_INVALID_ARG = 1, /* null pointer, rows < 0, N < 1, k < 1, k > N, B < 0, B2 < 0,
                                row_stride < N, unknown dtype                          */
     DS_ERR_ALIGNMENT = 2,   /* x, out_vals or out_idx not 16-byte aligned, or (rows > 1)
                                row_stride * sizeof(element) not a multiple of 16       */
@@ -83,9 +84,13 @@ typedef enum {
  *   row_stride  elements between row starts, >= N; when rows > 1, row_stride*sizeof(element)
  *               must be a multiple of 16 bytes (1024 recommended).
  *   k           1 <= k <= min(N, 4096).
- *   B, B2       block size and compaction slack of the method (>= 1); B*sizeof(element)
- *               must be a multiple of 16 bytes, k + B + B2 <= 2^20, and one CTA visits at
- *               most 1024 blocks (with one CTA per row: ceil(N/B) <= 1024).
+ *   B, B2       block size and compaction slack of the method (>= 1), or 0 for the
+ *               library's choice: B = 8192 when the rows fit one wave of CTAs
+ *               (ceil(rows / SMs) == 1) and 4096 otherwise, B2 = 4096 -- the shipped
+ *               CUDA configuration the DeepSelect TopK tutorial describes (section 4.7);
+ *               ds_get_plan reports the values in effect.  B*sizeof(element) must be a
+ *               multiple of 16 bytes, k + B + B2 <= 2^20, and one CTA visits at most 1024
+ *               blocks (with one CTA per row: ceil(N/B) <= 1024).
  *   seed        selects the block order (see above).
  *   out_vals    device, rows*k elements of dtype; 16-byte aligned.  Caller-owned.
  *   out_idx     device, rows*k int32; 16-byte aligned.  Caller-owned.
@@ -124,6 +129,10 @@ typedef struct {
                                that x was complete before that kernel started, and the
                                call starts reading x while that kernel is still running
                                (consecutive calls on static inputs overlap their edges) */
+    int32_t sorted;         /* nonzero: each row's k results in order of value descending
+                               (the key order above), equal values by column ascending
+                               -- the pages' sorted_value flag; a second kernel sorts the
+                               k results of each row in shared memory at the end      */
 } ds_options;
 
 /* ds_topk with explicit options (NULL = defaults, identical to ds_topk). */
@@ -145,6 +154,8 @@ typedef struct {
     int64_t workspace_bytes;/* device workspace needed (0 unless split over clusters)  */
     int32_t ctas_per_sm;    /* resident CTAs per SM for this configuration             */
     int32_t merge_launch;   /* 1 when a second (merge) kernel runs                      */
+    int32_t B;              /* block size in effect (the library's choice when 0 was passed) */
+    int32_t B2;             /* compaction slack in effect (likewise)                   */
 } ds_plan;
 
 /* Errors as ds_topk's host checks (DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED), and

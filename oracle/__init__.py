@@ -45,7 +45,7 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp]
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -72,6 +72,9 @@ def _load():
         lib.oracle_deepselect.argtypes = [vp, ctypes.c_int, i64, i64, i64, i32, i32, i32, u64,
                                           vp, vp, vp, vp, i32]
         lib.oracle_deepselect.restype = ctypes.c_int
+        lib.oracle_topk_sample.argtypes = [vp, ctypes.c_int, i64, i64, i64, i32, ctypes.c_double, vp, vp,
+                                           vp, vp, i32]
+        lib.oracle_topk_sample.restype = ctypes.c_int
         lib.oracle_work_bound.argtypes = [i64, i32, i32, i32]
         lib.oracle_work_bound.restype = ctypes.c_double
         lib.oracle_num_threads_max.argtypes = []
@@ -178,6 +181,24 @@ def deepselect(x: np.ndarray, dtype: int, k: int, B: int, B2: int, seed: int,
     if rc != 0:
         raise ValueError(f"oracle_deepselect rejected its arguments (rc={rc})")
     return vals, idx, stats
+
+
+def topk_sample(x: np.ndarray, dtype: int, k: int, temperature: float, uniforms, N: int | None = None,
+                threads: int = 1):
+    """Top-k sampling (see oracle.c): returns (token, prob, cdf) -- the sampled column and
+    its probability per row, and the normalised running sums (rows, k) of the weights in
+    the sorted top-k order."""
+    bits = _as_bits(x, dtype)
+    bits, rows, N, stride = _rows_view(bits, N, None)
+    u = np.ascontiguousarray(np.asarray(uniforms, dtype=np.float64).reshape(rows))
+    token = np.zeros(rows, dtype=np.int32)
+    prob = np.zeros(rows, dtype=np.float64)
+    cdf = np.zeros((rows, k), dtype=np.float64)
+    rc = _load().oracle_topk_sample(_ptr(bits), dtype, rows, N, stride, k, float(temperature), _ptr(u),
+                                    _ptr(token), _ptr(prob), _ptr(cdf), threads)
+    if rc != 0:
+        raise ValueError(f"oracle_topk_sample rejected its arguments (rc={rc})")
+    return token, prob, cdf
 
 
 def work_bound(N: int, k: int, B: int, B2: int) -> float:

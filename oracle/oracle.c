@@ -14,6 +14,9 @@
  *     (key descending, column ascending) and the first k entries are returned.  This is
  *     the stable-sort reference of the TileKernels two-backends tutorial (section on
  *     the stable_topk reference), which breaks ties toward the smaller index.
+ *   - oracle_topk_sample: top-k sampling from the top k of oracle_topk_sort (the
+ *     sampler's use of top-k, DeepSelect TopK tutorial, section 1.1), in double
+ *     precision; see the function.
  *   - oracle_deepselect: the DeepSelectTopk pseudocode of DeepSelect-deep-dive.md
  *     ("Algorithm"), step by step: threshold T = -inf, blocks of size B visited in a
  *     random order that does not depend on x, every element with key > T appended to
@@ -45,6 +48,7 @@
  * inputs, the harmonic-number bound, and published Philox known-answer vectors.
  */
 #include <stdint.h>
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -372,6 +376,70 @@ int oracle_deepselect(const void* x, int dtype, int64_t rows, int64_t N, int64_t
 /* ------------------------------------------------------- bound -------------------- */
 
 /* (1 + k/B2) * (k + B + B2) * H_m, m = ceil(N/B) */
+/* ------------------------------------------------------- top-k sampling ---------- */
+
+/* oracle_topk_sample: the sampler's use of top-k (DeepSelect TopK tutorial, section 1.1:
+ * at sampling time top-k picks candidate tokens out of the vocabulary's logits), read
+ * plainly as top-k sampling.  For each row: its top k in the order of oracle_topk_sort
+ * (key descending, column ascending), values v_0 >= v_1 >= ...; weights
+ * w_i = exp((v_i - v_0) / temperature); running sums s_i = w_0 + ... + w_i in that order;
+ * the row's token is the column of the first i with s_i > u * s_{k-1} (u = uniforms[row]
+ * in [0, 1)), or of the last candidate if none.  prob[row] = w_i / s_{k-1}; cdf (rows x k,
+ * may be NULL) receives s_i / s_{k-1}.  All in double precision. */
+int oracle_topk_sample(const void* x, int dtype, int64_t rows, int64_t N, int64_t stride, int32_t k,
+                       double temperature, const double* uniforms, int32_t* token, double* prob, double* cdf,
+                       int32_t nthreads)
+{
+    if (!x || !uniforms || !token || !prob || rows < 0 || N < 1 || k < 1 || k > N || stride < N) return -2;
+    if (!(temperature > 0.0)) return -2;
+    const int64_t es = or_esize(dtype);
+    int err = 0;
+#ifdef _OPENMP
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) reduction(| : err)
+#endif
+    for (int64_t r = 0; r < rows; ++r) {
+        const char* xrow = (const char*)x + r * stride * es;
+        uint32_t* vb = (uint32_t*)malloc((size_t)k * sizeof(uint32_t));
+        int32_t* ix = (int32_t*)malloc((size_t)k * sizeof(int32_t));
+        double* s = (double*)malloc((size_t)k * sizeof(double));
+        if (!vb || !ix || !s) {
+            err |= 1;
+        } else {
+            /* the sorted top k, as 32-bit patterns of the values */
+            uint16_t* v16 = (uint16_t*)vb;
+            if (or_topk_sort_row(xrow, dtype, N, k, dtype == OR_BF16 ? (void*)v16 : (void*)vb, ix)) err |= 1;
+            double v0 = 0.0;
+            for (int32_t i = 0; i < k; ++i) {
+                const uint32_t b = dtype == OR_BF16 ? ((uint32_t)v16[i] << 16) : vb[i];
+                float f;
+                memcpy(&f, &b, sizeof f);
+                if (i == 0) v0 = (double)f;
+                const double w = exp(((double)f - v0) / temperature);
+                s[i] = (i ? s[i - 1] : 0.0) + w;
+            }
+            const double total = s[k - 1];
+            const double target = uniforms[r] * total;
+            int32_t pick = k - 1;
+            for (int32_t i = 0; i < k; ++i) {
+                if (s[i] > target) {
+                    pick = i;
+                    break;
+                }
+            }
+            token[r] = ix[pick];
+            prob[r] = (s[pick] - (pick ? s[pick - 1] : 0.0)) / total;
+            if (cdf)
+                for (int32_t i = 0; i < k; ++i) cdf[r * (int64_t)k + i] = s[i] / total;
+        }
+        free(vb);
+        free(ix);
+        free(s);
+    }
+    (void)nthreads;
+    return err ? -1 : 0;
+}
+
 double oracle_work_bound(int64_t N, int32_t k, int32_t B, int32_t B2)
 {
     const int64_t m = (N + B - 1) / B;

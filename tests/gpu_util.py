@@ -32,7 +32,7 @@ def to_device(x_np, dtype):
     return torch.from_numpy(np.ascontiguousarray(x_np).view(np.float32)).cuda()
 
 
-def run_gpu(x_np, dtype, k, B, B2, seed, N=None, parts=0, cluster=0, stats=False, workspace=None):
+def run_gpu(x_np, dtype, k, B, B2, seed, N=None, parts=0, cluster=0, stats=False, workspace=None, sorted=False):
     """Returns (vals_bits, idx, stats-or-None) as numpy arrays."""
     import torch
     import top_selection_gb300 as ds
@@ -40,7 +40,7 @@ def run_gpu(x_np, dtype, k, B, B2, seed, N=None, parts=0, cluster=0, stats=False
     rows = x_np.shape[0]
     st = torch.zeros((rows, ds.DS_NSTAT), dtype=torch.int64, device="cuda") if stats else None
     vals, idx = ds.topk(xt, k, B, B2, seed=seed, N=N, parts=parts, cluster=cluster, stats=st,
-                        workspace=workspace)
+                        workspace=workspace, sorted=sorted)
     status = ds.ds_get_device_status(torch.cuda.current_stream().cuda_stream)
     assert status == 0, f"device status {status}"
     v = vals.cpu().numpy()
@@ -79,3 +79,21 @@ def check_topk_by_counts(x_f32_row, k, vals_f32, idx):
     v = vals_f32.min()
     assert int((vals_f32 > v).sum()) == int((x > v).sum())
     assert int((vals_f32 == v).sum()) <= int((x == v).sum())
+
+
+def check_sorted(x_np, dtype, k, vals, idx, N=None, threads=8):
+    """Sorted output: check_topk, and the sequence is the oracle's order -- values (bit
+    patterns) position by position, and the columns at every position whose key is above
+    the k-th key (values equal to the k-th may come from other columns, by column)."""
+    check_topk(x_np, dtype, k, vals, idx, N=N, threads=threads)
+    bits = bits_of(x_np, dtype)
+    n = bits.shape[1] if N is None else N
+    ref_v, ref_i = oracle.topk_sort(np.ascontiguousarray(bits[:, :n]), dtype, k, threads=threads)
+    for r in range(bits.shape[0]):
+        assert np.array_equal(vals[r], ref_v[r]), f"row {r}: value sequence differs from the oracle's"
+        kth = oracle.key(int(ref_v[r][-1]), dtype)
+        above = np.array([oracle.key(int(v), dtype) > kth for v in ref_v[r]], dtype=bool)
+        assert np.array_equal(idx[r][above], ref_i[r][above]), f"row {r}: column order differs above the k-th"
+        eq = ~above
+        cols = idx[r][eq].astype(np.int64)
+        assert np.all(np.diff(cols) > 0), f"row {r}: equal values not in column order"

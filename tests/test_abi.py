@@ -64,8 +64,8 @@ P = 1 << 20   # a 16-byte aligned fake device address
     (dict(dtype=2), 1),                         # unknown dtype
     (dict(k=0), 1),
     (dict(k=1001), 1),                          # k > N
-    (dict(B=0), 1),
-    (dict(B2=0), 1),
+    (dict(B=-1), 1),                            # (0 asks for the library's choice)
+    (dict(B2=-1), 1),
     (dict(N=0), 1),
     (dict(rows=-1), 1),
     (dict(row_stride=999), 1),                  # stride < N
@@ -195,3 +195,36 @@ def test_touching_a_kernel_header_marks_the_library_stale(lib):
     finally:
         os.utime(split, ns=(st.st_atime_ns, st.st_mtime_ns))
     assert build.up_to_date()
+
+
+_BLOCKS_SCRIPT = r"""
+import json, top_selection_gb300 as ds
+ds.load()
+out = {}
+for rows in (1, 64, 152, 153, 256, 1000):
+    p = ds.ds_get_plan(1, rows, 129280, 512, 0, 0)
+    out[rows] = (p["B"], p["B2"])
+q = ds.ds_get_plan(0, 64, 131072, 512, 4096, 0)
+out["given_B"] = (q["B"], q["B2"])
+q = ds.ds_get_plan(0, 64, 131072, 512, 0, 1024)
+out["given_B2"] = (q["B"], q["B2"])
+print(json.dumps(out))
+"""
+
+
+def test_library_chooses_block_sizes_on_a_described_device(lib):
+    """B = 0 / B2 = 0: B is 8192 while the rows fit one wave of CTAs (rows <= SMs), 4096
+    after that, B2 is 4096 (the shipped CUDA configuration the DeepSelect TopK tutorial
+    describes, section 4.7); values passed explicitly are kept."""
+    import json
+    import sys
+    env = dict(os.environ, DS_PLAN_DEVICE="152,232448,233472", CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", _BLOCKS_SCRIPT], env=env, cwd=ROOT, capture_output=True,
+                         text=True, check=True).stdout
+    got = json.loads(out.strip().splitlines()[-1])
+    for rows in ("1", "64", "152"):
+        assert got[rows] == [8192, 4096]
+    for rows in ("153", "256", "1000"):
+        assert got[rows] == [4096, 4096]
+    assert got["given_B"] == [4096, 4096]
+    assert got["given_B2"] == [8192, 1024]

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_util import bits_of, check_topk, check_topk_by_counts, pad_rows, run_gpu, to_device
+from gpu_util import bits_of, check_sorted, check_topk, check_topk_by_counts, pad_rows, run_gpu, to_device
 
 torch = pytest.importorskip("torch")
 
@@ -432,3 +432,67 @@ def test_concurrent_streams_multi_cluster_rows():
         x = xa if name == "a" else xb
         check_topk(x, synth.FP32, 512, v.cpu().numpy().view(np.uint32), i.cpu().numpy())
     check_topk(xc, synth.FP32, 512, vc.cpu().numpy().view(np.uint32), ic.cpu().numpy())
+
+
+@pytest.mark.parametrize("shape", ["row65536", "indexer", "sampler", "longctx", "huge"])
+def test_library_chosen_block_sizes(shape):
+    """B = B2 = 0 lets the library choose the block size and compaction slack; results
+    match the oracle on every workload shape (the 268M-element row by the count identity
+    and on a 4M-element slice)."""
+    import top_selection_gb300 as ds
+    if shape == "huge":
+        w = synth.huge_f32()
+        for k in (32, 4096):
+            v, i, _ = run_gpu(w.x, w.dtype, k, 0, 0, 0x5EED)
+            check_topk_by_counts(w.x[0], k, v[0].view(np.float32), i[0].astype(np.int64))
+        sl = np.ascontiguousarray(w.x[:, : 1 << 22])
+        v, i, _ = run_gpu(sl, w.dtype, 4096, 0, 0, 0x5EED)
+        check_topk(sl, w.dtype, 4096, v, i)
+        return
+    w = {"row65536": synth.row65536_f32, "indexer": synth.indexer_bf16, "sampler": synth.sampler_f32,
+         "longctx": lambda: synth.longctx_bf16("ascending")}[shape]()
+    plan = ds.ds_get_plan(w.dtype, w.rows, w.N, 512, 0, 0)
+    waves = -(-w.rows // torch.cuda.get_device_properties(0).multi_processor_count)
+    assert (plan["B"], plan["B2"]) == ((8192 if waves == 1 else 4096), 4096)
+    for k in (1, 512, 4096 if w.N >= 4096 else w.N):
+        v, i, _ = run_gpu(w.x, w.dtype, k, 0, 0, 0x5EED, N=w.N)
+        check_topk(w.x, w.dtype, k, v, i, N=w.N, threads=16)
+
+
+
+# ---------------------------------------------------------------- sorted output ----
+
+@pytest.mark.parametrize("shape", ["row65536", "indexer", "sampler", "longctx", "huge_slice"])
+def test_sorted_output_workloads(shape):
+    """options.sorted: each row's k results come in the oracle's order (value descending,
+    equal values by column ascending) on every workload shape, k from 1 to 4096."""
+    if shape == "huge_slice":
+        w = synth.huge_f32()
+        x = np.ascontiguousarray(w.x[:, : 1 << 22])
+        for k in (32, 4096):
+            v, i, _ = run_gpu(x, w.dtype, k, w.B, w.B2, 0x5EED, sorted=True)
+            check_sorted(x, w.dtype, k, v, i)
+        return
+    w = {"row65536": synth.row65536_f32, "indexer": lambda: synth.indexer_bf16(rows=16),
+         "sampler": lambda: synth.sampler_f32(rows=24), "longctx": lambda: synth.longctx_bf16("levels")}[shape]()
+    for k in (1, 2, 100, 512, 4096):
+        v, i, _ = run_gpu(w.x, w.dtype, k, w.B, w.B2, 0x5EED, N=w.N, sorted=True)
+        check_sorted(w.x, w.dtype, k, v, i, N=w.N, threads=16)
+
+
+@pytest.mark.parametrize("parts,cluster", [(1, 1), (0, 0), (16, 4)])
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.FP32])
+def test_sorted_output_every_path(parts, cluster, dtype):
+    """The one-CTA schedule, the split-row kernel and rows over several clusters (merge
+    kernel) all give sorted results with the option; ties and special values included."""
+    rng = np.random.default_rng(123 + parts + dtype)
+    rows, N = 3, 300000
+    x = np.round(rng.standard_normal((rows, N)) * 16).astype(np.float32) / 16   # many ties
+    x[0, ::1001] = np.float32(np.inf)
+    x[1, ::997] = -0.0
+    if dtype == synth.BF16:
+        x = synth.f32_to_bf16_bits(x)
+    B = 4096
+    for k in (7, 777, 4096):
+        v, i, _ = run_gpu(x, dtype, k, B, B, 5, parts=parts, cluster=cluster, sorted=True)
+        check_sorted(x, dtype, k, v, i)

@@ -380,3 +380,75 @@ def test_synth_bf16_rounding_matches_torch():
     ours = synth.f32_to_bf16_bits(f)
     ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- top-k sampling ----
+# Pins of oracle.topk_sample by cases whose answer is fixed without its formula: one
+# candidate, equal logits (uniform choice), two candidates (a logistic in the logit gap),
+# a vanishing temperature (the arg max), and the candidate order among equal values.
+
+def test_sample_k1_is_argmax(oracle_lib):
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((5, 300)).astype(np.float32)
+    x[2, 7] = x[2, 200] = 9.0            # a tie at the maximum: the smaller column
+    for u in (0.0, 0.3, 0.999999):
+        tok, prob, _ = oracle_lib.topk_sample(x, synth.FP32, 1, 0.8, [u] * 5)
+        assert tok.tolist() == [int(np.argmax(r)) for r in x]
+        assert np.all(prob == 1.0)
+
+
+def test_sample_equal_logits_is_uniform(oracle_lib):
+    k = 37
+    x = np.full((1, k), 1.25, dtype=np.float32)
+    for m in range(k):
+        u = (m + 0.5) / k
+        tok, prob, cdf = oracle_lib.topk_sample(x, synth.FP32, k, 1.7, [u])
+        assert tok[0] == m                      # equal values come by column
+        assert abs(prob[0] - 1.0 / k) < 1e-15
+        assert abs(cdf[0, m] - (m + 1) / k) < 1e-12
+
+
+def test_sample_two_candidates_logistic(oracle_lib):
+    for a, b, T in ((2.0, 0.5, 1.0), (0.0, -3.0, 0.5), (10.0, 9.0, 4.0)):
+        x = np.array([[b, a]], dtype=np.float32)      # the larger value sits in column 1
+        p_hi = 1.0 / (1.0 + math.exp((np.float32(b) - np.float32(a)) / T))
+        tok, prob, _ = oracle_lib.topk_sample(x, synth.FP32, 2, T, [p_hi - 1e-9])
+        assert tok[0] == 1 and abs(prob[0] - p_hi) < 1e-12
+        tok, prob, _ = oracle_lib.topk_sample(x, synth.FP32, 2, T, [p_hi + 1e-9])
+        assert tok[0] == 0 and abs(prob[0] - (1.0 - p_hi)) < 1e-12
+
+
+def test_sample_cold_temperature_and_bf16(oracle_lib):
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((4, 1000)).astype(np.float32)
+    xb = synth.f32_to_bf16_bits(x)
+    xf = synth.bf16_bits_to_f32(xb)
+    for u in (0.0, 0.5, 0.99):
+        tok, _, _ = oracle_lib.topk_sample(xb, synth.BF16, 64, 1e-6, [u] * 4)
+        assert tok.tolist() == [int(np.argmax(r)) for r in xf]
+
+
+def test_sample_candidate_order_with_ties(oracle_lib):
+    x = np.array([[5.0, 7.0, 7.0, 1.0]], dtype=np.float32)
+    # candidates: columns 1, 2 (weight 1 each), then 0 (weight e^-2); total 2 + e^-2
+    tot = 2.0 + math.exp(-2.0)
+    for u, want in ((0.4 / tot, 1), (1.4 / tot, 2), (2.05 / tot, 0)):
+        tok, _, _ = oracle_lib.topk_sample(x, synth.FP32, 3, 1.0, [u])
+        assert tok[0] == want
+
+
+def test_block_permutation_every_cell_uniform(oracle_lib):
+    """Chi-square over every (block, position) cell: with m = 32 blocks and 3,200 seeds,
+    each block lands in each position 100 times on average.  For a uniform permutation
+    the statistic has (m - 1)^2 = 961 degrees of freedom (mean 961, sd ~44); a bias at
+    any position, early or late, adds to it.  The bound is the mean + 6 sd."""
+    m, seeds = 32, 3200
+    counts = np.zeros((m, m), dtype=np.int64)
+    for s in range(seeds):
+        p = oracle_lib.block_permutation(0xC0FFEE + s, s % 7, m)
+        counts[p, np.arange(m)] += 1
+    assert np.all(counts.sum(axis=0) == seeds) and np.all(counts.sum(axis=1) == seeds)
+    e = seeds / m
+    chi2 = float(((counts - e) ** 2 / e).sum())
+    dof = (m - 1) ** 2
+    assert chi2 < dof + 6 * math.sqrt(2 * dof), chi2

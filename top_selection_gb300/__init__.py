@@ -47,7 +47,8 @@ class DSError(RuntimeError):
 class ds_options(ctypes.Structure):
     _fields_ = [("parts", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("stats", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_size_t), ("input_ready", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_size_t), ("input_ready", ctypes.c_int32),
+                ("sorted", ctypes.c_int32)]
 
 
 class ds_plan(ctypes.Structure):
@@ -55,7 +56,8 @@ class ds_plan(ctypes.Structure):
                 ("threads", ctypes.c_int32), ("chunk_elems", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
-                ("ctas_per_sm", ctypes.c_int32), ("merge_launch", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("merge_launch", ctypes.c_int32),
+                ("B", ctypes.c_int32), ("B2", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -105,9 +107,9 @@ def load():
         return lib
 
 
-def _opts(parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, input_ready=False):
+def _opts(parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, input_ready=False, sorted=False):
     return ds_options(int(parts), int(cluster), int(stats) or None, int(workspace) or None,
-                      int(workspace_bytes), 1 if input_ready else 0)
+                      int(workspace_bytes), 1 if input_ready else 0, 1 if sorted else 0)
 
 
 # ------------------------------------------------------------------ C ABI mirror ----
@@ -120,8 +122,8 @@ def ds_topk(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, st
 
 def ds_topk_ex(x, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx,
                parts=0, cluster=0, stats=0, workspace=0, workspace_bytes=0, input_ready=False,
-               stream=0) -> int:
-    o = _opts(parts, cluster, stats, workspace, workspace_bytes, input_ready)
+               stream=0, sorted=False) -> int:
+    o = _opts(parts, cluster, stats, workspace, workspace_bytes, input_ready, sorted)
     return load().ds_topk_ex(int(x) or None, dtype, rows, N, row_stride, k, B, B2, seed,
                              int(out_vals) or None, int(out_idx) or None, ctypes.byref(o),
                              int(stream) or None)
@@ -191,10 +193,11 @@ def _torch_dtype_code(t):
 
 def topk(x, k: int, B: int, B2: int, seed: int = 0x5EED, N: int | None = None,
          out=None, parts: int = 0, cluster: int = 0, stats=None, workspace=None, stream=None,
-         input_ready: bool = False):
+         input_ready: bool = False, sorted: bool = False):
     """Row-wise DeepSelect top-k of a CUDA tensor ``x`` of shape (rows, stride).
 
-    Returns (values, indices), each (rows, k), unordered within a row.  ``N`` (default:
+    Returns (values, indices), each (rows, k), unordered within a row unless ``sorted``
+    (then by value descending, equal values by column ascending).  ``N`` (default:
     the row length) may be shorter than the stride.  ``stats`` is an optional int64
     CUDA tensor (rows, DS_NSTAT) filled when each row is one part.  ``input_ready`` states
     that ``x`` was complete before the previous kernel on the stream started, which lets
@@ -223,7 +226,7 @@ def topk(x, k: int, B: int, B2: int, seed: int = 0x5EED, N: int | None = None,
     st = ds_topk_ex(x.data_ptr(), dtype, rows, n, stride, k, B, B2, seed, vals.data_ptr(),
                     idx.data_ptr(), parts=parts, cluster=cluster,
                     stats=0 if stats is None else stats.data_ptr(), workspace=ws_ptr,
-                    workspace_bytes=ws_bytes, input_ready=input_ready, stream=stream)
+                    workspace_bytes=ws_bytes, input_ready=input_ready, stream=stream, sorted=sorted)
     if st != 0:
         raise DSError(st)
     return vals, idx

@@ -738,6 +738,56 @@ __global__ void __launch_bounds__(kMergeThreads, 1) ds_merge_kernel(const MergeP
     }
 }
 
+// ---------------------------------------------------------------- sorted output ---
+// The optional last step of the operation (the pages' sorted_value flag; the DeepSelect
+// TopK tutorial notes that sorting happens only at the end, on the k survivors): each
+// row's k results, already exact, are put in order of key descending, column ascending.
+// One CTA per row sorts (key << 32 | ~column) descending with a bitonic network in
+// shared memory over the next power of two >= k (padding 0 sorts last: a real entry's
+// low word ~column is never 0, as columns are below 2^31).
+constexpr int kSortThreads = 512;
+
+template <typename KeyT>
+__global__ void __launch_bounds__(kSortThreads) ds_sort_kernel(void* vals, int32_t* idx, int k, int n2) {
+    constexpr int ES = sizeof(KeyT);
+    extern __shared__ __align__(16) unsigned long long sv[];
+    const int tid = threadIdx.x;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * k;
+    for (int i = tid; i < n2; i += kSortThreads) {
+        unsigned long long c = 0ull;
+        if (i < k) {
+            const uint32_t raw = ES == 2 ? static_cast<const uint16_t*>(vals)[base + i]
+                                         : static_cast<const uint32_t*>(vals)[base + i];
+            const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+            c = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx[base + i]));
+        }
+        sv[i] = c;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < (n2 >> 1); t += kSortThreads) {
+                const int lo = 2 * t - (t & (stride - 1));  // first of the pair (lo, lo + stride)
+                const int hi = lo + stride;
+                const bool desc = (lo & size) == 0;        // this run sorts descending
+                const unsigned long long a = sv[lo], b = sv[hi];
+                if ((a < b) == desc) {
+                    sv[lo] = b;
+                    sv[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = tid; i < k; i += kSortThreads) {
+        const unsigned long long c = sv[i];
+        const uint32_t key = static_cast<uint32_t>(c >> 32);
+        if (ES == 2) static_cast<uint16_t*>(vals)[base + i] = static_cast<uint16_t>(unkey_bf16(key));
+        else static_cast<uint32_t*>(vals)[base + i] = unkey_f32(key);
+        idx[base + i] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(c));
+    }
+}
+
 // ================================================================ host ============
 
 struct DevInfo {
@@ -807,12 +857,30 @@ static bool dev_info(int dev, DevInfo& out) {
 
 struct Plan {
     int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww, refine;
+    int B, B2;  // block size and compaction slack in effect (the library's choice when given as 0)
     bool split;  // the split-row kernel (also for one part per row), else the one-CTA-per-row kernel
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
     size_t off_gT, off_key, off_idx, off_cnt;
 };
+
+// B = 0 or B2 = 0 asks the library to choose them.  The choice follows the shipped CUDA
+// configuration the DeepSelect TopK tutorial describes (section 4.7, the wave rule of
+// api.cpp): with num_waves = ceil(rows / SMs) equal to 1 the block is 8192 elements,
+// otherwise 4096; the compaction slack (reconstruct threshold) is 4096.  Both are Theta(k)
+// for the supported k <= 4096, which the expected-work bound needs (tutorial section 3.7).
+static ds_status resolve_blocks(int dev, int64_t rows, int32_t& B, int32_t& B2) {
+    if (B < 0 || B2 < 0) return DS_ERR_INVALID_ARG;
+    if (B == 0) {
+        DevInfo di;
+        if (!dev_info(dev, di)) return DS_ERR_CUDA;
+        const int64_t waves = (rows + di.sms - 1) / di.sms;
+        B = waves <= 1 ? 8192 : 4096;
+    }
+    if (B2 == 0) B2 = 4096;
+    return DS_OK;
+}
 
 static ds_status validate(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
                           int32_t B, int32_t B2, const void* out_vals, const int32_t* out_idx) {
@@ -834,6 +902,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     DevInfo di;
     if (!dev_info(dev, di)) return DS_ERR_CUDA;
     P.dev = dev;
+    P.B = B;
+    P.B2 = B2;
     P.es = dtype == DS_BF16 ? 2 : 4;
     P.m = (N + B - 1) / B;
     P.chunk = B < kChunkBytesMax / P.es ? B : kChunkBytesMax / P.es;
@@ -1030,7 +1100,7 @@ static cudaError_t set_smem(Kern kern, int slot, int dev, size_t bytes, bool non
 template <typename KeyT>
 static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
                         int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, long long* stats,
-                        char* ws, bool early, cudaStream_t stream) {
+                        char* ws, bool early, bool sorted, cudaStream_t stream) {
     ScanParams sp;
     sp.x = static_cast<const char*>(x);
     sp.rows = rows;
@@ -1128,6 +1198,13 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
         mk<<<static_cast<unsigned>(rows), kMergeThreads, P.merge_smem, stream>>>(mp);
         if (cudaGetLastError() != cudaSuccess) return DS_ERR_CUDA;
     }
+    if (sorted && k > 1) {  // a plain launch: it starts once the results above are complete
+        int n2 = 1;
+        while (n2 < k) n2 <<= 1;
+        ds_sort_kernel<KeyT><<<static_cast<unsigned>(rows), kSortThreads, n2 * sizeof(unsigned long long), stream>>>(
+            out_vals, out_idx, k, n2);
+        if (cudaGetLastError() != cudaSuccess) return DS_ERR_CUDA;
+    }
     return DS_OK;
 }
 
@@ -1169,15 +1246,17 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
                       const ds_options* options, ds_plan* plan) {
     if (!plan) return DS_ERR_INVALID_ARG;
     if (dtype != DS_BF16 && dtype != DS_FP32) return DS_ERR_INVALID_ARG;
-    if (rows < 0 || N < 1 || k < 1 || k > N || B < 1 || B2 < 1) return DS_ERR_INVALID_ARG;
-    const int es = dtype == DS_BF16 ? 2 : 4;
-    if (k > kMaxK || N >= (int64_t(1) << 31) || (static_cast<int64_t>(B) * es) % 16 != 0) return DS_ERR_UNSUPPORTED;
+    if (rows < 0 || N < 1 || k < 1 || k > N || B < 0 || B2 < 0) return DS_ERR_INVALID_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {  // no device: only a described one (DS_PLAN_DEVICE) plans
         cudaGetLastError();
         if (!std::getenv("DS_PLAN_DEVICE")) return DS_ERR_CUDA;
         dev = 0;
     }
+    ds_status rs = resolve_blocks(dev, rows, B, B2);
+    if (rs != DS_OK) return rs;
+    const int es = dtype == DS_BF16 ? 2 : 4;
+    if (k > kMaxK || N >= (int64_t(1) << 31) || (static_cast<int64_t>(B) * es) % 16 != 0) return DS_ERR_UNSUPPORTED;
     Plan P;
     const ds_status st = make_plan(dev, dtype, rows, N, k, B, B2, options, P);
     if (st != DS_OK) return st;
@@ -1191,6 +1270,8 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
     plan->workspace_bytes = static_cast<int64_t>(P.ws_bytes);
     plan->ctas_per_sm = P.ctas_per_sm;
     plan->merge_launch = P.C > 1 ? 1 : 0;
+    plan->B = P.B;
+    plan->B2 = P.B2;
     return DS_OK;
 }
 
@@ -1207,7 +1288,14 @@ ds_status ds_workspace_bytes(int32_t dtype, int64_t rows, int64_t N, int32_t k, 
 ds_status ds_topk_ex(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
                      int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx,
                      const ds_options* options, cudaStream_t stream) {
-    ds_status st = validate(x, dtype, rows, N, row_stride, k, B, B2, out_vals, out_idx);
+    if (B < 0 || B2 < 0) return DS_ERR_INVALID_ARG;
+    if (rows > 0 && (B == 0 || B2 == 0)) {  // the library's choice (resolve_blocks)
+        int d = 0;
+        if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return DS_ERR_CUDA;
+        const ds_status rs = resolve_blocks(d, rows, B, B2);
+        if (rs != DS_OK) return rs;
+    }
+    ds_status st = validate(x, dtype, rows, N, row_stride, k, B ? B : 4096, B2 ? B2 : 4096, out_vals, out_idx);
     if (st != DS_OK) return st;
     if (rows == 0) return DS_OK;
     int dev = 0;
@@ -1232,10 +1320,12 @@ ds_status ds_topk_ex(const void* x, int32_t dtype, int64_t rows, int64_t N, int6
     }
     long long* stats = options ? reinterpret_cast<long long*>(options->stats) : nullptr;
     const bool early = options && options->input_ready;
+    const bool sorted = options && options->sorted;
     if (dtype == DS_BF16)
         return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, early,
-                                stream);
-    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, early, stream);
+                                sorted, stream);
+    return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, stats, ws, early, sorted,
+                            stream);
 }
 
 ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k, int32_t B,
@@ -1253,7 +1343,14 @@ ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t
 ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
                           int32_t B, int32_t B2, uint64_t seed, void* out_vals, int32_t* out_idx, int32_t parts,
                           int32_t cluster, cudaStream_t stream) {
-    ds_status st = validate(x, dtype, rows, N, row_stride, k, B, B2, out_vals, out_idx);
+    if (B < 0 || B2 < 0) return DS_ERR_INVALID_ARG;
+    if (rows > 0 && (B == 0 || B2 == 0)) {  // the library's choice (resolve_blocks)
+        int d = 0;
+        if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) return DS_ERR_CUDA;
+        const ds_status rs = resolve_blocks(d, rows, B, B2);
+        if (rs != DS_OK) return rs;
+    }
+    ds_status st = validate(x, dtype, rows, N, row_stride, k, B ? B : 4096, B2 ? B2 : 4096, out_vals, out_idx);
     if (st != DS_OK) return st;
     if (rows == 0) return DS_OK;
     int dev = 0;
@@ -1279,9 +1376,9 @@ ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N,
     }
     if (dtype == DS_BF16)
         return launch<uint16_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, false,
-                                stream);
+                                false, stream);
     return launch<uint32_t>(P, x, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, nullptr, ws, false,
-                            stream);
+                            false, stream);
 }
 
 size_t ds_noalloc_scratch_bytes(void) { return kStaticWorkspaceBytes; }
