@@ -289,7 +289,66 @@ def time_shapes(dev, ds, l2, peak, regions=7, budget_ms=3.0):
         del g
     cache.clear()
     torch.cuda.empty_cache()
+    out.append(_time_sampling(dev, ds, l2, peak, regions))
     return out
+
+
+def _time_sampling(dev, ds, l2, peak, regions, k=512, temperature=1.0):
+    """The sampler's use of top-k end to end on the device: ds_topk_sample on the sampler
+    shape (sorted top-k, softmax of the k logits, one draw per row from given uniforms)."""
+    import torch
+    import synth
+    w = synth.sampler_f32()
+    x0 = torch.from_numpy(w.x).to(dev)
+    R = max(1, -(-4 * l2 // x0.numel() // 4))
+    xs = [x0] + [x0.clone() for _ in range(R - 1)]
+    u = torch.rand(w.rows, generator=torch.Generator().manual_seed(7)).to(dev)
+    vals = torch.empty((w.rows, k), dtype=torch.float32, device=dev)
+    idx = torch.empty((w.rows, k), dtype=torch.int32, device=dev)
+    tok = torch.empty(w.rows, dtype=torch.int32, device=dev)
+    prob = torch.empty(w.rows, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def call(i):
+        st = ds.ds_topk_sample(xs[i % R].data_ptr(), w.dtype, w.rows, w.N, w.stride, k, w.B, w.B2, SEED, temperature,
+                               u.data_ptr(), vals.data_ptr(), idx.data_ptr(), tok.data_ptr(), prob.data_ptr(),
+                               stream.cuda_stream)
+        if st != 0:
+            raise ds.DSError(st)
+
+    with torch.cuda.stream(stream):
+        call(0)
+    stream.synchronize()
+    G = max(R, 40)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                call(i)
+        g.replay()
+    stream.synchronize()
+    ts = []
+    for _ in range(regions):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3 / G)
+    us = statistics.median(ts)
+    step_bytes = w.rows * w.N * 4
+    gbs = step_bytes / (us * 1e-6) / 1e9
+    res = {"workload": f"sampler_f32 256x129280 top-k sampling (sorted top-k, softmax, one draw per row; "
+                       f"temperature {temperature})", "k": k, "B": w.B, "B2": w.B2, "us_per_call": round(us, 3),
+           "us_min": round(min(ts), 3), "us_max": round(max(ts), 3), "value": round(gbs, 1), "unit": "GB/s",
+           "hbm_frac_of_peak": round(gbs / peak, 4), "calls_per_graph": G, "input_copies": R,
+           "device_status": ds.ds_get_device_status(stream.cuda_stream),
+           "launches_per_call": 3}
+    del g, xs
+    torch.cuda.empty_cache()
+    return res
 
 def _cpu_sort(seconds: float, sh: "Shape", threads: int | None = None):
     """The oracle's full stable sort (the definition of the result) over the workload's

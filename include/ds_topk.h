@@ -169,6 +169,29 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
 ds_status ds_workspace_bytes(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t B,
                              int32_t B2, const ds_options* options, size_t* bytes);
 
+/*
+ * ds_topk_sample -- top-k sampling, the sampler use of top-k (DeepSelect TopK tutorial,
+ * section 1.1: at sampling time top-k picks the candidate tokens out of the vocabulary's
+ * logits).  Per row: the k largest logits, sorted as with ds_options.sorted (value
+ * descending, equal values by column ascending), are written to out_vals / out_idx as by
+ * ds_topk_ex; candidate i gets weight w_i = exp((v_i - v_0) / temperature); the row's
+ * token is out_idx[row*k + j] for the first j whose running sum w_0 + ... + w_j exceeds
+ * uniforms[row] * (w_0 + ... + w_{k-1}) (the last candidate if rounding leaves none), and
+ * out_prob[row] = w_j / (sum of all w).  Weights and sums are fp32, summed in candidate
+ * order.
+ *   logits, dtype .. seed, out_vals, out_idx   as ds_topk (B = 0 / B2 = 0 allowed)
+ *   temperature  > 0 and finite, else DS_ERR_INVALID_ARG
+ *   uniforms     device, rows floats in [0, 1): the caller's random draws (one per row)
+ *   out_token    device, rows int32: the sampled column of each row
+ *   out_prob     device, rows floats, or NULL: the sampled candidate's probability
+ * Logits are expected finite (an infinite or NaN logit makes the weights undefined; the
+ * top-k part is exact for any values).  Asynchronous on `stream`.
+ */
+ds_status ds_topk_sample(const void* logits, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride,
+                         int32_t k, int32_t B, int32_t B2, uint64_t seed, float temperature,
+                         const float* uniforms, void* out_vals, int32_t* out_idx, int32_t* out_token,
+                         float* out_prob, cudaStream_t stream);
+
 /* Synchronizes `stream`, then reads and clears the calling device's status word:
    DS_OK, DS_ERR_TIMEOUT or DS_ERR_INTERNAL. */
 ds_status ds_get_device_status(cudaStream_t stream);

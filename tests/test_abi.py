@@ -228,3 +228,13 @@ def test_library_chooses_block_sizes_on_a_described_device(lib):
         assert got[rows] == [4096, 4096]
     assert got["given_B"] == [4096, 4096]
     assert got["given_B2"] == [8192, 1024]
+
+
+def test_topk_sample_host_validation(lib):
+    import top_selection_gb300 as ds
+    a = [P, 1, 2, 1000, 1024, 8, 64, 64, 1]
+    for t in (0.0, -1.0, float("nan"), float("inf")):
+        assert ds.ds_topk_sample(*a, t, P, P, P, P, P, 0) == 1
+    assert ds.ds_topk_sample(*a, 1.0, 0, P, P, P, P, 0) == 1      # no uniforms
+    assert ds.ds_topk_sample(*a, 1.0, P, P, P, 0, P, 0) == 1      # no token output
+    assert ds.ds_topk_sample(P, 1, 0, 1000, 1024, 8, 64, 64, 1, 1.0, 0, P, P, 0, 0, 0) == 0   # no rows

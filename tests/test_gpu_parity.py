@@ -496,3 +496,43 @@ def test_sorted_output_every_path(parts, cluster, dtype):
     for k in (7, 777, 4096):
         v, i, _ = run_gpu(x, dtype, k, B, B, 5, parts=parts, cluster=cluster, sorted=True)
         check_sorted(x, dtype, k, v, i)
+
+
+# ---------------------------------------------------------------- top-k sampling ----
+
+@pytest.mark.parametrize("shape,k,temperature", [
+    ("sampler", 1, 1.0), ("sampler", 64, 0.7), ("sampler", 512, 1.0), ("sampler", 512, 2.5),
+    ("sampler", 4096, 1.0), ("indexer", 512, 1.0)])
+def test_topk_sample_matches_oracle(shape, k, temperature):
+    """ds_topk_sample: the sorted top-k matches the oracle's sequence, and the sampled
+    column is the oracle's, except where the row's uniform draw lies within the fp32
+    rounding bound of a boundary of the oracle's running sums (the GPU sums weights in
+    fp32, the oracle in fp64); the reported probability matches within that bound."""
+    import top_selection_gb300 as ds
+    w = synth.sampler_f32(rows=48) if shape == "sampler" else synth.indexer_bf16(rows=16)
+    rng = np.random.default_rng(k * 7 + int(temperature * 10))
+    u = rng.random(w.rows).astype(np.float32)
+    u[0], u[1] = 0.0, np.float32(0.99999994)
+    xt = to_device(w.x, w.dtype)
+    tok, prob, vals, idx = ds.topk_sample(xt, k, temperature, torch.from_numpy(u).cuda(), B=w.B, B2=w.B2, N=w.N)
+    assert ds.ds_get_device_status() == 0
+    v = vals.cpu().numpy()
+    v = v.view(np.uint16) if w.dtype == synth.BF16 else v.view(np.uint32)
+    i = idx.cpu().numpy()
+    check_sorted(w.x, w.dtype, k, v, i, N=w.N, threads=16)
+    bits = bits_of(w.x, w.dtype)
+    otok, oprob, ocdf = oracle.topk_sample(np.ascontiguousarray(bits[:, :w.N]), w.dtype, k, temperature,
+                                           u.astype(np.float64), threads=16)
+    tok, prob = tok.cpu().numpy(), prob.cpu().numpy()
+    tol = (k + 8) * 2.0 ** -22
+    for r in range(w.rows):
+        pos = np.nonzero(i[r] == tok[r])[0]
+        assert pos.size == 1, f"row {r}: sampled column is not one of the row's top-k"
+        p = int(pos[0])
+        if tok[r] != otok[r]:
+            lo = ocdf[r, p - 1] if p > 0 else 0.0
+            assert lo - tol <= u[r] <= ocdf[r, p] + tol, f"row {r}: token {tok[r]} vs oracle {otok[r]}"
+        else:
+            assert abs(prob[r] - oprob[r]) <= tol + 1e-6 * oprob[r], f"row {r}: probability"
+    if k == 1:
+        assert np.array_equal(tok, i[:, 0])

@@ -101,6 +101,9 @@ def load():
         lib.ds_wait_probe.restype = ctypes.c_int
         lib.ds_topk_noalloc.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, u64, vp, vp, i32, i32, vp]
         lib.ds_topk_noalloc.restype = ctypes.c_int
+        lib.ds_topk_sample.argtypes = [vp, i32, i64, i64, i64, i32, i32, i32, u64, ctypes.c_float, vp, vp, vp,
+                                       vp, vp, vp]
+        lib.ds_topk_sample.restype = ctypes.c_int
         lib.ds_noalloc_scratch_bytes.argtypes = []
         lib.ds_noalloc_scratch_bytes.restype = ctypes.c_size_t
         _lib = lib
@@ -230,3 +233,43 @@ def topk(x, k: int, B: int, B2: int, seed: int = 0x5EED, N: int | None = None,
     if st != 0:
         raise DSError(st)
     return vals, idx
+
+
+def ds_topk_sample(x, dtype, rows, N, row_stride, k, B, B2, seed, temperature, uniforms, out_vals, out_idx,
+                   out_token, out_prob=0, stream=0) -> int:
+    """Raw C call (device pointers as ints); returns the ds_status code."""
+    return load().ds_topk_sample(int(x) or None, dtype, rows, N, row_stride, k, B, B2, seed, float(temperature),
+                                 int(uniforms) or None, int(out_vals) or None, int(out_idx) or None,
+                                 int(out_token) or None, int(out_prob) or None, int(stream) or None)
+
+
+def topk_sample(x, k: int, temperature: float, uniforms, B: int = 0, B2: int = 0, seed: int = 0x5EED,
+                N: int | None = None, stream=None):
+    """Top-k sampling of each row of the CUDA logits tensor ``x`` (rows, stride): the
+    sorted top-k (values, columns), then one column drawn per row from the softmax of the
+    k values at ``temperature`` with the row's uniform draw from ``uniforms`` (a CUDA
+    float32 tensor of rows values in [0, 1)).  Returns (token, prob, values, indices)."""
+    import torch
+    if not x.is_cuda or not uniforms.is_cuda:
+        raise ValueError("x and uniforms must be CUDA tensors (there is no CPU path)")
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with unit column stride")
+    if uniforms.dtype != torch.float32 or uniforms.numel() != x.shape[0] or not uniforms.is_contiguous():
+        raise ValueError("uniforms must be a contiguous float32 tensor with one value per row")
+    dtype = _torch_dtype_code(x)
+    rows = x.shape[0]
+    n = x.shape[1] if N is None else int(N)
+    stride = x.stride(0) if rows > 1 else x.shape[1]
+    vals = torch.empty((rows, k), dtype=x.dtype, device=x.device)
+    idx = torch.empty((rows, k), dtype=torch.int32, device=x.device)
+    token = torch.empty(rows, dtype=torch.int32, device=x.device)
+    prob = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = ds_topk_sample(x.data_ptr(), dtype, rows, n, stride, k, B, B2, seed, temperature, uniforms.data_ptr(),
+                        vals.data_ptr(), idx.data_ptr(), token.data_ptr(), prob.data_ptr(), stream)
+    if st != 0:
+        raise DSError(st, "ds_topk_sample")
+    return token, prob, vals, idx

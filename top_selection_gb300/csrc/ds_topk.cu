@@ -788,6 +788,73 @@ __global__ void __launch_bounds__(kSortThreads) ds_sort_kernel(void* vals, int32
     }
 }
 
+// ---------------------------------------------------------------- sampling ------
+// Top-k sampling, the second place the pages put top-k (the DeepSelect TopK tutorial,
+// section 1.1: the sampler picks candidate tokens from the vocabulary's logits with
+// top-k).  After the sorted top-k of a row (value descending, equal values by column
+// ascending), candidate i gets weight e_i = exp((v_i - v_0) / temperature) and the token
+// is the candidate at the first i whose running sum of weights exceeds u * (sum of all
+// weights), u being the row's uniform draw in [0, 1) (supplied by the caller).  One CTA
+// per row: each thread sums a run of consecutive candidates, a CTA scan gives each run's
+// offset, and the count of running sums <= u * total is the chosen position.  fp32
+// throughout (expf, sums in this fixed order).
+constexpr int kSampleThreads = 256;
+
+template <typename KeyT>
+__global__ void __launch_bounds__(kSampleThreads) ds_sample_kernel(const void* vals, const int32_t* idx, int k,
+                                                                   float inv_temp, const float* uniforms,
+                                                                   int32_t* out_token, float* out_prob) {
+    constexpr int ES = sizeof(KeyT);
+    __shared__ float wsum[kSampleThreads / 32];
+    __shared__ int wcnt[kSampleThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * k;
+    const auto value = [&](int i) -> float {
+        if (ES == 2) return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(vals)[base + i]) << 16);
+        return static_cast<const float*>(vals)[base + i];
+    };
+    const float v0 = value(0);
+    const int per = (k + kSampleThreads - 1) / kSampleThreads;
+    const int i0 = tid * per, i1 = min(i0 + per, k);
+    float run = 0.f;
+    for (int i = i0; i < i1; ++i) run += expf((value(i) - v0) * inv_temp);
+    // exclusive scan of the runs over the CTA (warp scan, then the warp totals)
+    float incl = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const float t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += t;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    float before = 0.f, total = 0.f;
+    for (int w = 0; w < kSampleThreads / 32; ++w) {
+        const float t = wsum[w];
+        before += w < warp ? t : 0.f;
+        total += t;
+    }
+    before += incl - run;
+    const float target = uniforms[blockIdx.x] * total;
+    // positions whose running sum is <= target: the token is the next one
+    int cnt = 0;
+    float acc = before;
+    for (int i = i0; i < i1; ++i) {
+        acc += expf((value(i) - v0) * inv_temp);
+        cnt += acc <= target ? 1 : 0;
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, d);
+    if (lane == 0) wcnt[warp] = cnt;
+    __syncthreads();
+    if (tid == 0) {
+        int c = 0;
+        for (int w = 0; w < kSampleThreads / 32; ++w) c += wcnt[w];
+        const int pos = c < k ? c : k - 1;
+        out_token[blockIdx.x] = idx[base + pos];
+        if (out_prob) out_prob[blockIdx.x] = expf((value(pos) - v0) * inv_temp) / total;
+    }
+}
+
 // ================================================================ host ============
 
 struct DevInfo {
@@ -1382,6 +1449,29 @@ ds_status ds_topk_noalloc(const void* x, int32_t dtype, int64_t rows, int64_t N,
 }
 
 size_t ds_noalloc_scratch_bytes(void) { return kStaticWorkspaceBytes; }
+
+// Top-k sampling: the sorted top-k of each row (ds_topk_ex with options.sorted), then
+// ds_sample_kernel draws one token per row from the softmax of the k values.
+ds_status ds_topk_sample(const void* logits, int32_t dtype, int64_t rows, int64_t N, int64_t row_stride, int32_t k,
+                         int32_t B, int32_t B2, uint64_t seed, float temperature, const float* uniforms,
+                         void* out_vals, int32_t* out_idx, int32_t* out_token, float* out_prob,
+                         cudaStream_t stream) {
+    if (!(temperature > 0.f) || !(temperature < INFINITY)) return DS_ERR_INVALID_ARG;
+    if (rows > 0 && (!uniforms || !out_token)) return DS_ERR_INVALID_ARG;
+    ds_options opt = {};
+    opt.sorted = 1;
+    const ds_status st = ds_topk_ex(logits, dtype, rows, N, row_stride, k, B, B2, seed, out_vals, out_idx, &opt,
+                                    stream);
+    if (st != DS_OK || rows == 0) return st;
+    const float inv = 1.0f / temperature;
+    if (dtype == DS_BF16)
+        ds_sample_kernel<uint16_t><<<static_cast<unsigned>(rows), kSampleThreads, 0, stream>>>(
+            out_vals, out_idx, k, inv, uniforms, out_token, out_prob);
+    else
+        ds_sample_kernel<uint32_t><<<static_cast<unsigned>(rows), kSampleThreads, 0, stream>>>(
+            out_vals, out_idx, k, inv, uniforms, out_token, out_prob);
+    return cudaGetLastError() == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
 
 ds_status ds_get_device_status(cudaStream_t stream) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return DS_ERR_CUDA;
