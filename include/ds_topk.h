@@ -234,7 +234,10 @@ ds_status ds_wait_probe(int64_t cycles, cudaStream_t stream);
  * library routine.
  *
  * The first call on a device that needs the scratch looks up its device address (with
- * that device current); make that first call before any stream capture.  All calls
+ * that device current); make that first call before any stream capture.  The address is
+ * kept per device index for the life of the process: after cudaDeviceReset (or with a
+ * different primary context for that device) the kept address is stale, so such a
+ * process must not call this entry point again on that device.  All calls
  * share the one array: calls whose work overlaps on the GPU (for instance on different
  * streams) race on it and must be ordered by the caller.
  */

@@ -536,3 +536,22 @@ def test_topk_sample_matches_oracle(shape, k, temperature):
             assert abs(prob[r] - oprob[r]) <= tol + 1e-6 * oprob[r], f"row {r}: probability"
     if k == 1:
         assert np.array_equal(tok, i[:, 0])
+
+
+@pytest.mark.slow
+def test_workload_huge_f32_full_row_against_the_oracle():
+    """The whole 268,435,456-element row (not a slice): the GPU's top 32 and top 4096, in
+    the launch the planner picks for it (256 parts over clusters of 8 and the merge
+    kernel), against the oracle's full stable sort of the same row (a few minutes of CPU)."""
+    w = synth.huge_f32()
+    got = {k: run_gpu(w.x, w.dtype, k, w.B, w.B2, 0x5EED)[:2] for k in (32, 4096)}
+    bits = w.x.view(np.uint32)
+    ref_v, ref_i = oracle.topk_sort(bits, w.dtype, 4096, threads=1)
+    for k, (v, i) in got.items():
+        rv, ri = ref_v[:, :k], ref_i[:, :k]
+        assert sorted(v[0].tolist()) == sorted(rv[0].tolist()), f"k={k}: value multiset differs"
+        ir = i[0].astype(np.int64)
+        assert len(set(ir.tolist())) == k and np.array_equal(bits[0][ir], v[0])
+        kth = oracle.key(int(rv[0][-1]), w.dtype)
+        keys = np.array([oracle.key(int(x), w.dtype) for x in rv[0]], dtype=np.int64)
+        assert set(ri[0][keys > kth].tolist()) <= set(ir.tolist()), f"k={k}: a value above the k-th is missing"
