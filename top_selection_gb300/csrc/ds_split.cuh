@@ -1164,6 +1164,20 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             break;
         }
         krem -= pv.above;
+        if (s > 0 || bstar == kXBins - 1) {
+            // The bin holds exactly the keys still needed: take it whole, with every key
+            // above it, and stop (no further pass to find the pivot key inside it).
+            uint32_t binc = 0u;
+            for (int c = 0; c < G; ++c) binc += reinterpret_cast<const uint16_t*>(rows)[c * kXBins + bstar];
+            const uint32_t lo_bin = lbase + (static_cast<uint32_t>(bstar) << s);
+            if (binc == krem && lo_bin > 0u) {
+                pivot = lo_bin - 1u;  // keys above it are taken; none equal to it is
+                gt_lower += pv.eq_lower;
+                gt_all += binc;
+                krem = 0u;
+                break;
+            }
+        }
         if (s == 0 && bstar < kXBins - 1) {
             pivot = lbase + static_cast<uint32_t>(bstar);
             eq_lower = pv.eq_lower;
