@@ -209,6 +209,58 @@ def test_longctx_ascending_compactions_make_progress(seed):
     check_topk(w.x, w.dtype, 2048, v, i, N=w.N, threads=16)
 
 
+# ---------------------------------------------------------------- hot sampled blocks -
+
+def _spikes_in_sampled_blocks(w, k, seed):
+    """w's rows with spikes U(8, 12) in the first block each part of the planned split
+    visits (that block is always in the warm-up's sample), k - 32 of them per row in all:
+    the sample holds nearly all of the row's largest values, fewer than k, and its group
+    maxima overstate how many large values the rest of the row holds."""
+    import top_selection_gb300 as ds
+    plan = ds.ds_get_plan(w.dtype, w.rows, w.N, k, w.B, w.B2)
+    parts = plan["parts"]
+    m = -(-w.N // w.B)
+    mq, mr = divmod(m, parts)
+    x = w.x[:, : w.N].copy()
+    xf = synth.bf16_bits_to_f32(x) if w.dtype == synth.BF16 else x
+    rng = np.random.default_rng(0xB10C)
+    per = (k - 32) // parts
+    for r in range(w.rows):
+        for p in range(parts):
+            b0 = p * mq + min(p, mr)
+            mp = mq + (1 if p < mr else 0)
+            first = min((oracle.block_draw(seed, r, b), b) for b in range(b0, b0 + mp))[1]
+            lo, hi = first * w.B, min(first * w.B + w.B, w.N)
+            cols = lo + rng.choice(hi - lo, size=per, replace=False)
+            xf[r, cols] = rng.uniform(8.0, 12.0, size=per).astype(np.float32)
+    return synth.f32_to_bf16_bits(xf) if w.dtype == synth.BF16 else xf
+
+
+@pytest.mark.parametrize("shape,k", [("indexer", 512), ("indexer", 2048), ("row65536", 512)])
+def test_spikes_in_every_sampled_block(shape, k):
+    w = {"indexer": synth.indexer_bf16, "row65536": synth.row65536_f32}[shape]()
+    seed = 0x5EED
+    x = _spikes_in_sampled_blocks(w, k, seed)
+    v, i, _ = run_gpu(x, w.dtype, k, w.B, w.B2, seed)
+    check_topk(x, w.dtype, k, v, i, threads=16)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_one_hot_block_per_row(seed):
+    # One block per row with k - 32 spikes, at a random position: the warm-up samples the
+    # hot block in some rows and not in others.
+    w = synth.indexer_bf16()
+    x = synth.bf16_bits_to_f32(w.x[:, : w.N].copy())
+    rng = np.random.default_rng(seed)
+    for r in range(w.rows):
+        b = int(rng.integers(0, w.N // w.B))
+        cols = b * w.B + rng.choice(w.B, size=480, replace=False)
+        x[r, cols] = rng.uniform(8.0, 12.0, size=480).astype(np.float32)
+    x = synth.f32_to_bf16_bits(x)
+    v, i, _ = run_gpu(x, w.dtype, 512, w.B, w.B2, seed)
+    check_topk(x, w.dtype, 512, v, i, threads=16)
+
+
 @pytest.mark.parametrize("k", [32, 4096])
 def test_workload_huge_f32(k):
     w = synth.huge_f32()

@@ -635,7 +635,11 @@ __device__ __forceinline__ uint32_t split_output(const KeyT* ckey, const uint32_
     return bad;
 }
 
-template <typename KeyT>
+// HELD: every CTA's chunks fit its ring at once (no refills, no streamed-row threshold
+// raises or refined warm-up, a sample of at most 8 vectors per thread); MCT: rows span
+// several clusters.  The launch picks the instance for its plan, so each call runs only
+// its own class's code.
+template <typename KeyT, bool HELD, bool MCT>
 __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanParams p) {
     constexpr int NC = kSplitThreads;
     constexpr int NT = kSplitThreads;
@@ -679,7 +683,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         }
     };
     const int nq = mp * cpb;
-    const bool MC = p.C > 1;
+    constexpr bool MC = MCT;
     const uint32_t cap = static_cast<uint32_t>(p.cap);
 
     // The next kernel on the stream may start as this one's CTAs leave.  This kernel may
@@ -835,7 +839,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // log2 of vectors per group
             const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            if (VT <= 8) {
+            if (HELD || VT <= 8) {
                 uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
                 if (VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
                 else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
@@ -920,7 +924,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // this needs no exchange).  At least k maxima, each an element of the row, lie
             // at or above it.
             uint32_t edge = 0u;
-            if (!p.refine) {
+            if (HELD || !p.refine) {
                 if (total >= static_cast<uint32_t>(p.k) && bstar > 0) {
                     edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
                     if (tid == 0) ctrl->wedge = edge;
@@ -974,7 +978,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             bool have = hasT;
             {
                 uint32_t sh = gnext;
-                if ((G > 1 || p.rstep) && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+                if ((G > 1 || (!HELD && p.rstep)) && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
                 sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
                 if (sh != 0u && (!have || sh > tk)) {
                     tk = sh;
@@ -1013,7 +1017,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 }
             }
             __syncwarp();  // every lane is done with the stage: refill it with this warp's next chunk there
-            if (lane == 0 && got && q + p.stages < nq && !*reinterpret_cast<volatile int*>(&ctrl->abort)) {
+            if (!HELD && lane == 0 && got && q + p.stages < nq &&
+                !*reinterpret_cast<volatile int*>(&ctrl->abort)) {
                 int bj = bi + dS, sj = sub + rS;
                 if (sj >= cpb) {
                     sj -= cpb;
@@ -1021,7 +1026,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 }
                 issue_to(s, use + 1, bj, sj);
             }
-            if (p.rstep) {  // one warp raises the threshold each time the buffer passes the mark
+            if (!HELD && p.rstep) {  // one warp raises the threshold each time the buffer passes the mark
                 int due = 0;
                 if (lane == 0) {
                     const uint32_t c = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&ctrl->cnt));

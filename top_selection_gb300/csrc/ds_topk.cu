@@ -958,6 +958,7 @@ struct Plan {
     int dev, es, parts, G, C, chunk, stages, cap, perm_cap, ctas_per_sm, wm, ww, refine;
     int B, B2;  // block size and compaction slack in effect (the library's choice when given as 0)
     bool split;  // the split-row kernel (also for one part per row), else the one-CTA-per-row kernel
+    bool held;   // split rows: every CTA's chunks fit its ring at once
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -1055,6 +1056,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.wm = 0;
     P.ww = 1;
     P.refine = 0;
+    P.held = false;
     P.split = parts > 1 || split1;
     if (P.split) {
         // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
@@ -1128,6 +1130,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             ok = fit(c, kNCW, static_cast<size_t>(di.smem_optin));
         if (!ok && first * P.es < 1024) ok = fit(first, kNCW, static_cast<size_t>(di.smem_optin));
         if (!ok) return DS_ERR_UNSUPPORTED;
+        P.held = (P.m + parts - 1) / parts * ((static_cast<int64_t>(B) + P.chunk - 1) / P.chunk) <= P.stages;
     } else {
         const auto layout_bytes = [&](int s) -> size_t {
             return scan_layout(P.es, P.chunk, s, P.cap, P.perm_cap).total;
@@ -1179,8 +1182,8 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
 // call under stream capture only launches.
 template <typename Kern>
 static cudaError_t set_smem(Kern kern, int slot, int dev, size_t bytes, bool nonportable) {
-    static size_t done[8][64];
-    static bool np_done[8][64];
+    static size_t done[16][64];
+    static bool np_done[16][64];
     std::lock_guard<std::mutex> lk(g_mu);
     if (done[slot][dev] < bytes) {
         cudaError_t e =
@@ -1252,8 +1255,10 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     if (!P.split) {
         kern = ds_scan_kernel<KeyT>;
     } else {
-        kern = ds_split_kernel<KeyT>;
-        slot += 2;
+        // one instance per plan class: held whole or streamed, one cluster or several
+        kern = P.held ? (P.C > 1 ? ds_split_kernel<KeyT, true, true> : ds_split_kernel<KeyT, true, false>)
+                      : (P.C > 1 ? ds_split_kernel<KeyT, false, true> : ds_split_kernel<KeyT, false, false>);
+        slot += 8 + 2 * (P.held ? 1 : 0) + 4 * (P.C > 1 ? 1 : 0);
     }
     if (set_smem(kern, slot, P.dev, P.smem, P.G > 8) != cudaSuccess) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
