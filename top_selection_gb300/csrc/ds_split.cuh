@@ -299,6 +299,134 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
     return r;
 }
 
+// The bucket of the kk-th largest count among 2048, found by the whole CTA (kSplitThreads
+// threads): thread t sums buckets [8t, 8t + 8), suffix sums over the threads (a shuffle
+// scan in each warp, then the warps' totals through `wt`) pick the thread whose buckets
+// hold it, and that thread walks its eight.  Sets ctrl->bstar (-1 when all buckets
+// together hold fewer than kk), ctrl->above (the count in buckets above it; all of them
+// when none) and ctrl->bcount (the total).  Every thread calls it; it ends with a barrier.
+__device__ __forceinline__ void cta_bucket_2048(const uint32_t* hist, uint32_t kk, int tid, uint32_t* wt, Ctrl* ctrl) {
+    static_assert(kBins == 8 * kSplitThreads, "eight buckets per thread");
+    const int lane = tid & 31, warp = tid >> 5;
+    const uint4 a = reinterpret_cast<const uint4*>(hist)[2 * tid];
+    const uint4 b = reinterpret_cast<const uint4*>(hist)[2 * tid + 1];
+    const uint32_t c[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const uint32_t t = c[0] + c[1] + c[2] + c[3] + c[4] + c[5] + c[6] + c[7];
+    uint32_t sf = t;  // buckets of this warp's threads >= tid
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
+        if (lane + d < 32) sf += u;
+    }
+    if (lane == 0) wt[warp] = sf;
+    __syncthreads();
+    uint32_t tot = 0u, up = 0u;
+#pragma unroll
+    for (int w = 0; w < kSplitThreads / 32; ++w) {
+        const uint32_t x = wt[w];
+        tot += x;
+        up += w > warp ? x : 0u;
+    }
+    const uint32_t incl = sf + up;  // buckets of threads >= tid
+    if (incl >= kk && incl - t < kk) {
+        uint32_t acc = incl - t;
+        int bs = 8 * tid;
+        bool found = false;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            if (!found) {
+                if (acc + c[j] >= kk) {
+                    found = true;
+                    bs = 8 * tid + j;
+                } else {
+                    acc += c[j];
+                }
+            }
+        }
+        ctrl->bstar = bs;
+        ctrl->above = acc;
+    }
+    if (tid == 0) {
+        if (tot < kk) {
+            ctrl->bstar = -1;
+            ctrl->above = tot;
+        }
+        ctrl->bcount = tot;
+    }
+    __syncthreads();
+}
+
+// warp_pivot_x's result found by the whole CTA: thread t owns bins 2t and 2t + 1 (word t
+// of every CTA's row), suffix sums go through `wt` as in cta_bucket_2048, and the thread
+// holding the krem-th largest key writes the pivot to ctrl->fp_tot[0..3] (bstar, above,
+// low_above, eq_lower).  Every thread calls it; it ends with a barrier.
+__device__ __forceinline__ void cta_pivot_x(const uint32_t* rows, int G, int crank, uint32_t krem, int tid,
+                                            uint32_t* wt, Ctrl* ctrl) {
+    static_assert(kXBins == 2 * kSplitThreads, "two bins per thread");
+    constexpr int XW = kXBins / 2;
+    constexpr int NW = kSplitThreads / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t a0 = 0u, a1 = 0u, l0 = 0u, l1 = 0u;  // bins 2t, 2t + 1: all CTAs, CTAs of rank below crank
+#pragma unroll 4
+    for (int c = 0; c < G; ++c) {
+        if (c == crank) {
+            l0 = a0;
+            l1 = a1;
+        }
+        const uint32_t w = rows[static_cast<size_t>(c) * XW + tid];
+        a0 += w & 0xFFFFu;
+        a1 += w >> 16;
+    }
+    const uint32_t t = a0 + a1, tl = l0 + l1;
+    uint32_t sf = t, sl = tl;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
+        const uint32_t v = __shfl_down_sync(0xFFFFFFFFu, sl, d);
+        if (lane + d < 32) {
+            sf += u;
+            sl += v;
+        }
+    }
+    if (lane == 0) {
+        wt[warp] = sf;
+        wt[NW + warp] = sl;
+    }
+    __syncthreads();
+    uint32_t tot = 0u, totl = 0u, up = 0u, upl = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const uint32_t x = wt[w], y = wt[NW + w];
+        tot += x;
+        totl += y;
+        up += w > warp ? x : 0u;
+        upl += w > warp ? y : 0u;
+    }
+    const uint32_t incl = sf + up, incll = sl + upl;  // keys in bins >= 2t
+    if (incl >= krem && incl - t < krem) {
+        uint32_t acc = incl - t, lacc = incll - tl;
+        int bs = 2 * tid + 1;
+        uint32_t eql = l1;
+        if (acc + a1 < krem) {
+            acc += a1;
+            lacc += l1;
+            bs = 2 * tid;
+            eql = l0;
+        }
+        ctrl->fp_tot[0] = static_cast<uint32_t>(bs);
+        ctrl->fp_tot[1] = acc;
+        ctrl->fp_tot[2] = lacc;
+        ctrl->fp_tot[3] = eql;
+    }
+    if (tid == 0 && tot < krem) {
+        ctrl->fp_tot[0] = static_cast<uint32_t>(-1);
+        ctrl->fp_tot[1] = tot;
+        ctrl->fp_tot[2] = totl;
+        ctrl->fp_tot[3] = 0u;
+    }
+    __syncthreads();
+}
+
 // Counts a key in the final select's first histogram (kXBins 16-bit counts in pairs):
 // keys from `edge` up, in bins of 2^s keys, the last bin open-ended.
 __device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t edge, int s) {
@@ -497,7 +625,8 @@ __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, ui
     const int cb = ctrl->cut_bin;
     const uint32_t keep = ctrl->cut_keep;
     uint32_t nt;
-    if (cb > 0 && keep <= static_cast<uint32_t>(k + (cap - k) / 2) && keep + static_cast<uint32_t>(room) <= static_cast<uint32_t>(cap)) {
+    if (cb > 0 && keep <= static_cast<uint32_t>(k + (cap - k) / 2) &&
+        keep + static_cast<uint32_t>(room) <= static_cast<uint32_t>(cap)) {
         const uint32_t lo = hedge + (static_cast<uint32_t>(cb) << hs0);
         constexpr int PER = 4;
         uint32_t off = 0u;
@@ -778,8 +907,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // every consumer warp calls this together (from its chunk loop or the drain); the
         // work is out of line, away from the chunk loop's code
         const auto join_compaction = [&]() {
-            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.chunk, p.k, tmax, tid, hasT, T, xh0, hedge, hs0, G,
-                                       MC ? p.gT + row : nullptr, p.epoch);
+            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.chunk, p.k, tmax, tid, hasT, T, xh0, hedge,
+                                       hs0, G, MC ? p.gT + row : nullptr, p.epoch);
             hasT = true;
         };
         // A warp waiting for its next chunk joins any compaction requested meanwhile, so
@@ -870,53 +999,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
             }
             __syncthreads();
-            // the bucket of the k-th largest, found by warp 0: lane l sums buckets
-            // [64l, 64l + 64), then the lanes split the chosen lane's buckets in pairs
-            if (warp == 0) {
-                const uint32_t kk = static_cast<uint32_t>(p.k);
-                const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 16 * lane;
-                uint32_t t = 0u;
-#pragma unroll 4
-                for (int j = 0; j < 16; ++j) {
-                    const uint4 x = h4[(j + lane) & 15];  // rotated: fewer bank conflicts
-                    t += x.x + x.y + x.z + x.w;
-                }
-                uint32_t sf = t;  // buckets of lanes >= lane
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, sf, d);
-                    if (lane + d < 32) sf += u;
-                }
-                const uint32_t tot = __shfl_sync(0xFFFFFFFFu, sf, 0);
-                const uint32_t hit = __ballot_sync(0xFFFFFFFFu, sf >= kk);
-                int bs = -1;
-                uint32_t ab = tot;
-                if (hit) {
-                    const int L = 31 - __clz(hit);
-                    const uint32_t aboveL = __shfl_sync(0xFFFFFFFFu, sf - t, L);
-                    const uint2 c2 = reinterpret_cast<const uint2*>(hist)[32 * L + lane];
-                    const uint32_t c = c2.x + c2.y;
-                    uint32_t s2 = c;
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const uint32_t u = __shfl_down_sync(0xFFFFFFFFu, s2, d);
-                        if (lane + d < 32) s2 += u;
-                    }
-                    const uint32_t hit2 = __ballot_sync(0xFFFFFFFFu, aboveL + s2 >= kk);
-                    const int J = 31 - __clz(hit2);
-                    const uint32_t aJ = __shfl_sync(0xFFFFFFFFu, aboveL + s2 - c, J);
-                    const uint32_t hiJ = __shfl_sync(0xFFFFFFFFu, c2.y, J);
-                    const bool top = aJ + hiJ >= kk;
-                    bs = 64 * L + 2 * J + (top ? 1 : 0);
-                    ab = top ? aJ : aJ + hiJ;
-                }
-                if (lane == 0) {
-                    ctrl->bstar = bs;
-                    ctrl->above = ab;
-                    ctrl->bcount = tot;
-                }
-            }
-            __syncthreads();
+            // the bucket of the k-th largest maximum
+            cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
             const int bstar = ctrl->bstar;
             const uint32_t above = ctrl->above, total = ctrl->bcount;
             // The edge: the smallest key of the pivot bucket, or (refine) of the 32nd part of
@@ -978,7 +1062,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             bool have = hasT;
             {
                 uint32_t sh = gnext;
-                if ((G > 1 || (!HELD && p.rstep)) && lane == 0) sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
+                if ((G > 1 || (!HELD && p.rstep)) && lane == 0)
+                    sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
                 sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
                 if (sh != 0u && (!have || sh > tk)) {
                     tk = sh;
@@ -1144,18 +1229,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // ago and every peer has used it since): clear it for the next pass
         uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
         for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
-        // the cluster's histogram: warp 0 finds the pivot bin, the CTA reads it after a barrier
+        // the cluster's histogram: the CTA finds the pivot bin
         const uint32_t* rows = xr + static_cast<size_t>(lvl & 1) * G * XW;
-        if (warp == 0) {
-            const XPivot w0 = warp_pivot_x(rows, G, static_cast<int>(crank), krem, lane);
-            if (lane == 0) {
-                ctrl->fp_tot[0] = static_cast<uint32_t>(w0.bstar);
-                ctrl->fp_tot[1] = w0.above;
-                ctrl->fp_tot[2] = w0.low_above;
-                ctrl->fp_tot[3] = w0.eq_lower;
-            }
-        }
-        __syncthreads();
+        cta_pivot_x(rows, G, static_cast<int>(crank), krem, tid, ctrl->warp_tot[0], ctrl);
         XPivot pv;
         pv.bstar = static_cast<int>(ctrl->fp_tot[0]);
         pv.above = ctrl->fp_tot[1];
