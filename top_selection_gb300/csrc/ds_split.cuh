@@ -299,6 +299,28 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
     return r;
 }
 
+// Calls f(key) for each of keys[0, n), the CTA's threads taking one 16-byte vector each
+// at a time (n a multiple of the keys per vector, `keys` 16-byte aligned): the loads of a
+// thread's keys do not wait on one another.
+template <typename KeyT, typename F>
+__device__ __forceinline__ void each_key(const KeyT* keys, int n, int tid, F&& f) {
+    constexpr int KPV = 16 / static_cast<int>(sizeof(KeyT));
+    const uint4* v4 = reinterpret_cast<const uint4*>(keys);
+    for (int j = tid; j < n / KPV; j += kSplitThreads) {
+        const uint4 v = v4[j];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (sizeof(KeyT) == 2) {
+                f(w[i] & 0xFFFFu);
+                f(w[i] >> 16);
+            } else {
+                f(w[i]);
+            }
+        }
+    }
+}
+
 // The bucket of the kk-th largest count among 2048, found by the whole CTA (kSplitThreads
 // threads): thread t sums buckets [8t, 8t + 8), suffix sums over the threads (a shuffle
 // scan in each warp, then the warps' totals through `wt`) pick the thread whose buckets
@@ -994,10 +1016,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             }
             // histogram of the union's maxima by their top 11 key bits, and the bucket of
             // the k-th largest
-            for (int j = tid; j < G * wm; j += NC) {
-                const uint32_t kk = wx[j];
+            each_key<KeyT>(wx, G * wm, tid, [&](uint32_t kk) {
                 if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
-            }
+            });
             __syncthreads();
             // the bucket of the k-th largest maximum
             cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
@@ -1016,11 +1037,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             } else if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
                 constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
                 uint32_t* sub = ctrl->block_cnt[0];     // zero since start-up
-                for (int j = tid; j < G * wm; j += NC) {
-                    const uint32_t kk = wx[j];
+                each_key<KeyT>(wx, G * wm, tid, [&](uint32_t kk) {
                     if (kk && (kk >> (KW - kDigitBits)) == static_cast<uint32_t>(bstar))
                         atomicAdd(&sub[(kk >> SB) & 31u], 1u);
-                }
+                });
                 __syncthreads();
                 if (warp == 0) {
                     uint32_t sfx = sub[lane];  // maxima in parts >= lane of the bucket
@@ -1043,7 +1063,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 hedge = edge;
                 hs0 = ES == 2 ? 0 : 23 - kXBits;
             }
-            if (tid == 0 && hasT && (G > 1 || MC)) publish_T(T);
+            // (every CTA of the cluster derived this same threshold: only the row's other
+            // clusters need it)
+            if (tid == 0 && hasT && MC) publish_T(T);
         }
 
         // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
