@@ -59,6 +59,7 @@ struct Ctrl {
     int cut_bin;                 // split rows: a compaction's cut from that histogram (bin,
     uint32_t cut_keep;           //   keys kept)
     int last_kept;               // split rows: the buffer's count after the last compaction
+    uint32_t lmax;               // split rows: the largest of this CTA's warm-up group maxima
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

@@ -62,8 +62,8 @@ __host__ __device__ inline size_t split_scratch_bytes(int k) {
 }
 
 // wm: group maxima per CTA in the warm-up (a multiple of 256).  Regions that other CTAs
-// write into (wx: the warm-up's maxima, xf: two rounds of the final select's uint16
-// histograms) are separate from the copy ring and from each other, so a CTA that runs
+// write into (wx: the warm-up's maxima and each CTA's largest, xf: two rounds of the final
+// select's uint16 histograms) are separate from the copy ring and from each other, so a CTA that runs
 // ahead never writes over memory a slower CTA still uses.
 __host__ __device__ inline SplitLayout split_layout(int es, int chunk, int stages, int cap, int G, int wm, int k,
                                                    int perm_cap) {
@@ -77,8 +77,8 @@ __host__ __device__ inline SplitLayout split_layout(int es, int chunk, int stage
     off += align_up(static_cast<size_t>(cap) * 4, 16);
     L.scratch = off;
     off += split_scratch_bytes(k);
-    L.wx = off;
-    off += align_up(static_cast<size_t>(G) * wm * es, 16);
+    L.wx = off;  // G rows of wm maxima, each followed by a 16-byte slot for its largest
+    off += static_cast<size_t>(G) * (static_cast<size_t>(wm) * es + 16);
     L.xf = off;
     off += align_up(static_cast<size_t>(4) * kXBins * G, 16);
     L.perm = off;
@@ -185,12 +185,13 @@ __device__ __forceinline__ void warm_maxima(const uint4* v0, int tid, int cvec, 
 
 // The same for samples of 9..16 vectors per thread (rows streamed through the ring): up
 // to 8 chunks, groups of 2^gsh consecutive vectors of the thread, each group's key stored
-// straight to out[g] for g < R (no register array of groups).
+// straight to out[g] for g < R (no register array of groups).  Returns the largest key
+// stored.
 template <typename KeyT>
-__device__ __forceinline__ void warm_maxima16(const uint4* v0, int tid, int cvec, int ww, int VT, int gsh, int R,
+__device__ __forceinline__ uint32_t warm_maxima16(const uint4* v0, int tid, int cvec, int ww, int VT, int gsh, int R,
                                               bool gotw, const int (&nvw)[8], KeyT* out) {
     constexpr int ES = sizeof(KeyT);
-    uint32_t cur = 0u;
+    uint32_t cur = 0u, top = 0u;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int v = tid + j * kSplitThreads;
@@ -214,10 +215,14 @@ __device__ __forceinline__ void warm_maxima16(const uint4* v0, int tid, int cvec
         }
         if (((j + 1) & ((1 << gsh) - 1)) == 0) {
             const int g = j >> gsh;
-            if (g < R) out[g] = static_cast<KeyT>(cur);
+            if (g < R) {
+                out[g] = static_cast<KeyT>(cur);
+                top = max(top, cur);
+            }
             cur = 0u;
         }
     }
+    return top;
 }
 
 // The pivot of a final-select pass, found by every warp on its own (no barrier).  The
@@ -299,15 +304,17 @@ __device__ __forceinline__ XPivot warp_pivot_x(const uint32_t* rows, int G, int 
     return r;
 }
 
-// Calls f(key) for each of keys[0, n), the CTA's threads taking one 16-byte vector each
-// at a time (n a multiple of the keys per vector, `keys` 16-byte aligned): the loads of a
-// thread's keys do not wait on one another.
+// Calls f(key) for each key of G rows of wm keys, each row followed by one 16-byte vector
+// that is skipped (wm / keys-per-vector a power of two, `keys` 16-byte aligned), the CTA's
+// threads taking one 16-byte vector each at a time: the loads of a thread's keys do not
+// wait on one another.
 template <typename KeyT, typename F>
-__device__ __forceinline__ void each_key(const KeyT* keys, int n, int tid, F&& f) {
+__device__ __forceinline__ void each_key(const KeyT* keys, int G, int wm, int tid, F&& f) {
     constexpr int KPV = 16 / static_cast<int>(sizeof(KeyT));
+    const int W = wm / KPV, wl = 31 - __clz(W);  // vectors per row
     const uint4* v4 = reinterpret_cast<const uint4*>(keys);
-    for (int j = tid; j < n / KPV; j += kSplitThreads) {
-        const uint4 v = v4[j];
+    for (int j = tid; j < G * W; j += kSplitThreads) {
+        const uint4 v = v4[(j >> wl) * (W + 1) + (j & (W - 1))];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -787,7 +794,7 @@ __device__ __forceinline__ uint32_t split_output(const KeyT* ckey, const uint32_
 }
 
 // HELD: every CTA's chunks fit its ring at once (no refills, no streamed-row threshold
-// raises or refined warm-up, a sample of at most 8 vectors per thread); MCT: rows span
+// raises or refined warm-up, a sample of at most 4 vectors per thread); MCT: rows span
 // several clusters.  The launch picks the instance for its plan, so each call runs only
 // its own class's code.
 template <typename KeyT, bool HELD, bool MCT>
@@ -986,76 +993,117 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // and splits them into R groups; a group's maximum is taken on the packed values
             // (NaNs ignored) and keyed once
             const int R = wm / 256;
+            const int WS = wm + 16 / ES;  // row stride of the union in wx: the maxima, then a slot
             const int VT = (ww * cvec + NC - 1) / NC;  // at most 16
             // log2 of vectors per group
             const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
+            uint32_t lm = 0u;  // the largest of this thread's group maxima
             if (HELD || VT <= 8) {
                 uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
-                if (VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+                if (HELD || VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
                 else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
 #pragma unroll
-                for (int r = 0; r < 4; ++r)
-                    if (r < R) wx[crank * wm + tid * R + r] = static_cast<KeyT>(gk[r]);
+                for (int r = 0; r < 4; ++r) {
+                    if (r < R) {
+                        wx[crank * WS + tid * R + r] = static_cast<KeyT>(gk[r]);
+                        lm = max(lm, gk[r]);
+                    }
+                }
             } else {
-                warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * wm + tid * R);
+                lm = warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * WS + tid * R);
+            }
+            if (!HELD) {  // (streamed rows bin the union below its largest maximum)
+                lm = __reduce_max_sync(0xFFFFFFFFu, lm);
+                if (lane == 0) atomicMax(&ctrl->lmax, lm);
             }
             fence_proxy_async_smem();
             named_bar_sync(1, NC);
             if (G > 1) {
                 asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-                if (tid == 0) {
-                    const uint32_t bytes = static_cast<uint32_t>(wm) * ES;
+                if (tid == 0) {  // the row (and its largest, in the slot after it) to every peer
+                    if (!HELD) {
+                        *reinterpret_cast<uint32_t*>(wx + crank * WS + wm) = ctrl->lmax;
+                        fence_proxy_async_smem();
+                    }
+                    const uint32_t bytes = static_cast<uint32_t>(HELD ? wm : WS) * ES;
                     mbar_arrive_expect_tx(&ctrl->wbar, bytes * static_cast<uint32_t>(G - 1));
                     for (int r = 0; r < G; ++r)
                         if (r != static_cast<int>(crank))
-                            bulk_s2s_cluster(map_rank(wx + crank * wm, r), wx + crank * wm, bytes,
+                            bulk_s2s_cluster(map_rank(wx + crank * WS, r), wx + crank * WS, bytes,
                                              map_rank(&ctrl->wbar, r));
                 }
                 wait_bounded_cluster(&ctrl->wbar, 0, ctrl);
             }
-            // histogram of the union's maxima by their top 11 key bits, and the bucket of
-            // the k-th largest
-            each_key<KeyT>(wx, G * wm, tid, [&](uint32_t kk) {
-                if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
-            });
-            __syncthreads();
-            // the bucket of the k-th largest maximum
-            cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
-            const int bstar = ctrl->bstar;
-            const uint32_t above = ctrl->above, total = ctrl->bcount;
-            // The edge: the smallest key of the pivot bucket, or (refine) of the 32nd part of
-            // it that holds the k-th largest maximum (every CTA holds the whole union, so
-            // this needs no exchange).  At least k maxima, each an element of the row, lie
-            // at or above it.
+            // The edge: the smallest key of the bin of a histogram of the union's maxima that
+            // holds the k-th largest.  At least k maxima, each an element of the row, lie at or
+            // above it.  Streamed rows bin the maxima in kBins bins of 2^FS keys below M, the
+            // union's largest maximum (one key each for bf16, 1/1024 of an octave for fp32);
+            // rows held whole, and rows with fewer than k maxima in that range, by the top
+            // kDigitBits key bits, streamed rows then narrowing the bucket to its 32nd part
+            // that holds the k-th largest (refine).  (On rows held whole the narrower edge
+            // saves fewer appends than finding it costs.)
             uint32_t edge = 0u;
-            if (HELD || !p.refine) {
-                if (total >= static_cast<uint32_t>(p.k) && bstar > 0) {
-                    edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
-                    if (tid == 0) ctrl->wedge = edge;
-                }
-            } else if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
-                constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
-                uint32_t* sub = ctrl->block_cnt[0];     // zero since start-up
-                each_key<KeyT>(wx, G * wm, tid, [&](uint32_t kk) {
-                    if (kk && (kk >> (KW - kDigitBits)) == static_cast<uint32_t>(bstar))
-                        atomicAdd(&sub[(kk >> SB) & 31u], 1u);
+            bool coarse = HELD;
+            if (!HELD) {
+                uint32_t M = ctrl->lmax;
+                for (int r = 0; r < G; ++r)
+                    if (r != static_cast<int>(crank)) M = max(M, *reinterpret_cast<const uint32_t*>(wx + r * WS + wm));
+                constexpr int FS = ES == 2 ? 0 : 13;
+                each_key<KeyT>(wx, G, wm, tid, [&](uint32_t kk) {
+                    const uint32_t d = (M - kk) >> FS;
+                    if (kk && d < static_cast<uint32_t>(kBins)) atomicAdd(&hist[kBins - 1 - d], 1u);
                 });
                 __syncthreads();
-                if (warp == 0) {
-                    uint32_t sfx = sub[lane];  // maxima in parts >= lane of the bucket
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, sfx, d);
-                        if (lane + d < 32) sfx += t;
-                    }
-                    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, above + sfx >= static_cast<uint32_t>(p.k));
-                    const uint32_t l = hit ? 31u - __clz(hit) : 0u;
-                    if (lane == 0)
-                        ctrl->wedge = (static_cast<uint32_t>(bstar) << (KW - kDigitBits)) | (l << SB);
+                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
+                if (ctrl->bcount >= static_cast<uint32_t>(p.k) && ctrl->bstar >= 0) {
+                    const int64_t lo =
+                        static_cast<int64_t>(M) - (static_cast<int64_t>(kBins - ctrl->bstar) << FS) + 1;
+                    edge = lo > 0 ? static_cast<uint32_t>(lo) : 0u;
+                    if (tid == 0) ctrl->wedge = edge;
+                } else {
+                    coarse = true;
+                    __syncthreads();  // (every thread has read the bin above)
+                    for (int b = tid; b < kBins; b += NC) hist[b] = 0u;
+                    __syncthreads();
                 }
+            }
+            if (coarse) {
+                each_key<KeyT>(wx, G, wm, tid, [&](uint32_t kk) {
+                    if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
+                });
                 __syncthreads();
-                edge = ctrl->wedge;
+                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
+                const int bstar = ctrl->bstar;
+                const uint32_t above = ctrl->above, total = ctrl->bcount;
+                if (HELD || !p.refine) {
+                    if (total >= static_cast<uint32_t>(p.k) && bstar > 0) {
+                        edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
+                        if (tid == 0) ctrl->wedge = edge;
+                    }
+                } else if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
+                    constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
+                    uint32_t* sub = ctrl->block_cnt[0];     // zero since start-up
+                    each_key<KeyT>(wx, G, wm, tid, [&](uint32_t kk) {
+                        if (kk && (kk >> (KW - kDigitBits)) == static_cast<uint32_t>(bstar))
+                            atomicAdd(&sub[(kk >> SB) & 31u], 1u);
+                    });
+                    __syncthreads();
+                    if (warp == 0) {
+                        uint32_t sfx = sub[lane];  // maxima in parts >= lane of the bucket
+#pragma unroll
+                        for (int d = 1; d < 32; d <<= 1) {
+                            const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, sfx, d);
+                            if (lane + d < 32) sfx += t;
+                        }
+                        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, above + sfx >= static_cast<uint32_t>(p.k));
+                        const uint32_t l = hit ? 31u - __clz(hit) : 0u;
+                        if (lane == 0)
+                            ctrl->wedge = (static_cast<uint32_t>(bstar) << (KW - kDigitBits)) | (l << SB);
+                    }
+                    __syncthreads();
+                    edge = ctrl->wedge;
+                }
             }
             if (edge > 0u) {
                 hasT = true;

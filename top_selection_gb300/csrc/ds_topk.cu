@@ -1130,7 +1130,10 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
             ok = fit(c, kNCW, static_cast<size_t>(di.smem_optin));
         if (!ok && first * P.es < 1024) ok = fit(first, kNCW, static_cast<size_t>(di.smem_optin));
         if (!ok) return DS_ERR_UNSUPPORTED;
-        P.held = (P.m + parts - 1) / parts * ((static_cast<int64_t>(B) + P.chunk - 1) / P.chunk) <= P.stages;
+        // (held rows also keep chunks of at most 8 KB: their warm-up samples at most two
+        // chunks, so a thread's sample is at most 4 vectors)
+        P.held = (P.m + parts - 1) / parts * ((static_cast<int64_t>(B) + P.chunk - 1) / P.chunk) <= P.stages &&
+                 P.chunk * P.es <= 8192;
     } else {
         const auto layout_bytes = [&](int s) -> size_t {
             return scan_layout(P.es, P.chunk, s, P.cap, P.perm_cap).total;
