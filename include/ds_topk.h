@@ -97,8 +97,10 @@ typedef enum {
  *   stream      CUDA stream (0 = legacy default stream).
  * The library chooses how many CTAs share a row: rows split over a cluster, or rows
  * that already fill the GPU one per CTA, run the split-row kernel (warm-up threshold
- * from a sample of the row, compaction when a chunk's survivors do not fit); only
- * ds_topk_ex with parts = 1 runs the pages' one-CTA schedule exactly.  When a row is
+ * from a sample of the row, compaction when a chunk's survivors do not fit; rows held
+ * whole in one cluster start from a speculative threshold, checked and redone when it
+ * was too high -- ds_plan.spec_k); only ds_topk_ex with parts = 1 runs the pages'
+ * one-CTA schedule exactly.  Results are exact on every path.  When a row is
  * split over more than one thread-block cluster it uses a library-owned workspace, one
  * per (device, stream) -- per thread as well for cudaStreamPerThread -- so calls on
  * different streams may run concurrently.  It is grown with cudaMalloc (and cleared with
@@ -156,6 +158,12 @@ typedef struct {
     int32_t merge_launch;   /* 1 when a second (merge) kernel runs                      */
     int32_t B;              /* block size in effect (the library's choice when 0 was passed) */
     int32_t B2;             /* compaction slack in effect (likewise)                   */
+    int32_t spec_k;         /* rows held whole in one cluster: the first attempt filters
+                               from an estimate of the spec_k-th largest sampled group
+                               maximum, a threshold nothing proves; the final select
+                               checks that k keys reach it and otherwise filters the
+                               row's chunks, still in shared memory, from the proven
+                               threshold (0 = no speculation)                          */
 } ds_plan;
 
 /* Errors as ds_topk's host checks (DS_ERR_INVALID_ARG, DS_ERR_UNSUPPORTED), and

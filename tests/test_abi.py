@@ -230,6 +230,52 @@ def test_library_chooses_block_sizes_on_a_described_device(lib):
     assert got["given_B2"] == [8192, 1024]
 
 
+_SPEC_SCRIPT = r"""
+import json, top_selection_gb300 as ds
+ds.load()
+out = {
+    "indexer": ds.ds_get_plan(0, 64, 131072, 512, 4096, 4096),
+    "indexer_k64": ds.ds_get_plan(0, 64, 131072, 64, 4096, 4096),
+    "indexer_k2048": ds.ds_get_plan(0, 64, 131072, 2048, 4096, 4096),
+    "longctx": ds.ds_get_plan(0, 4, 1048576, 512, 4096, 4096),
+    "row65536": ds.ds_get_plan(1, 1, 65536, 512, 1024, 1024),
+    "sampler": ds.ds_get_plan(1, 256, 129280, 512, 8192, 4096),
+    "one_cta": ds.ds_get_plan(0, 64, 131072, 512, 4096, 4096, parts=1),
+    "spread": ds.ds_get_plan(1, 1, 1 << 26, 512, 8192, 4096),
+}
+print(json.dumps(out))
+"""
+
+
+def test_speculative_rank_on_a_described_device(lib):
+    """Rows held whole in one cluster speculate with spec_k = ceil(2 k S / N), S = the
+    cluster's sampled elements (CTAs x two chunks x chunk), when 64 <= spec_k < k; rows
+    streamed through the ring, rows over several clusters and the one-CTA schedule never
+    do."""
+    import json
+    import sys
+    env = dict(os.environ, DS_PLAN_DEVICE="152,232448,233472", CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", _SPEC_SCRIPT], env=env, cwd=ROOT, capture_output=True,
+                         text=True, check=True).stdout
+    got = json.loads(out.strip().splitlines()[-1])
+
+    def expect(p, k, N):
+        blocks = -(-(-(-N // p["B"])) // p["parts"])
+        assert blocks * -(-p["B"] // p["chunk_elems"]) <= p["stages"]  # every chunk in the ring
+        S = p["cluster"] * 2 * p["chunk_elems"]
+        sk = -(-2 * k * S // N)
+        return sk if 64 <= sk < k else 0
+
+    assert got["indexer"]["spec_k"] == expect(got["indexer"], 512, 131072) == 256
+    assert got["indexer_k64"]["spec_k"] == 0              # 32 < 64: too noisy
+    assert got["indexer_k2048"]["spec_k"] == expect(got["indexer_k2048"], 2048, 131072) == 512
+    assert got["row65536"]["spec_k"] == expect(got["row65536"], 512, 65536) == 256
+    assert got["longctx"]["stages"] < 16 and got["longctx"]["spec_k"] == 0  # 16 chunks per CTA: streamed
+    assert got["sampler"]["spec_k"] == 0                   # streamed through the ring
+    assert got["one_cta"]["spec_k"] == 0                   # the pages' one-CTA schedule
+    assert got["spread"]["merge_launch"] == 1 and got["spread"]["spec_k"] == 0  # several clusters
+
+
 def test_topk_sample_host_validation(lib):
     import top_selection_gb300 as ds
     a = [P, 1, 2, 1000, 1024, 8, 64, 64, 1]

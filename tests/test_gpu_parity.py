@@ -215,9 +215,12 @@ def _spikes_in_sampled_blocks(w, k, seed):
     """w's rows with spikes U(8, 12) in the first block each part of the planned split
     visits (that block is always in the warm-up's sample), k - 32 of them per row in all:
     the sample holds nearly all of the row's largest values, fewer than k, and its group
-    maxima overstate how many large values the rest of the row holds."""
+    maxima overstate how many large values the rest of the row holds.  On rows held whole
+    the speculative edge then lands among the spikes, fewer than k keys reach it, and the
+    kernel must filter the row again from the proven edge."""
     import top_selection_gb300 as ds
     plan = ds.ds_get_plan(w.dtype, w.rows, w.N, k, w.B, w.B2)
+    assert plan["spec_k"] > 0, plan
     parts = plan["parts"]
     m = -(-w.N // w.B)
     mq, mr = divmod(m, parts)

@@ -57,7 +57,7 @@ class ds_plan(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("capacity", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("ctas_per_sm", ctypes.c_int32), ("merge_launch", ctypes.c_int32),
-                ("B", ctypes.c_int32), ("B2", ctypes.c_int32)]
+                ("B", ctypes.c_int32), ("B2", ctypes.c_int32), ("spec_k", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -35,7 +35,8 @@ struct Ctrl {
     int observed[kMaxStages];    // copies seen complete per stage
     int cnt;                     // append cursor of the candidate buffer
     uint32_t maxkey;             // largest key appended (reduced from the threads at each select)
-    uint32_t sharedT;            // split rows: the cluster's threshold key (each CTA's copy), 0 = none
+    uint32_t sharedT[2];         // split rows: the cluster's threshold key (each CTA's copy), 0 = none;
+                                 //   one word per attempt of a row held whole (see wedge_p)
     int abort;                   // a bounded wait ran out: skip the remaining waits
     int bstar;                   // pivot search results
     uint32_t above;
@@ -48,7 +49,12 @@ struct Ctrl {
     int fail_base;               // split rows: first slot of a reservation that did not fit
     uint64_t wbar;               // split rows: warm-up exchange of group maxima
     uint64_t xbar[2];            // split rows: final-select histogram exchange, by pass parity
-    uint32_t wedge;              // split rows: smallest key of the warm-up's pivot bucket
+    uint32_t wedge;              // split rows: the edge the final select starts from (the warm-up's;
+                                 //   speculative while the first attempt runs on one)
+    uint32_t wedge_p;            // split rows held whole: the proven edge (k keys of the row at or above)
+    int spec_b;                  // split rows held whole: the warm-up bucket of the speculative rank,
+    uint32_t spec_above;         //   the maxima above it and in it
+    uint32_t spec_c;
     int fin_n;                   // consumer state handed to the whole CTA after the scan
     int fin_hasT;
     uint32_t fin_T;

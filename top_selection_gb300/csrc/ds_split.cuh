@@ -333,8 +333,11 @@ __device__ __forceinline__ void each_key(const KeyT* keys, int G, int wm, int ti
 // scan in each warp, then the warps' totals through `wt`) pick the thread whose buckets
 // hold it, and that thread walks its eight.  Sets ctrl->bstar (-1 when all buckets
 // together hold fewer than kk), ctrl->above (the count in buckets above it; all of them
-// when none) and ctrl->bcount (the total).  Every thread calls it; it ends with a barrier.
-__device__ __forceinline__ void cta_bucket_2048(const uint32_t* hist, uint32_t kk, int tid, uint32_t* wt, Ctrl* ctrl) {
+// when none) and ctrl->bcount (the total); for a second rank k2 > 0, ctrl->spec_b,
+// spec_above and spec_c (the bucket's own count) the same way.  Every thread calls it; it
+// ends with a barrier.
+__device__ __forceinline__ void cta_bucket_2048(const uint32_t* hist, uint32_t kk, uint32_t k2, int tid, uint32_t* wt,
+                                                Ctrl* ctrl) {
     static_assert(kBins == 8 * kSplitThreads, "eight buckets per thread");
     const int lane = tid & 31, warp = tid >> 5;
     const uint4 a = reinterpret_cast<const uint4*>(hist)[2 * tid];
@@ -357,29 +360,45 @@ __device__ __forceinline__ void cta_bucket_2048(const uint32_t* hist, uint32_t k
         up += w > warp ? x : 0u;
     }
     const uint32_t incl = sf + up;  // buckets of threads >= tid
-    if (incl >= kk && incl - t < kk) {
+    // the bucket of rank r when this thread holds it: index, count above, own count
+    const auto locate = [&](uint32_t r, int& bs, uint32_t& ab, uint32_t& cnt) -> bool {
+        if (!(incl >= r && incl - t < r)) return false;
         uint32_t acc = incl - t;
-        int bs = 8 * tid;
+        bs = 8 * tid;
+        cnt = 0u;
         bool found = false;
 #pragma unroll
         for (int j = 7; j >= 0; --j) {
             if (!found) {
-                if (acc + c[j] >= kk) {
+                if (acc + c[j] >= r) {
                     found = true;
                     bs = 8 * tid + j;
+                    cnt = c[j];
                 } else {
                     acc += c[j];
                 }
             }
         }
+        ab = acc;
+        return true;
+    };
+    int bs;
+    uint32_t ab, cnt;
+    if (locate(kk, bs, ab, cnt)) {
         ctrl->bstar = bs;
-        ctrl->above = acc;
+        ctrl->above = ab;
+    }
+    if (k2 && locate(k2, bs, ab, cnt)) {
+        ctrl->spec_b = bs;
+        ctrl->spec_above = ab;
+        ctrl->spec_c = cnt;
     }
     if (tid == 0) {
         if (tot < kk) {
             ctrl->bstar = -1;
             ctrl->above = tot;
         }
+        if (k2 && tot < k2) ctrl->spec_b = -1;
         ctrl->bcount = tot;
     }
     __syncthreads();
@@ -609,8 +628,8 @@ template <typename KeyT>
 __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, uint32_t* hist, Ctrl* ctrl, int cap,
                                                   int room, int k, uint32_t tmax, int tid, bool hasT, uint32_t T,
                                                   uint32_t* xh0,
-                                                  uint32_t hedge, int hs0, int G, unsigned long long* gT,
-                                                  uint32_t epoch) {
+                                                  uint32_t hedge, int hs0, int G, uint32_t* shT,
+                                                  unsigned long long* gT, uint32_t epoch) {
     constexpr int NC = kSplitThreads;
     const int lane = tid & 31;
     named_bar_sync(2, NC);
@@ -707,7 +726,7 @@ __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, ui
         for (int i = tid; i < k; i += NC) xhist_add(xh0, static_cast<uint32_t>(ckey[i]), hedge, hs0);
     }
     if (tid == 0) {
-        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), nt);
+        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(shT, r), nt);
         if (gT) atomicMax(gT, (static_cast<unsigned long long>(epoch) << 32) | nt);
         ctrl->last_kept = ctrl->cnt;
     }
@@ -843,6 +862,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     const int nq = mp * cpb;
     constexpr bool MC = MCT;
     const uint32_t cap = static_cast<uint32_t>(p.cap);
+    // Rows held whole in one cluster may start from a speculative edge (spec_k > 0): every
+    // chunk stays in its CTA's ring, so a second attempt can filter them all again.
+    const bool spec_ok = HELD && !MC && p.spec_k > 0;
 
     // The next kernel on the stream may start as this one's CTAs leave.  This kernel may
     // have started before the previous one completed: it waits for it before reading x
@@ -886,7 +908,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         chunk_of(bi, sub, c0, ce);
     };
     const auto publish_T = [&](uint32_t t) {
-        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT, r), t);
+        for (int r = 0; r < G; ++r) red_cluster_max_u32(map_rank(&ctrl->sharedT[0], r), t);
         if (MC) atomicMax(p.gT + row, (static_cast<unsigned long long>(p.epoch) << 32) | t);
     };
 
@@ -922,6 +944,15 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     // cluster's CTAs meet while the first copies are in flight.
     if (G > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
+    // the final select's outcome (set by the last attempt)
+    int n = 0;
+    uint32_t edge = 0u, pivot = 0u;
+    uint32_t gt_all = 0u, gt_lower = 0u;   // keys above the pivot: all CTAs, CTAs of lower rank
+    uint32_t eq_lower = 0u, eq_mine = 0u;  // pivot-equal keys: CTAs of lower rank, this CTA
+    bool take_all = false;
+    // two rounds of G histograms of kXBins uint16 counts, as pairs in 32-bit words
+    constexpr int XW = kXBins / 2;
+    uint32_t* const xr = reinterpret_cast<uint32_t*>(smem + L.xf);
     {
         bool hasT = false;
         uint32_t T = 0u;
@@ -930,14 +961,16 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         // The final select's first histogram (this CTA's slot of its first exchange round)
         // is counted as keys are appended: keys from the warm-up's edge up, in bins of
         // 2^hs0 keys (set once the edge is known).
-        uint32_t* const xh0 = reinterpret_cast<uint32_t*>(smem + L.xf) + static_cast<size_t>(crank) * (kXBins / 2);
+        int att = 0;  // attempt: 1 after a speculative edge failed (rows held whole only)
+        // attempt a counts its first histogram into this CTA's slot of round a
+        const auto xh0 = [&]() { return xr + (static_cast<size_t>(att) * G + crank) * XW; };
         uint32_t hedge = 0u;
         int hs0 = KW - kXBits;
         // every consumer warp calls this together (from its chunk loop or the drain); the
         // work is out of line, away from the chunk loop's code
         const auto join_compaction = [&]() {
-            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.chunk, p.k, tmax, tid, hasT, T, xh0, hedge,
-                                       hs0, G, MC ? p.gT + row : nullptr, p.epoch);
+            T = split_compaction<KeyT>(ckey, cidx, hist, ctrl, p.cap, p.chunk, p.k, tmax, tid, hasT, T, xh0(), hedge,
+                                       hs0, G, ctrl->sharedT + att, MC ? p.gT + row : nullptr, p.epoch);
             hasT = true;
         };
         // A warp waiting for its next chunk joins any compaction requested meanwhile, so
@@ -1043,7 +1076,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // kDigitBits key bits, streamed rows then narrowing the bucket to its 32nd part
             // that holds the k-th largest (refine).  (On rows held whole the narrower edge
             // saves fewer appends than finding it costs.)
-            uint32_t edge = 0u;
+            uint32_t wedge0 = 0u;
             bool coarse = HELD;
             if (!HELD) {
                 uint32_t M = ctrl->lmax;
@@ -1055,12 +1088,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     if (kk && d < static_cast<uint32_t>(kBins)) atomicAdd(&hist[kBins - 1 - d], 1u);
                 });
                 __syncthreads();
-                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
+                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), 0u, tid, ctrl->warp_tot[0], ctrl);
                 if (ctrl->bcount >= static_cast<uint32_t>(p.k) && ctrl->bstar >= 0) {
                     const int64_t lo =
                         static_cast<int64_t>(M) - (static_cast<int64_t>(kBins - ctrl->bstar) << FS) + 1;
-                    edge = lo > 0 ? static_cast<uint32_t>(lo) : 0u;
-                    if (tid == 0) ctrl->wedge = edge;
+                    wedge0 = lo > 0 ? static_cast<uint32_t>(lo) : 0u;
+                    if (tid == 0) ctrl->wedge = wedge0;
                 } else {
                     coarse = true;
                     __syncthreads();  // (every thread has read the bin above)
@@ -1073,13 +1106,14 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     if (kk) atomicAdd(&hist[(kk << (32 - KW)) >> (32 - kDigitBits)], 1u);
                 });
                 __syncthreads();
-                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), tid, ctrl->warp_tot[0], ctrl);
+                cta_bucket_2048(hist, static_cast<uint32_t>(p.k), spec_ok ? static_cast<uint32_t>(p.spec_k) : 0u, tid,
+                                ctrl->warp_tot[0], ctrl);
                 const int bstar = ctrl->bstar;
                 const uint32_t above = ctrl->above, total = ctrl->bcount;
                 if (HELD || !p.refine) {
                     if (total >= static_cast<uint32_t>(p.k) && bstar > 0) {
-                        edge = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
-                        if (tid == 0) ctrl->wedge = edge;
+                        wedge0 = static_cast<uint32_t>(bstar) << (KW - kDigitBits);
+                        if (!HELD && tid == 0) ctrl->wedge = wedge0;
                     }
                 } else if (total >= static_cast<uint32_t>(p.k) && bstar >= 0) {
                     constexpr int SB = KW - kDigitBits - 5;  // shift of the 5 bits below the bucket's
@@ -1102,13 +1136,34 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                             ctrl->wedge = (static_cast<uint32_t>(bstar) << (KW - kDigitBits)) | (l << SB);
                     }
                     __syncthreads();
-                    edge = ctrl->wedge;
+                    wedge0 = ctrl->wedge;
                 }
             }
-            if (edge > 0u) {
+            // Rows held whole may start from a speculative edge: the spec_k-th largest
+            // maximum (spec_k about twice the sample's expected share of the row's k largest),
+            // placed in its bucket as if the bucket's maxima were spread evenly over its keys.
+            // Nothing proves that k keys of the row reach it; the final select's first pass
+            // counts every key at or above it over the cluster and, when there are fewer than
+            // k, the chunks (all still in the ring) are filtered again from the proven edge.
+            uint32_t sedge = wedge0;
+            if (HELD) {
+                if (spec_ok && wedge0 > 0u && ctrl->spec_b >= 0) {
+                    constexpr uint64_t BW = uint64_t(1) << (KW - kDigitBits);  // keys per bucket
+                    const uint64_t bc = ctrl->spec_c;
+                    const uint64_t r = static_cast<uint64_t>(p.spec_k) - ctrl->spec_above;  // 1 <= r <= bc
+                    const uint64_t top = (static_cast<uint64_t>(ctrl->spec_b) + 1u) * BW;      // one past the bucket
+                    const uint64_t down = (r * BW + bc - 1u) / bc;                            // 1 <= down <= BW
+                    sedge = max(wedge0, static_cast<uint32_t>(top - down));
+                }
+                if (tid == 0) {
+                    ctrl->wedge = sedge;
+                    ctrl->wedge_p = wedge0;
+                }
+            }
+            if (sedge > 0u) {
                 hasT = true;
-                T = edge - 1u;
-                hedge = edge;
+                T = sedge - 1u;
+                hedge = sedge;
                 hs0 = ES == 2 ? 0 : 23 - kXBits;
             }
             // (every CTA of the cluster derived this same threshold: only the row's other
@@ -1116,234 +1171,260 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             if (tid == 0 && hasT && MC) publish_T(T);
         }
 
-        // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
-        // this warp's chunk q: ring stage s = q % stages and use q / stages, block index bi
-        // and sub-chunk sub, stepped by kNCW chunks per round
-        int st = warp, use = 0, bi, sub, d8, r8, dS, rS;
-        qdiv(warp, bi, sub);
-        qdiv(kNCW, d8, r8);      // kNCW chunks ahead
-        qdiv(p.stages, dS, rS);  // one ring ahead
-        for (int q = warp; q < nq; q += kNCW) {
-            int req = 0;
-            if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
-            if (__shfl_sync(0xFFFFFFFFu, req, 0)) join_compaction();
-            // the threshold: this CTA's, the cluster's and the other clusters'
-            uint32_t tk = T;
-            bool have = hasT;
-            {
-                uint32_t sh = gnext;
-                if ((G > 1 || (!HELD && p.rstep)) && lane == 0)
-                    sh = max(sh, *reinterpret_cast<volatile uint32_t*>(&ctrl->sharedT));
-                sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
-                if (sh != 0u && (!have || sh > tk)) {
-                    tk = sh;
-                    have = true;
-                }
-                if (MC && lane == 0) {
-                    const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
-                    gnext = static_cast<uint32_t>(g >> 32) == p.epoch ? static_cast<uint32_t>(g) : 0u;
-                }
-            }
-            int64_t c0, ce;
-            chunk_of(bi, sub, c0, ce);
-            const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
-            const int s = st;
-            const bool got = wait_data(&ctrl->full[s], use & 1);
-            if (lane == 0 && got) ctrl->observed[s] = use + 1;
-            if (hasT && (!have || T > tk)) {  // a compaction ran while the warp waited
-                tk = T;
-                have = true;
-            }
-            if (got && ce > 0) {
-                const int nvec = static_cast<int>(bytes / 16);
-                const int tail = static_cast<int>(ce - bytes / ES);
-                int pass = 0;
-                while (!warp_chunk<KeyT>(ring + static_cast<size_t>(s) * chunk_bytes, nvec, static_cast<uint32_t>(c0),
-                                         xrow, c0 + bytes / ES, tail, compare_bits<KeyT>(have, tk), ckey, cidx, ctrl,
-                                         cap, lane, pass, tmax, xh0, hedge, hs0)) {
-                    join_compaction();
-                    if (!have || T > tk) {
-                        tk = T;
+        // The chunks, the drain and the final select, once, or twice when a speculative edge
+        // failed (rows held whole only).
+        for (;; ++att) {
+            // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
+            // this warp's chunk q: ring stage s = q % stages and use q / stages, block index bi
+            // and sub-chunk sub, stepped by kNCW chunks per round
+            int st = warp, use = 0, bi, sub, d8, r8, dS, rS;
+            qdiv(warp, bi, sub);
+            qdiv(kNCW, d8, r8);      // kNCW chunks ahead
+            qdiv(p.stages, dS, rS);  // one ring ahead
+            for (int q = warp; q < nq; q += kNCW) {
+                int req = 0;
+                if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                if (__shfl_sync(0xFFFFFFFFu, req, 0)) join_compaction();
+                // the threshold: this CTA's, the cluster's and the other clusters'
+                uint32_t tk = T;
+                bool have = hasT;
+                {
+                    uint32_t sh = gnext;
+                    if ((G > 1 || (!HELD && p.rstep)) && lane == 0)
+                        sh = max(sh, *reinterpret_cast<volatile uint32_t*>(ctrl->sharedT + att));
+                    sh = __shfl_sync(0xFFFFFFFFu, sh, 0);
+                    if (sh != 0u && (!have || sh > tk)) {
+                        tk = sh;
                         have = true;
                     }
-                    int ab = 0;
-                    if (lane == 0) ab = *reinterpret_cast<volatile int*>(&ctrl->abort);
-                    if (__shfl_sync(0xFFFFFFFFu, ab, 0)) break;
+                    if (MC && lane == 0) {
+                        const unsigned long long g = ld_relaxed_gpu_u64(p.gT + row);
+                        gnext = static_cast<uint32_t>(g >> 32) == p.epoch ? static_cast<uint32_t>(g) : 0u;
+                    }
+                }
+                int64_t c0, ce;
+                chunk_of(bi, sub, c0, ce);
+                const uint32_t bytes = static_cast<uint32_t>(ce * ES) & ~15u;
+                const int s = st;
+                const bool got = wait_data(&ctrl->full[s], use & 1);
+                if (lane == 0 && got) ctrl->observed[s] = use + 1;
+                if (hasT && (!have || T > tk)) {  // a compaction ran while the warp waited
+                    tk = T;
+                    have = true;
+                }
+                if (got && ce > 0) {
+                    const int nvec = static_cast<int>(bytes / 16);
+                    const int tail = static_cast<int>(ce - bytes / ES);
+                    int pass = 0;
+                    while (!warp_chunk<KeyT>(ring + static_cast<size_t>(s) * chunk_bytes, nvec,
+                                             static_cast<uint32_t>(c0), xrow, c0 + bytes / ES, tail,
+                                             compare_bits<KeyT>(have, tk), ckey, cidx, ctrl, cap, lane, pass, tmax,
+                                             xh0(), hedge, hs0)) {
+                        join_compaction();
+                        if (!have || T > tk) {
+                            tk = T;
+                            have = true;
+                        }
+                        int ab = 0;
+                        if (lane == 0) ab = *reinterpret_cast<volatile int*>(&ctrl->abort);
+                        if (__shfl_sync(0xFFFFFFFFu, ab, 0)) break;
+                    }
+                }
+                __syncwarp();  // every lane is done with the stage: refill it with this warp's next chunk there
+                if (!HELD && lane == 0 && got && q + p.stages < nq &&
+                    !*reinterpret_cast<volatile int*>(&ctrl->abort)) {
+                    int bj = bi + dS, sj = sub + rS;
+                    if (sj >= cpb) {
+                        sj -= cpb;
+                        ++bj;
+                    }
+                    issue_to(s, use + 1, bj, sj);
+                }
+                if (!HELD && p.rstep) {  // one warp raises the threshold each time the buffer passes the mark
+                    int due = 0;
+                    if (lane == 0) {
+                        const uint32_t c = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&ctrl->cnt));
+                        const uint32_t mk = *reinterpret_cast<volatile uint32_t*>(&ctrl->raise_mark);
+                        if (c >= (mk ? mk : static_cast<uint32_t>(p.rmark)))
+                            due = atomicCAS(&ctrl->raise_mark, mk, c + static_cast<uint32_t>(p.rstep)) == mk;
+                    }
+                    if (__shfl_sync(0xFFFFFFFFu, due, 0)) {
+                        const uint32_t t = split_raise<KeyT>(xh0(), p.k, hedge, hs0, lane);
+                        if (lane == 0 && t != 0u) {
+                            if (G > 1 || MC) publish_T(t);
+                            else atomicMax(&ctrl->sharedT[0], t);
+                        }
+                    }
+                }
+                bi += d8;
+                sub += r8;
+                if (sub >= cpb) {
+                    sub -= cpb;
+                    ++bi;
+                }
+                st += kNCW;
+                if (st >= p.stages) {
+                    st -= p.stages;
+                    ++use;
                 }
             }
-            __syncwarp();  // every lane is done with the stage: refill it with this warp's next chunk there
-            if (!HELD && lane == 0 && got && q + p.stages < nq &&
-                !*reinterpret_cast<volatile int*>(&ctrl->abort)) {
-                int bj = bi + dS, sj = sub + rS;
-                if (sj >= cpb) {
-                    sj -= cpb;
-                    ++bj;
-                }
-                issue_to(s, use + 1, bj, sj);
-            }
-            if (!HELD && p.rstep) {  // one warp raises the threshold each time the buffer passes the mark
-                int due = 0;
-                if (lane == 0) {
-                    const uint32_t c = static_cast<uint32_t>(*reinterpret_cast<volatile int*>(&ctrl->cnt));
-                    const uint32_t mk = *reinterpret_cast<volatile uint32_t*>(&ctrl->raise_mark);
-                    if (c >= (mk ? mk : static_cast<uint32_t>(p.rmark)))
-                        due = atomicCAS(&ctrl->raise_mark, mk, c + static_cast<uint32_t>(p.rstep)) == mk;
-                }
-                if (__shfl_sync(0xFFFFFFFFu, due, 0)) {
-                    const uint32_t t = split_raise<KeyT>(xh0, p.k, hedge, hs0, lane);
-                    if (lane == 0 && t != 0u) {
-                        if (G > 1 || MC) publish_T(t);
-                        else atomicMax(&ctrl->sharedT, t);
+            // A warp out of chunks still joins compactions other warps request: it reads the
+            // count of finished warps before the request flag, so a request raised by the
+            // last warp before it finished is always seen.
+            __threadfence_block();
+            if (lane == 0) atomicAdd(&ctrl->done_warps, 1);
+            {
+                const long long t0 = clock64();
+                while (true) {
+                    int d = 0, f = 0;
+                    if (lane == 0) {
+                        d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
+                        __threadfence_block();
+                        f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+                    }
+                    d = __shfl_sync(0xFFFFFFFFu, d, 0);
+                    f = __shfl_sync(0xFFFFFFFFu, f, 0);
+                    if (f) {
+                        join_compaction();
+                        continue;
+                    }
+                    if (d >= kNCW) break;
+                    if (clock64() - t0 > kSpinLimit) {  // cannot happen; keep the CTA alive
+                        set_status(kErrTimeout);
+                        break;
                     }
                 }
             }
-            bi += d8;
-            sub += r8;
-            if (sub >= cpb) {
-                sub -= cpb;
-                ++bi;
+            named_bar_sync(1, NC);
+            if (tid == 0) {
+                ctrl->fin_n = ctrl->cnt < p.cap ? ctrl->cnt : p.cap;
             }
-            st += kNCW;
-            if (st >= p.stages) {
-                st -= p.stages;
-                ++use;
+            __syncthreads();
+            if (ctrl->abort && tid == 0) {
+                for (int s = 0; s < p.stages; ++s)
+                    if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
             }
-        }
-        // A warp out of chunks still joins compactions other warps request: it reads the
-        // count of finished warps before the request flag, so a request raised by the
-        // last warp before it finished is always seen.
-        __threadfence_block();
-        if (lane == 0) atomicAdd(&ctrl->done_warps, 1);
-        {
-            const long long t0 = clock64();
-            while (true) {
-                int d = 0, f = 0;
-                if (lane == 0) {
-                    d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
-                    __threadfence_block();
-                    f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
+            __syncthreads();
+
+            // ---------------------------- final selection over the cluster ------------
+            n = ctrl->fin_n;
+            // Keys below the edge are out of play: at least k keys of the cluster's union lie
+            // at or above it (on a speculative edge, the first pass checks that they do).
+            edge = ctrl->wedge;  // the same in every CTA of the cluster
+            const uint32_t kmax = KW == 16 ? 0xFFFFu : 0xFFFFFFFFu;
+            const auto in_play = [&](uint32_t kk) { return kk >= edge; };
+            // pass state (identical in every CTA): keys in [lbase, lhi] binned by
+            // (key - lbase) >> s, the last bin open-ended
+            uint32_t lbase = edge, lhi = kmax;
+            int s = edge ? (ES == 2 ? 0 : 23 - kXBits) : (KW - kXBits);
+            uint32_t krem = static_cast<uint32_t>(p.k);
+            gt_all = gt_lower = eq_lower = eq_mine = pivot = 0u;
+            take_all = false;
+            bool retry = false;
+            // Pass lvl exchanges its histograms through round lvl % 2; attempt a starts with
+            // pass a, whose counts this CTA made as keys were appended.
+            for (int lvl = att;; ++lvl) {
+                uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
+                if (lvl > att) {  // (the slot was cleared before the previous pass's last barrier)
+#pragma unroll 4
+                    for (int i = tid; i < n; i += NT) {
+                        const uint32_t kk = ckey[i];
+                        if (in_play(kk) && kk >= lbase && kk <= lhi) {
+                            uint32_t d = (kk - lbase) >> s;
+                            d = d < kXBins - 1 ? d : kXBins - 1;
+                            atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
+                        }
+                    }
                 }
-                d = __shfl_sync(0xFFFFFFFFu, d, 0);
-                f = __shfl_sync(0xFFFFFFFFu, f, 0);
-                if (f) {
-                    join_compaction();
-                    continue;
+                fence_proxy_async_smem();
+                __syncthreads();
+                uint64_t* xb = &ctrl->xbar[lvl & 1];
+                if (G > 1) {
+                    if (tid == 0) {
+                        const uint32_t bytes = XW * 4u;
+                        mbar_arrive_expect_tx(xb, bytes * static_cast<uint32_t>(G - 1));
+                        for (int r = 0; r < G; ++r)
+                            if (r != static_cast<int>(crank))
+                                bulk_s2s_cluster(map_rank(mine, r), mine, bytes, map_rank(xb, r));
+                    }
+                    wait_bounded_cluster(xb, (lvl >> 1) & 1, ctrl);
                 }
-                if (d >= kNCW) break;
-                if (clock64() - t0 > kSpinLimit) {  // cannot happen; keep the CTA alive
-                    set_status(kErrTimeout);
+                // this CTA's slot of the other round is free again (what it held was pushed a round
+                // ago and every peer has used it since): clear it for the next pass
+                uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
+                for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
+                // the cluster's histogram: the CTA finds the pivot bin
+                const uint32_t* rows = xr + static_cast<size_t>(lvl & 1) * G * XW;
+                cta_pivot_x(rows, G, static_cast<int>(crank), krem, tid, ctrl->warp_tot[0], ctrl);
+                XPivot pv;
+                pv.bstar = static_cast<int>(ctrl->fp_tot[0]);
+                pv.above = ctrl->fp_tot[1];
+                pv.low_above = ctrl->fp_tot[2];
+                pv.eq_lower = ctrl->fp_tot[3];
+                const int bstar = pv.bstar;
+                gt_lower += pv.low_above;
+                gt_all += pv.above;
+                if (bstar < 0) {  // fewer than krem keys in play (only possible in the first pass)
+                    if (spec_ok && att == 0 && edge > ctrl->wedge_p) {  // the speculative edge failed
+                        retry = true;
+                        break;
+                    }
+                    take_all = true;  // keep them all
                     break;
                 }
-            }
-        }
-        named_bar_sync(1, NC);
-        if (tid == 0) {
-            ctrl->fin_n = ctrl->cnt < p.cap ? ctrl->cnt : p.cap;
-            ctrl->fin_hasT = hasT ? 1 : 0;
-            ctrl->fin_T = T;
-        }
-    }
-    __syncthreads();
-    if (ctrl->abort && tid == 0) {
-        for (int s = 0; s < p.stages; ++s)
-            if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
-    }
-    __syncthreads();
-
-    // ------------------------------ final selection over the cluster ----------------
-    const int n = ctrl->fin_n;
-    // Keys below the warm-up bucket's edge are out of play: at least k keys of the
-    // cluster's union lie at or above it.
-    const uint32_t edge = ctrl->wedge;  // the same in every CTA of the cluster
-    const uint32_t kmax = KW == 16 ? 0xFFFFu : 0xFFFFFFFFu;
-    const auto in_play = [&](uint32_t kk) { return kk >= edge; };
-    // pass state (identical in every CTA): keys in [lbase, lhi] binned by (key - lbase) >> s,
-    // the last bin open-ended
-    uint32_t lbase = edge, lhi = kmax;
-    int s = edge ? (ES == 2 ? 0 : 23 - kXBits) : (KW - kXBits);
-    uint32_t krem = static_cast<uint32_t>(p.k);
-    uint32_t gt_all = 0u, gt_lower = 0u;      // keys above the pivot: all CTAs, CTAs of lower rank
-    uint32_t eq_lower = 0u, eq_mine = 0u;     // pivot-equal keys: CTAs of lower rank, this CTA
-    uint32_t pivot = 0u;
-    bool take_all = false;
-    // two rounds of G histograms of kXBins uint16 counts, as pairs in 32-bit words; this
-    // CTA's slot of round 0 holds the first pass's counts, made as keys were appended
-    constexpr int XW = kXBins / 2;
-    uint32_t* xr = reinterpret_cast<uint32_t*>(smem + L.xf);
-    for (int lvl = 0;; ++lvl) {
-        uint32_t* mine = xr + (static_cast<size_t>(lvl & 1) * G + crank) * XW;
-        if (lvl > 0) {  // (the slot was cleared before the previous pass's last barrier)
-#pragma unroll 4
-            for (int i = tid; i < n; i += NT) {
-                const uint32_t kk = ckey[i];
-                if (in_play(kk) && kk >= lbase && kk <= lhi) {
-                    uint32_t d = (kk - lbase) >> s;
-                    d = d < kXBins - 1 ? d : kXBins - 1;
-                    atomicAdd(&mine[d >> 1], 1u << ((d & 1u) * 16u));
+                krem -= pv.above;
+                if (s > 0 || bstar == kXBins - 1) {
+                    // The bin holds exactly the keys still needed: take it whole, with every key
+                    // above it, and stop (no further pass to find the pivot key inside it).
+                    uint32_t binc = 0u;
+                    for (int c = 0; c < G; ++c) binc += reinterpret_cast<const uint16_t*>(rows)[c * kXBins + bstar];
+                    const uint32_t lo_bin = lbase + (static_cast<uint32_t>(bstar) << s);
+                    if (binc == krem && lo_bin > 0u) {
+                        pivot = lo_bin - 1u;  // keys above it are taken; none equal to it is
+                        gt_lower += pv.eq_lower;
+                        gt_all += binc;
+                        krem = 0u;
+                        break;
+                    }
+                }
+                if (s == 0 && bstar < kXBins - 1) {
+                    pivot = lbase + static_cast<uint32_t>(bstar);
+                    eq_lower = pv.eq_lower;
+                    eq_mine = reinterpret_cast<const uint16_t*>(rows)[crank * kXBins + bstar];
+                    break;
+                }
+                if (bstar < kXBins - 1) {
+                    lbase += static_cast<uint32_t>(bstar) << s;
+                    const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
+                    lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
+                    s = s > kXBits ? s - kXBits : 0;
+                } else {  // the open top bin: its keys all lie in [lbase + (kXBins - 1) << s, lhi]
+                    lbase += static_cast<uint32_t>(kXBins - 1) << s;
+                    const int sb = bit_length(lhi - lbase) - kXBits;
+                    s = sb > 0 ? sb : 0;
                 }
             }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        uint64_t* xb = &ctrl->xbar[lvl & 1];
-        if (G > 1) {
+            if (!retry) break;
+            // Fewer than k keys of the row reach the speculative edge.  Every chunk is still in
+            // the ring: filter them all again from the proven edge, counting the first
+            // histogram into this CTA's slot of the next round (cleared by the pass above).
+            const uint32_t pe = ctrl->wedge_p;
+            __syncthreads();  // every thread has read the pass's results
             if (tid == 0) {
-                const uint32_t bytes = XW * 4u;
-                mbar_arrive_expect_tx(xb, bytes * static_cast<uint32_t>(G - 1));
-                for (int r = 0; r < G; ++r)
-                    if (r != static_cast<int>(crank)) bulk_s2s_cluster(map_rank(mine, r), mine, bytes, map_rank(xb, r));
+                ctrl->cnt = 0;
+                ctrl->fail_base = 0x7FFFFFFF;
+                ctrl->done_warps = 0;
+                ctrl->compact_req = 0;
+                ctrl->last_kept = 0;
+                ctrl->raise_mark = 0u;
+                ctrl->wedge = pe;
             }
-            wait_bounded_cluster(xb, (lvl >> 1) & 1, ctrl);
-        }
-        // this CTA's slot of the other round is free again (what it held was pushed a round
-        // ago and every peer has used it since): clear it for the next pass
-        uint32_t* next_mine = xr + (static_cast<size_t>((lvl + 1) & 1) * G + crank) * XW;
-        for (int i = tid; i < XW; i += NT) next_mine[i] = 0u;
-        // the cluster's histogram: the CTA finds the pivot bin
-        const uint32_t* rows = xr + static_cast<size_t>(lvl & 1) * G * XW;
-        cta_pivot_x(rows, G, static_cast<int>(crank), krem, tid, ctrl->warp_tot[0], ctrl);
-        XPivot pv;
-        pv.bstar = static_cast<int>(ctrl->fp_tot[0]);
-        pv.above = ctrl->fp_tot[1];
-        pv.low_above = ctrl->fp_tot[2];
-        pv.eq_lower = ctrl->fp_tot[3];
-        const int bstar = pv.bstar;
-        gt_lower += pv.low_above;
-        gt_all += pv.above;
-        if (bstar < 0) {  // fewer than krem keys in play: keep them all
-            take_all = true;
-            break;
-        }
-        krem -= pv.above;
-        if (s > 0 || bstar == kXBins - 1) {
-            // The bin holds exactly the keys still needed: take it whole, with every key
-            // above it, and stop (no further pass to find the pivot key inside it).
-            uint32_t binc = 0u;
-            for (int c = 0; c < G; ++c) binc += reinterpret_cast<const uint16_t*>(rows)[c * kXBins + bstar];
-            const uint32_t lo_bin = lbase + (static_cast<uint32_t>(bstar) << s);
-            if (binc == krem && lo_bin > 0u) {
-                pivot = lo_bin - 1u;  // keys above it are taken; none equal to it is
-                gt_lower += pv.eq_lower;
-                gt_all += binc;
-                krem = 0u;
-                break;
-            }
-        }
-        if (s == 0 && bstar < kXBins - 1) {
-            pivot = lbase + static_cast<uint32_t>(bstar);
-            eq_lower = pv.eq_lower;
-            eq_mine = reinterpret_cast<const uint16_t*>(rows)[crank * kXBins + bstar];
-            break;
-        }
-        if (bstar < kXBins - 1) {
-            lbase += static_cast<uint32_t>(bstar) << s;
-            const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
-            lhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
-            s = s > kXBits ? s - kXBits : 0;
-        } else {  // the open top bin: its keys all lie in [lbase + (kXBins - 1) << s, lhi]
-            lbase += static_cast<uint32_t>(kXBins - 1) << s;
-            const int sb = bit_length(lhi - lbase) - kXBits;
-            s = sb > 0 ? sb : 0;
+            hasT = true;
+            T = pe - 1u;
+            hedge = pe;
+            tmax = 0u;
+            gnext = 0u;
+            __syncthreads();
         }
     }
     // Every CTA has read and pushed all it will: the cluster barrier's arrival goes now and

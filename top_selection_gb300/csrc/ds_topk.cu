@@ -47,6 +47,8 @@ constexpr int kScanThreads = (kNCW + 1) * 32;
 constexpr int kMergeThreads = 512;              // one CTA per row over several clusters
 constexpr int kChunkBytesMax = 16384;          // one bulk copy
 constexpr int kLiteralStages = 8;              // deepest ring of one-CTA rows
+constexpr int kSpecMargin = 2;                 // speculative rank: this many times the sample's
+constexpr int kSpecMin = 64;                   //   expected share of the top k, at least kSpecMin
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -95,6 +97,8 @@ struct ScanParams {
     int32_t early;                // start reading x before the previous kernel completes
     int32_t rmark, rstep;         // split rows: raise T from the appended keys' histogram when the
                                   //   buffer holds rmark keys, then every rstep more (0 = never)
+    int32_t spec_k;               // split rows held whole: the first attempt filters from the
+                                  //   spec_k-th largest sampled maximum (0 = never)
     uint32_t epoch;
     unsigned long long* gT;       // per-row shared threshold (C > 1)
     uint32_t* ws_key;             // per (row, cluster) partial results (C > 1)
@@ -959,6 +963,7 @@ struct Plan {
     int B, B2;  // block size and compaction slack in effect (the library's choice when given as 0)
     bool split;  // the split-row kernel (also for one part per row), else the one-CTA-per-row kernel
     bool held;   // split rows: every CTA's chunks fit its ring at once
+    int spec_k;  // split rows held whole in one cluster: the speculative rank (0 = none)
     int64_t m;
     size_t smem, merge_smem, ws_bytes;
     int merge_cap;
@@ -1057,6 +1062,7 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
     P.ww = 1;
     P.refine = 0;
     P.held = false;
+    P.spec_k = 0;
     P.split = parts > 1 || split1;
     if (P.split) {
         // Split rows: each consumer warp owns whole chunks, so the ring depth is a multiple
@@ -1134,6 +1140,16 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         // chunks, so a thread's sample is at most 4 vectors)
         P.held = (P.m + parts - 1) / parts * ((static_cast<int64_t>(B) + P.chunk - 1) / P.chunk) <= P.stages &&
                  P.chunk * P.es <= 8192;
+        // Rows held whole in one cluster speculate: the cluster's sample of S elements holds
+        // about k * S / N of the row's k largest, so its spec_k-th largest maximum, spec_k
+        // twice that, likely lies below the row's k-th largest and well above the proven
+        // edge.  The final select checks it, and a failure filters the resident chunks once
+        // more.  Too small a spec_k (a noisy estimate) or one not below k turns it off.
+        if (P.held && G == parts) {
+            const int64_t S = static_cast<int64_t>(G) * P.ww * P.chunk;
+            const int64_t sk = (kSpecMargin * static_cast<int64_t>(k) * S + N - 1) / N;
+            if (sk >= kSpecMin && sk < k) P.spec_k = static_cast<int>(sk);
+        }
     } else {
         const auto layout_bytes = [&](int s) -> size_t {
             return scan_layout(P.es, P.chunk, s, P.cap, P.perm_cap).total;
@@ -1239,6 +1255,7 @@ static ds_status launch(const Plan& P, const void* x, int64_t rows, int64_t N, i
     // the buffer holds k keys plus a step (or half of its room past k), then every step.
     sp.rstep = P.split && P.refine ? (k > 256 ? k : 256) : 0;
     sp.rmark = sp.rstep ? k + (sp.rstep < (P.cap - k) / 2 ? sp.rstep : (P.cap - k) / 2) : 0;
+    sp.spec_k = P.spec_k;
     sp.epoch = 0;
     sp.gT = nullptr;
     sp.ws_key = nullptr;
@@ -1378,6 +1395,7 @@ ds_status ds_get_plan(int32_t dtype, int64_t rows, int64_t N, int32_t k, int32_t
     plan->merge_launch = P.C > 1 ? 1 : 0;
     plan->B = P.B;
     plan->B2 = P.B2;
+    plan->spec_k = P.spec_k;
     return DS_OK;
 }
 
