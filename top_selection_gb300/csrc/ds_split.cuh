@@ -1295,19 +1295,20 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     }
                 }
             }
+            // every warp is done: the buffer, its count and the first histogram are final
+            // (the histogram leaves by bulk copy: the async proxy must see the appends)
+            fence_proxy_async_smem();
             named_bar_sync(1, NC);
-            if (tid == 0) {
-                ctrl->fin_n = ctrl->cnt < p.cap ? ctrl->cnt : p.cap;
+            if (ctrl->abort) {
+                if (tid == 0)
+                    for (int s = 0; s < p.stages; ++s)
+                        if (ctrl->issued[s] > ctrl->observed[s])
+                            drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
+                __syncthreads();
             }
-            __syncthreads();
-            if (ctrl->abort && tid == 0) {
-                for (int s = 0; s < p.stages; ++s)
-                    if (ctrl->issued[s] > ctrl->observed[s]) drain_wait(&ctrl->full[s], (ctrl->issued[s] - 1) & 1);
-            }
-            __syncthreads();
 
             // ---------------------------- final selection over the cluster ------------
-            n = ctrl->fin_n;
+            n = ctrl->cnt < p.cap ? ctrl->cnt : p.cap;
             // Keys below the edge are out of play: at least k keys of the cluster's union lie
             // at or above it (on a speculative edge, the first pass checks that they do).
             edge = ctrl->wedge;  // the same in every CTA of the cluster
@@ -1336,8 +1337,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                         }
                     }
                 }
-                fence_proxy_async_smem();
-                __syncthreads();
+                if (lvl > att) {  // (the attempt's first pass was ordered after the drain)
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                }
                 uint64_t* xb = &ctrl->xbar[lvl & 1];
                 if (G > 1) {
                     if (tid == 0) {
