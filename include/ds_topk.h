@@ -19,8 +19,8 @@
  * Block order.  Block b of row r is visited in the order of
  *   u_b = Philox4x32-10(key = (seed & 0xffffffff, seed >> 32), counter = (b, r, 0, 0))[0]
  * ascending, ties by b (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2, 3",
- * SC'11).  When a row is split into parts, each part visits its own contiguous range of
- * blocks in the order of the same draws.
+ * SC'11).  When a row is split into P parts, part p takes every P-th block from block p
+ * (blocks p, p + P, p + 2P, ...) and visits them in the order of the same draws.
  *
  * Results.  out_vals[r*k + j] / out_idx[r*k + j], j < k, hold the k largest values of
  * row r (bit copies of the input) and their columns, in no particular order (in order of
@@ -118,8 +118,9 @@ ds_status ds_topk(const void* x, int32_t dtype, int64_t rows, int64_t N, int64_t
 
 typedef struct {
     int32_t parts;          /* CTAs per row: 0 = library choice; 1 = one CTA per row (the
-                               pages' schedule, required for stats); >1 splits each row
-                               into that many contiguous ranges of blocks             */
+                               pages' schedule, required for stats); P > 1 splits each
+                               row's blocks into P interleaved sets (block b to part
+                               b mod P)                                               */
     int32_t cluster;        /* CTAs per thread-block cluster (divides parts, <= 16);
                                0 = library choice                                     */
     int64_t* stats;         /* optional device array rows*DS_NSTAT, parts == 1 only    */

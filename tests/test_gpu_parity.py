@@ -223,16 +223,13 @@ def _spikes_in_sampled_blocks(w, k, seed):
     assert plan["spec_k"] > 0, plan
     parts = plan["parts"]
     m = -(-w.N // w.B)
-    mq, mr = divmod(m, parts)
     x = w.x[:, : w.N].copy()
     xf = synth.bf16_bits_to_f32(x) if w.dtype == synth.BF16 else x
     rng = np.random.default_rng(0xB10C)
     per = (k - 32) // parts
     for r in range(w.rows):
-        for p in range(parts):
-            b0 = p * mq + min(p, mr)
-            mp = mq + (1 if p < mr else 0)
-            first = min((oracle.block_draw(seed, r, b), b) for b in range(b0, b0 + mp))[1]
+        for p in range(parts):  # part p holds blocks p, p + parts, ...
+            first = min((oracle.block_draw(seed, r, b), b) for b in range(p, m, parts))[1]
             lo, hi = first * w.B, min(first * w.B + w.B, w.N)
             cols = lo + rng.choice(hi - lo, size=per, replace=False)
             xf[r, cols] = rng.uniform(8.0, 12.0, size=per).astype(np.float32)

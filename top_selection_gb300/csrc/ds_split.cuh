@@ -841,8 +841,9 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
     const int part = cta - rowi * p.parts;
     const int cl = part / G;
     const uint32_t crank = G > 1 ? cluster_ctarank() : 0u;
-    // this part's blocks: parts [0, mr) take mq + 1 blocks, the others mq
-    const int64_t b0 = static_cast<int64_t>(part) * p.mq + (part < p.mr ? part : p.mr);
+    // this part's blocks: every parts-th block of the row from block `part` (parts [0, mr)
+    // take mq + 1 blocks, the others mq), so that rows whose large values sit in one
+    // region spread them over the CTAs
     const int mp = static_cast<int>(p.mq) + (part < p.mr ? 1 : 0);
     const char* xrow = p.x + row * p.stride_bytes;
     const int chunk_bytes = p.chunk * ES;
@@ -892,7 +893,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         uint32_t* x0 = reinterpret_cast<uint32_t*>(smem + L.xf) + static_cast<size_t>(crank) * (kXBins / 2);
         for (int i = tid; i < kXBins / 2; i += NT) x0[i] = 0u;
     }
-    block_order<NT>(p.seed, row, b0, mp, hist, perm, tid);
+    block_order<NT>(p.seed, row, part, p.parts, mp, hist, perm, tid);
 
     // chunk slot q: block perm[bi] with bi = q / cpb, sub-chunk q % cpb (empty past the
     // row's end); the chunk loop steps (bi, sub) without dividing

@@ -368,12 +368,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// Visiting order of blocks b0 .. b0+mp-1 of `row`: draw u_b = Philox(seed; b, row) for
-// each block, and place each block at its rank in (u_b, b) order.  `draws` is scratch of
-// mp words.  Ends with a CTA barrier.
+// Visiting order of the mp blocks b0, b0 + stride, ..., b0 + (mp - 1) * stride of `row`:
+// draw u_b = Philox(seed; b, row) for each block, and place each block at its rank in
+// (u_b, b) order -- the row's own order restricted to these blocks.  `draws` is scratch
+// of mp words.  Ends with a CTA barrier.
 template <int NT>
-__device__ void block_order(uint64_t seed, int64_t row, int64_t b0, int mp, uint32_t* draws, int32_t* perm, int tid) {
-    for (int j = tid; j < mp; j += NT) draws[j] = block_draw(seed, row, b0 + j);
+__device__ void block_order(uint64_t seed, int64_t row, int64_t b0, int64_t stride, int mp, uint32_t* draws,
+                            int32_t* perm, int tid) {
+    for (int j = tid; j < mp; j += NT) draws[j] = block_draw(seed, row, b0 + j * stride);
     __syncthreads();
     for (int j = tid; j < mp; j += NT) {
         const uint32_t u = draws[j];
@@ -382,7 +384,7 @@ __device__ void block_order(uint64_t seed, int64_t row, int64_t b0, int mp, uint
             const uint32_t v = draws[j2];
             r += (v < u || (v == u && j2 < j)) ? 1 : 0;
         }
-        perm[r] = static_cast<int32_t>(b0 + j);
+        perm[r] = static_cast<int32_t>(b0 + j * stride);
     }
     __syncthreads();
 }
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(256) ds_block_order_kernel(uint64_t seed, int6
                                                               int32_t* out) {
     __shared__ uint32_t draws[kPermMax];
     __shared__ int32_t perm[kPermMax];
-    block_order<256>(seed, row, b0, mp, draws, perm, threadIdx.x);
+    block_order<256>(seed, row, b0, 1, mp, draws, perm, threadIdx.x);
     for (int j = threadIdx.x; j < mp; j += 256) out[j] = perm[j];
 }
 
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) ds_scan_kernel(const ScanPara
         mbar_init(&ctrl->empty[tid], kNCW);
         fence_mbar_init();
     }
-    block_order<NT>(p.seed, row, 0, mp, hist, perm, tid);
+    block_order<NT>(p.seed, row, 0, 1, mp, hist, perm, tid);
     if (!p.early) pdl_wait();
 
     if (warp == kNCW) {
