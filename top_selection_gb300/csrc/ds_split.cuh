@@ -1165,10 +1165,14 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 hasT = true;
                 T = sedge - 1u;
                 hedge = sedge;
-                hs0 = ES == 2 ? 0 : 23 - kXBits;
+                // (fp32: bins of 2^14 keys span an octave above the edge; a speculative edge
+                // lies close below the k-th key, so bins four times narrower usually leave
+                // the pivot's bin holding just the keys still needed: one pass)
+                hs0 = ES == 2 ? 0 : (sedge > wedge0 ? 23 - kXBits - 2 : 23 - kXBits);
             }
             // (every CTA of the cluster derived this same threshold: only the row's other
             // clusters need it)
+            if (tid == 0) ctrl->hshift = hs0;
             if (tid == 0 && hasT && MC) publish_T(T);
         }
 
@@ -1318,7 +1322,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // pass state (identical in every CTA): keys in [lbase, lhi] binned by
             // (key - lbase) >> s, the last bin open-ended
             uint32_t lbase = edge, lhi = kmax;
-            int s = edge ? (ES == 2 ? 0 : 23 - kXBits) : (KW - kXBits);
+            int s = edge ? ctrl->hshift : (KW - kXBits);
             uint32_t krem = static_cast<uint32_t>(p.k);
             gt_all = gt_lower = eq_lower = eq_mine = pivot = 0u;
             take_all = false;
@@ -1426,6 +1430,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             hasT = true;
             T = pe - 1u;
             hedge = pe;
+            hs0 = ES == 2 ? 0 : 23 - kXBits;
+            if (tid == 0) ctrl->hshift = hs0;
             tmax = 0u;
             gnext = 0u;
             __syncthreads();
