@@ -109,7 +109,9 @@ print(json.dumps({n: ds.ds_get_plan(*a) for n, a in shapes.items()}))
 def test_plans_on_a_described_device(lib):
     """The planner's choices for the workload shapes, on a described 152-SM part with
     228 KB of shared memory per SM (no GPU needed): rows under 16 MB stay in one cluster
-    (no merge pass), huge rows spread over clusters, one-CTA rows where k is large."""
+    (no merge pass), huge rows spread over clusters, one-CTA rows where k is large; where
+    the CTAs are no more than the SMs (long-context and single rows), each CTA takes a
+    whole SM's shared memory and holds all its chunks in a ring of up to 16 stages."""
     import json
     import sys
     env = dict(os.environ, DS_PLAN_DEVICE="152,232448,233472", CUDA_VISIBLE_DEVICES="")
@@ -124,11 +126,15 @@ def test_plans_on_a_described_device(lib):
     assert pc("longctx") == (16, 16, 0)
     assert pc("row65536") == (8, 8, 0)
     assert pc("huge") == (256, 8, 1)
+    rows = {"indexer": 64, "sampler": 256, "sampler_k4096": 256, "longctx": 4, "row65536": 1, "huge": 1}
     for n, p in plans.items():
         assert p["smem_bytes"] <= 232448, n
         if p["threads"] == 256:
             assert p["stages"] in (8, 16), n          # warp-owned stages
-            assert p["ctas_per_sm"] == 2, n
+            if rows[n] * p["parts"] <= 152:
+                assert p["ctas_per_sm"] == 1 and p["chunk_elems"] * (2 if n in ("indexer", "longctx") else 4) <= 8192, n
+            else:
+                assert p["ctas_per_sm"] == 2, n
 
 
 _PLAN_SWEEP = """
@@ -270,7 +276,7 @@ def test_speculative_rank_on_a_described_device(lib):
     assert got["indexer_k64"]["spec_k"] == 0              # 32 < 64: too noisy
     assert got["indexer_k2048"]["spec_k"] == expect(got["indexer_k2048"], 2048, 131072) == 512
     assert got["row65536"]["spec_k"] == expect(got["row65536"], 512, 65536) == 256
-    assert got["longctx"]["stages"] < 16 and got["longctx"]["spec_k"] == 0  # 16 chunks per CTA: streamed
+    assert got["longctx"]["spec_k"] == expect(got["longctx"], 512, 1048576) == 128  # a whole SM per CTA: held
     assert got["sampler"]["spec_k"] == 0                   # streamed through the ring
     assert got["one_cta"]["spec_k"] == 0                   # the pages' one-CTA schedule
     assert got["spread"]["merge_launch"] == 1 and got["spread"]["spec_k"] == 0  # several clusters

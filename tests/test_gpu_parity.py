@@ -236,9 +236,11 @@ def _spikes_in_sampled_blocks(w, k, seed):
     return synth.f32_to_bf16_bits(xf) if w.dtype == synth.BF16 else xf
 
 
-@pytest.mark.parametrize("shape,k", [("indexer", 512), ("indexer", 2048), ("row65536", 512)])
+@pytest.mark.parametrize("shape,k", [("indexer", 512), ("indexer", 2048), ("row65536", 512), ("longctx", 512),
+                                     ("longctx", 2048)])
 def test_spikes_in_every_sampled_block(shape, k):
-    w = {"indexer": synth.indexer_bf16, "row65536": synth.row65536_f32}[shape]()
+    w = {"indexer": synth.indexer_bf16, "row65536": synth.row65536_f32,
+         "longctx": lambda: synth.longctx_bf16("iid")}[shape]()
     seed = 0x5EED
     x = _spikes_in_sampled_blocks(w, k, seed)
     v, i, _ = run_gpu(x, w.dtype, k, w.B, w.B2, seed)

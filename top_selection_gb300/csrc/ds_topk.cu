@@ -1132,6 +1132,15 @@ static ds_status make_plan(int dev, int32_t dtype, int64_t rows, int64_t N, int3
         const int first = B < kChunkBytesMax / P.es ? B : kChunkBytesMax / P.es;
         const size_t two = static_cast<size_t>(di.smem_per_sm) / 2 - 1024;
         bool ok = false;
+        // Rows whose CTAs each get an SM of their own (rows x parts <= SMs) keep each part's
+        // chunks in the ring at once where a ring of at most 16 stages of at most 8 KB fits
+        // an SM's whole shared memory: every copy issues at start-up and the rows run the
+        // held instance, instead of streaming through a ring sized for two CTAs per SM.
+        if (rows * parts <= di.sms) {
+            const int c = first * P.es <= 8192 ? first : 8192 / P.es;
+            const int64_t chunks = (P.m + parts - 1) / parts * ((static_cast<int64_t>(B) + c - 1) / c);
+            if (chunks <= 2 * kNCW) ok = fit(c, chunks <= kNCW ? kNCW : 2 * kNCW, static_cast<size_t>(di.smem_optin));
+        }
         for (int c = first; !ok && c * P.es >= 1024; c = (c / 2) / unit * unit)
             ok = fit(c, 2 * kNCW, two) || fit(c, kNCW, two);
         for (int c = first; !ok && c * P.es >= 1024; c = (c / 2) / unit * unit)
