@@ -66,7 +66,8 @@ struct Ctrl {
     uint32_t cut_keep;           //   keys kept)
     int last_kept;               // split rows: the buffer's count after the last compaction
     uint32_t lmax;               // split rows: the largest of this CTA's warm-up group maxima
-    int hshift;                  // split rows: the first final histogram's bins are 2^hshift keys wide
+    int hshift;                  // split rows: the first final histogram's bins are 2^hshift keys wide,
+    uint32_t hbase;              //   from key hbase up
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

@@ -1079,10 +1079,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // saves fewer appends than finding it costs.)
             uint32_t wedge0 = 0u;
             bool coarse = HELD;
+            uint32_t Mw = 0u;  // the union's largest maximum (streamed rows)
             if (!HELD) {
                 uint32_t M = ctrl->lmax;
                 for (int r = 0; r < G; ++r)
                     if (r != static_cast<int>(crank)) M = max(M, *reinterpret_cast<const uint32_t*>(wx + r * WS + wm));
+                Mw = M;
                 constexpr int FS = ES == 2 ? 0 : 13;
                 each_key<KeyT>(wx, G, wm, tid, [&](uint32_t kk) {
                     const uint32_t d = (M - kk) >> FS;
@@ -1170,9 +1172,23 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 // the pivot's bin holding just the keys still needed: one pass)
                 hs0 = ES == 2 ? 0 : (sedge > wedge0 ? 23 - kXBits - 2 : 23 - kXBits);
             }
+            // Streamed rows without a warm-up edge (k beyond what the sample can bound) still
+            // bin the first final histogram below M: kXBins bins of one key (bf16) or 2^16
+            // keys (fp32, 4 octaves in all), M in the next-to-last, so that threshold raises
+            // and compaction cuts see fine bins.  Nothing proves the k-th key lies there; the
+            // final select's first pass checks it and counts the whole range otherwise.
+            if (!HELD && sedge == 0u && Mw > 0u) {
+                constexpr int WSH = ES == 2 ? 0 : 16;
+                const uint32_t span = static_cast<uint32_t>(kXBins - 2) << WSH;
+                hedge = Mw > span ? Mw - span : 0u;
+                hs0 = WSH;
+            }
+            if (tid == 0) {
+                ctrl->hshift = hs0;
+                ctrl->hbase = hedge;
+            }
             // (every CTA of the cluster derived this same threshold: only the row's other
             // clusters need it)
-            if (tid == 0) ctrl->hshift = hs0;
             if (tid == 0 && hasT && MC) publish_T(T);
         }
 
@@ -1321,8 +1337,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             const auto in_play = [&](uint32_t kk) { return kk >= edge; };
             // pass state (identical in every CTA): keys in [lbase, lhi] binned by
             // (key - lbase) >> s, the last bin open-ended
-            uint32_t lbase = edge, lhi = kmax;
-            int s = edge ? ctrl->hshift : (KW - kXBits);
+            uint32_t lbase = ctrl->hbase, lhi = kmax;  // the first pass: the appends' bins
+            int s = ctrl->hshift;
             uint32_t krem = static_cast<uint32_t>(p.k);
             gt_all = gt_lower = eq_lower = eq_mine = pivot = 0u;
             take_all = false;
@@ -1376,6 +1392,14 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     if (spec_ok && att == 0 && edge > ctrl->wedge_p) {  // the speculative edge failed
                         retry = true;
                         break;
+                    }
+                    if (lbase > edge && lvl == att) {  // the keys below the first pass's bins:
+                        lbase = edge;                  // count the whole range from the edge
+                        lhi = kmax;
+                        s = edge ? (ES == 2 ? 0 : 23 - kXBits) : (KW - kXBits);
+                        krem = static_cast<uint32_t>(p.k);
+                        gt_all = gt_lower = 0u;
+                        continue;
                     }
                     take_all = true;  // keep them all
                     break;
@@ -1431,7 +1455,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             T = pe - 1u;
             hedge = pe;
             hs0 = ES == 2 ? 0 : 23 - kXBits;
-            if (tid == 0) ctrl->hshift = hs0;
+            if (tid == 0) {
+                ctrl->hshift = hs0;
+                ctrl->hbase = pe;
+            }
             tmax = 0u;
             gnext = 0u;
             __syncthreads();
