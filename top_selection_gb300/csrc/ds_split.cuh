@@ -1172,16 +1172,23 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 // the pivot's bin holding just the keys still needed: one pass)
                 hs0 = ES == 2 ? 0 : (sedge > wedge0 ? 23 - kXBits - 2 : 23 - kXBits);
             }
-            // Streamed rows without a warm-up edge (k beyond what the sample can bound) still
-            // bin the first final histogram below M: kXBins bins of one key (bf16) or 2^16
-            // keys (fp32, 4 octaves in all), M in the next-to-last, so that threshold raises
-            // and compaction cuts see fine bins.  Nothing proves the k-th key lies there; the
-            // final select's first pass checks it and counts the whole range otherwise.
-            if (!HELD && sedge == 0u && Mw > 0u) {
+            // A window below M: kXBins bins of one key (bf16) or 2^16 keys (fp32, 4 octaves in
+            // all), M in the next-to-last.  Streamed rows with no warm-up edge, or with one so
+            // far below M that M lies past the edge's bins and the edge below the window (k
+            // beyond what the sample can bound tightly), bin their first final histogram there
+            // instead, so that threshold raises and compaction cuts see fine bins.  Nothing
+            // proves the k-th key lies in the window; the final select's first pass checks it
+            // and counts the whole range from the edge otherwise.
+            if (!HELD && Mw > 0u) {
                 constexpr int WSH = ES == 2 ? 0 : 16;
                 const uint32_t span = static_cast<uint32_t>(kXBins - 2) << WSH;
-                hedge = Mw > span ? Mw - span : 0u;
-                hs0 = WSH;
+                const uint64_t reach =  // where the edge's bins end (the last is open-ended)
+                    sedge ? static_cast<uint64_t>(sedge) + (static_cast<uint64_t>(kXBins - 1) << hs0) : 0u;
+                const uint32_t wb = Mw > span ? Mw - span : 0u;
+                if (Mw >= reach && (sedge == 0u || wb > sedge)) {  // (the edge lies below the window)
+                    hedge = wb;
+                    hs0 = WSH;
+                }
             }
             if (tid == 0) {
                 ctrl->hshift = hs0;
