@@ -496,10 +496,12 @@ __device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t e
 // one and-or per compared word keeps one bit of it, so a vector costs four compares and
 // four logic ops.  bf16: word w holds vectors 4w..4w+3; bit h*16 + 4*(i%4) + q is element
 // 2q+h of vector i.  fp32: word w holds vectors 8w..8w+7; bit 4*(i%8) + q is element q.
-// Appends go in two steps: each lane writes the chunk columns of its hits into its run of
-// the reserved index slots, then the warp walks the reserved slots together (contiguous
-// accesses) to store each hit's key and its row column.  The row's tail elements take the
-// last slots.
+// Sparse passes append in two steps: each lane writes the chunk columns of its hits into
+// its run of the reserved index slots, then the warp walks the reserved slots together
+// (contiguous accesses) to store each hit's key and its row column.  Dense passes (a fifth
+// or more of the elements pass) skip the per-lane bit loop: the warp walks the pass's
+// element positions, one ballot each, and its lanes' hits take consecutive slots.  The
+// row's tail elements take the last slots.
 template <typename KeyT>
 __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint32_t col0, const char* xrow,
                                            int64_t tail_first, int tail_n, uint32_t tb, KeyT* ckey, uint32_t* cidx,
@@ -572,32 +574,77 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
         }
         if (!__shfl_sync(0xFFFFFFFFu, fits, 0)) return false;
         base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        // step 1: the chunk columns of this lane's hits
-        uint32_t pos = base + incl - c;
-        const int cl = (p0 + lane) * EPV;  // column of the lane's first element in the pass
+        if (nbits * 5u >= 512u * EPV) {
+            // dense pass (a fifth or more of its elements pass): the warp writes its hits
+            // position by position, lanes in order, to consecutive slots -- no per-lane bit
+            // loop, no bank conflicts
+            const uint32_t ltm = lanemask_lt();
+            uint32_t run = base;
+#pragma unroll 1
+            for (int i = 0; i < 16; ++i) {
+                const int v = p0 + lane + 32 * i;
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (v < nvec) x = vec[v];
+                const int wsel = i / VPW;
+                uint32_t mw = m[0];
 #pragma unroll
-        for (int w = 0; w < MW; ++w) {
-            uint32_t mm = m[w];
-            while (mm) {
-                const int bb = __ffs(mm) - 1;
-                mm &= mm - 1u;
-                int col;
-                if (ES == 2) col = cl + 32 * EPV * (w * VPW + ((bb & 15) >> 2)) + 2 * (bb & 3) + (bb >> 4);
-                else col = cl + 32 * EPV * (w * VPW + (bb >> 2)) + (bb & 3);
-                cidx[pos++] = static_cast<uint32_t>(col);
+                for (int w = 1; w < MW; ++w)
+                    if (wsel == w) mw = m[w];
+                const int sh = 4 * (i % VPW);
+                const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+                const uint32_t cb = static_cast<uint32_t>(v * EPV);  // column of the vector's first element
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    int bit;
+                    uint32_t raw;
+                    if (ES == 2) {
+                        bit = (e & 1) * 16 + sh + (e >> 1);
+                        raw = (e & 1) ? (xw[e >> 1] >> 16) : (xw[e >> 1] & 0xFFFFu);
+                    } else {
+                        bit = sh + e;
+                        raw = xw[e];
+                    }
+                    const bool hit = (mw >> bit) & 1u;
+                    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hit);
+                    if (hit) {
+                        const uint32_t slot = run + static_cast<uint32_t>(__popc(bal & ltm));
+                        const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+                        ckey[slot] = static_cast<KeyT>(key);
+                        cidx[slot] = col0 + cb + static_cast<uint32_t>(e);
+                        tmax = max(tmax, key);
+                        xhist_add(xh, key, hedge, hs);
+                    }
+                    run += static_cast<uint32_t>(__popc(bal));
+                }
             }
-        }
-        __syncwarp();
-        // step 2: keys and row columns, the warp's slots in order
-        for (uint32_t j = static_cast<uint32_t>(lane); j < nbits; j += 32u) {
-            const uint32_t col = cidx[base + j];
-            const uint32_t raw = ES == 2 ? reinterpret_cast<const uint16_t*>(stage)[col]
-                                         : reinterpret_cast<const uint32_t*>(stage)[col];
-            const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
-            ckey[base + j] = static_cast<KeyT>(key);
-            cidx[base + j] = col0 + col;
-            tmax = max(tmax, key);
-            xhist_add(xh, key, hedge, hs);
+        } else {  // sparse pass
+            // step 1: the chunk columns of this lane's hits
+            uint32_t pos = base + incl - c;
+            const int cl = (p0 + lane) * EPV;  // column of the lane's first element in the pass
+#pragma unroll
+            for (int w = 0; w < MW; ++w) {
+                uint32_t mm = m[w];
+                while (mm) {
+                    const int bb = __ffs(mm) - 1;
+                    mm &= mm - 1u;
+                    int col;
+                    if (ES == 2) col = cl + 32 * EPV * (w * VPW + ((bb & 15) >> 2)) + 2 * (bb & 3) + (bb >> 4);
+                    else col = cl + 32 * EPV * (w * VPW + (bb >> 2)) + (bb & 3);
+                    cidx[pos++] = static_cast<uint32_t>(col);
+                }
+            }
+            __syncwarp();
+            // step 2: keys and row columns, the warp's slots in order
+            for (uint32_t j = static_cast<uint32_t>(lane); j < nbits; j += 32u) {
+                const uint32_t col = cidx[base + j];
+                const uint32_t raw = ES == 2 ? reinterpret_cast<const uint16_t*>(stage)[col]
+                                             : reinterpret_cast<const uint32_t*>(stage)[col];
+                const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+                ckey[base + j] = static_cast<KeyT>(key);
+                cidx[base + j] = col0 + col;
+                tmax = max(tmax, key);
+                xhist_add(xh, key, hedge, hs);
+            }
         }
         if (thit) {
             const uint32_t slot = base + nbits + static_cast<uint32_t>(__popc(tmask & lanemask_lt()));
