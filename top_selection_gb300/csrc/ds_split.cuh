@@ -498,7 +498,7 @@ __device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t e
 // 2q+h of vector i.  fp32: word w holds vectors 8w..8w+7; bit 4*(i%8) + q is element q.
 // Sparse passes append in two steps: each lane writes the chunk columns of its hits into
 // its run of the reserved index slots, then the warp walks the reserved slots together
-// (contiguous accesses) to store each hit's key and its row column.  Dense passes (a fifth
+// (contiguous accesses) to store each hit's key and its row column.  Dense passes (a third
 // or more of the elements pass) skip the per-lane bit loop: the warp walks the pass's
 // element positions, one ballot each, and its lanes' hits take consecutive slots.  The
 // row's tail elements take the last slots.
@@ -574,8 +574,8 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
         }
         if (!__shfl_sync(0xFFFFFFFFu, fits, 0)) return false;
         base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        if (nbits * 5u >= 512u * EPV) {
-            // dense pass (a fifth or more of its elements pass): the warp writes its hits
+        if (nbits * 3u >= 512u * EPV) {
+            // dense pass (a third or more of its elements pass): the warp writes its hits
             // position by position, lanes in order, to consecutive slots -- no per-lane bit
             // loop, no bank conflicts
             const uint32_t ltm = lanemask_lt();
