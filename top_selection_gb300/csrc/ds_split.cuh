@@ -225,6 +225,56 @@ __device__ __forceinline__ uint32_t warm_maxima16(const uint4* v0, int tid, int 
     return top;
 }
 
+// The warm-up maxima when every sampled chunk is whole and the sample a multiple of the
+// CTA's threads (the usual case): no per-vector chunk bookkeeping, and each group's
+// values are reduced packed (NaNs ignored) and keyed once.  Same results as warm_maxima
+// and warm_maxima16.
+template <typename KeyT>
+__device__ __forceinline__ uint32_t packed_max(uint32_t a, uint32_t b) {
+    if (sizeof(KeyT) == 2) return max_bf16x2(a, b);
+    return __float_as_uint(fmaxf(__uint_as_float(a), __uint_as_float(b)));
+}
+template <typename KeyT>
+__device__ __forceinline__ uint32_t vec_max(const uint4& x) {
+    return packed_max<KeyT>(packed_max<KeyT>(x.x, x.y), packed_max<KeyT>(x.z, x.w));
+}
+template <typename KeyT, int NV>
+__device__ __forceinline__ void warm_maxima_whole(const uint4* v0, int tid, int VT, int gsh, uint32_t (&gk)[4]) {
+    constexpr uint32_t kNaN = sizeof(KeyT) == 2 ? 0x7FC07FC0u : 0x7FC00000u;  // (ignored by the max)
+    uint32_t acc[4] = {kNaN, kNaN, kNaN, kNaN};
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        if (j < VT) {
+            const uint32_t m = vec_max<KeyT>(v0[tid + j * kSplitThreads]);
+            const int g = j >> gsh;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                if (g == r) acc[r] = packed_max<KeyT>(acc[r], m);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) gk[r] = max_word_key<KeyT>(acc[r]);
+}
+template <typename KeyT>
+__device__ __forceinline__ uint32_t warm_maxima16_whole(const uint4* v0, int tid, int VT, int gsh, int R, KeyT* out) {
+    constexpr uint32_t kNaN = sizeof(KeyT) == 2 ? 0x7FC07FC0u : 0x7FC00000u;
+    uint32_t acc = kNaN, top = 0u;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (j < VT) acc = packed_max<KeyT>(acc, vec_max<KeyT>(v0[tid + j * kSplitThreads]));
+        if (((j + 1) & ((1 << gsh) - 1)) == 0) {
+            const int g = j >> gsh;
+            if (g < R) {
+                const uint32_t kk = max_word_key<KeyT>(acc);
+                out[g] = static_cast<KeyT>(kk);
+                top = max(top, kk);
+            }
+            acc = kNaN;
+        }
+    }
+    return top;
+}
+
 // The pivot of a final-select pass, found by every warp on its own (no barrier).  The
 // cluster's histogram is G rows of kXBins 16-bit counts (pairs in 32-bit words), row c
 // from the CTA of rank c; lane l owns bins [16l, 16l + 16), higher bins holding larger
@@ -1080,10 +1130,19 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
             uint32_t lm = 0u;  // the largest of this thread's group maxima
+            bool whole = gotw && (ww * cvec) % NC == 0;  // every sampled chunk whole
+#pragma unroll
+            for (int q = 0; q < 8; ++q) whole = whole && (q >= ww || nvw[q] == cvec);
             if (HELD || VT <= 8) {
                 uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
-                if (HELD || VT <= 4) warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
-                else warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+                if (whole) {
+                    if (HELD || VT <= 4) warm_maxima_whole<KeyT, 4>(v0, tid, VT, gsh, gk);
+                    else warm_maxima_whole<KeyT, 8>(v0, tid, VT, gsh, gk);
+                } else if (HELD || VT <= 4) {
+                    warm_maxima<KeyT, 4>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+                } else {
+                    warm_maxima<KeyT, 8>(v0, tid, cvec, ww, VT, gsh, gotw, nvw, gk);
+                }
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     if (r < R) {
@@ -1092,7 +1151,8 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     }
                 }
             } else {
-                lm = warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * WS + tid * R);
+                lm = whole ? warm_maxima16_whole<KeyT>(v0, tid, VT, gsh, R, wx + crank * WS + tid * R)
+                           : warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * WS + tid * R);
             }
             if (!HELD) {  // (streamed rows bin the union below its largest maximum)
                 lm = __reduce_max_sync(0xFFFFFFFFu, lm);
