@@ -256,12 +256,13 @@ __device__ __forceinline__ void warm_maxima_whole(const uint4* v0, int tid, int 
     for (int r = 0; r < 4; ++r) gk[r] = max_word_key<KeyT>(acc[r]);
 }
 template <typename KeyT>
-__device__ __forceinline__ uint32_t warm_maxima16_whole(const uint4* v0, int tid, int VT, int gsh, int R, KeyT* out) {
+__device__ __forceinline__ uint32_t warm_maxima16_whole(const uint4* v0, int tid, int stride, int VT, int gsh, int R,
+                                                        KeyT* out) {
     constexpr uint32_t kNaN = sizeof(KeyT) == 2 ? 0x7FC07FC0u : 0x7FC00000u;
     uint32_t acc = kNaN, top = 0u;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        if (j < VT) acc = packed_max<KeyT>(acc, vec_max<KeyT>(v0[tid + j * kSplitThreads]));
+        if (j < VT) acc = packed_max<KeyT>(acc, vec_max<KeyT>(v0[tid + j * stride]));
         if (((j + 1) & ((1 << gsh) - 1)) == 0) {
             const int g = j >> gsh;
             if (g < R) {
@@ -1109,31 +1110,48 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                 nvw[q] = static_cast<int>(ce * ES / 16);
             }
         }
-        bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
-        if (tid == 0 && got0) ctrl->observed[0] = 1;
-        if (lane == 0)
-            for (int q = warp < ww ? warp + kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
-        bool gotw = got0;
-        for (int q = 1; q < ww; ++q) {
-            const bool g = wait_bounded(&ctrl->full[q], 0, ctrl);
-            if (tid == 0 && g) ctrl->observed[q] = 1;
-            gotw = gotw && g;
+        // With one sampled chunk per warp (streamed rows sampling kNCW whole chunks) each warp
+        // takes the group maxima of its own chunk as soon as that chunk lands.
+        const int R = wm / 256;
+        const int VT = (ww * cvec + NC - 1) / NC;  // at most 16
+        // log2 of vectors per group
+        const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
+        const int WS = wm + 16 / ES;  // row stride of the union in wx: the maxima, then a slot
+        bool whole = (ww * cvec) % NC == 0;  // every sampled chunk whole
+#pragma unroll
+        for (int q = 0; q < 8; ++q) whole = whole && (q >= ww || nvw[q] == cvec);
+        const bool perwarp = !HELD && ww == kNCW && whole;
+        uint32_t lm = 0u;  // the largest of this thread's group maxima
+        bool gotw;
+        if (perwarp) {
+            gotw = wait_bounded(&ctrl->full[warp], 0, ctrl);
+            if (lane == 0 && gotw) ctrl->observed[warp] = 1;
+            if (lane == 0)
+                for (int q = warp + kNCW; q < nq && q < p.stages; q += kNCW) issue(q);
+            if (gotw) {
+                const uint4* own = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(warp) * chunk_bytes);
+                lm = warm_maxima16_whole<KeyT>(own, lane, 32, VT, gsh, R, wx + crank * WS + tid * R);
+            }
+        } else {
+            const bool got0 = wait_bounded(&ctrl->full[0], 0, ctrl);
+            if (tid == 0 && got0) ctrl->observed[0] = 1;
+            if (lane == 0)
+                for (int q = warp < ww ? warp + kNCW : warp; q < nq && q < p.stages; q += kNCW) issue(q);
+            gotw = got0;
+            for (int q = 1; q < ww; ++q) {
+                const bool g = wait_bounded(&ctrl->full[q], 0, ctrl);
+                if (tid == 0 && g) ctrl->observed[q] = 1;
+                gotw = gotw && g;
+            }
         }
         {
             // group maxima: thread t owns vectors t, t + NC, ... of the sample (VT of them)
             // and splits them into R groups; a group's maximum is taken on the packed values
             // (NaNs ignored) and keyed once
-            const int R = wm / 256;
-            const int WS = wm + 16 / ES;  // row stride of the union in wx: the maxima, then a slot
-            const int VT = (ww * cvec + NC - 1) / NC;  // at most 16
-            // log2 of vectors per group
-            const int gsh = VT >= 16 * R ? 4 : (VT >= 8 * R ? 3 : (VT >= 4 * R ? 2 : (VT >= 2 * R ? 1 : 0)));
             const uint4* v0 = reinterpret_cast<const uint4*>(ring);
-            uint32_t lm = 0u;  // the largest of this thread's group maxima
-            bool whole = gotw && (ww * cvec) % NC == 0;  // every sampled chunk whole
-#pragma unroll
-            for (int q = 0; q < 8; ++q) whole = whole && (q >= ww || nvw[q] == cvec);
-            if (HELD || VT <= 8) {
+            if (perwarp) {
+                // (done above)
+            } else if (HELD || VT <= 8) {
                 uint32_t gk[4] = {0u, 0u, 0u, 0u};  // key of each group's maximum (0: none)
                 if (whole) {
                     if (HELD || VT <= 4) warm_maxima_whole<KeyT, 4>(v0, tid, VT, gsh, gk);
@@ -1151,7 +1169,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     }
                 }
             } else {
-                lm = whole ? warm_maxima16_whole<KeyT>(v0, tid, VT, gsh, R, wx + crank * WS + tid * R)
+                lm = whole ? warm_maxima16_whole<KeyT>(v0, tid, NC, VT, gsh, R, wx + crank * WS + tid * R)
                            : warm_maxima16<KeyT>(v0, tid, cvec, ww, VT, gsh, R, gotw, nvw, wx + crank * WS + tid * R);
             }
             if (!HELD) {  // (streamed rows bin the union below its largest maximum)
