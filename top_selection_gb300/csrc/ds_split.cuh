@@ -1097,6 +1097,12 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             }
         };
 
+        // the chunk loop's stepping (block and sub-chunk of this warp's first chunk, of
+        // kNCW chunks ahead and of one ring ahead), set up before the warm-up's waits
+        int bi0, sub0, d8, r8, dS, rS;
+        qdiv(warp, bi0, sub0);
+        qdiv(kNCW, d8, r8);
+        qdiv(p.stages, dS, rS);
         // ---- warm-up on the first ww chunks (all consumer warps) ----
         for (int b = tid; b < kBins; b += NC) hist[b] = 0u;  // the warm-up's histogram, while the sample lands
         const int cvec = chunk_bytes / 16;  // vectors per full chunk
@@ -1330,10 +1336,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             // ---- the chunks, one warp each (warp 0 takes chunk 0 too) ----
             // this warp's chunk q: ring stage s = q % stages and use q / stages, block index bi
             // and sub-chunk sub, stepped by kNCW chunks per round
-            int st = warp, use = 0, bi, sub, d8, r8, dS, rS;
-            qdiv(warp, bi, sub);
-            qdiv(kNCW, d8, r8);      // kNCW chunks ahead
-            qdiv(p.stages, dS, rS);  // one ring ahead
+            int st = warp, use = 0, bi = bi0, sub = sub0;
             for (int q = warp; q < nq; q += kNCW) {
                 int req = 0;
                 if (lane == 0) req = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
