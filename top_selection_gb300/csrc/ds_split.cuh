@@ -1282,11 +1282,15 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             uint32_t sedge = wedge0;
             if (HELD) {
                 if (spec_ok && wedge0 > 0u && ctrl->spec_b >= 0) {
-                    constexpr uint64_t BW = uint64_t(1) << (KW - kDigitBits);  // keys per bucket
-                    const uint64_t bc = ctrl->spec_c;
-                    const uint64_t r = static_cast<uint64_t>(p.spec_k) - ctrl->spec_above;  // 1 <= r <= bc
-                    const uint64_t top = (static_cast<uint64_t>(ctrl->spec_b) + 1u) * BW;      // one past the bucket
-                    const uint64_t down = (r * BW + bc - 1u) / bc;                            // 1 <= down <= BW
+                    constexpr uint32_t BW = 1u << (KW - kDigitBits);  // keys per bucket
+                    const uint32_t bc = ctrl->spec_c;
+                    const uint32_t r = static_cast<uint32_t>(p.spec_k) - ctrl->spec_above;  // 1 <= r <= bc
+                    const uint64_t top = (static_cast<uint64_t>(ctrl->spec_b) + 1u) * BW;  // one past the bucket
+                    // about r * BW / bc keys below the top, rounded up, within [1, BW]: an estimate
+                    // needs no exact quotient (a 64-bit integer division here cost every thread
+                    // several hundred cycles)
+                    const float q = __fdividef(static_cast<float>(r), static_cast<float>(bc)) * static_cast<float>(BW);
+                    const uint32_t down = min(BW, max(1u, static_cast<uint32_t>(ceilf(q))));
                     sedge = max(wedge0, static_cast<uint32_t>(top - down));
                 }
                 if (tid == 0) {
