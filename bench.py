@@ -20,6 +20,9 @@ step's input from pinned host memory (on a copy stream, into one of two device b
 so the next step's upload overlaps this step's call), runs ds_topk, and reads the
 results back; the timed region runs from the first upload to the last read-back.
 
+cold_call: one call alone, the stream idle and the L2 flushed just before it, CUDA events
+around that call (median of 5): what a caller pays for a single isolated call.
+
 --impl reference: the oracle (the CPU transcription of the method, oracle/) timed on
 this host's cores on a bounded sample of the same workload.
 
@@ -629,6 +632,27 @@ def run_gpu(args):
            "h2d_bytes_per_step": ROWS * STRIDE * sh.es, "d2h_bytes_per_step": ROWS * K_TOP * (sh.es + 4),
            "steps": e_steps}
 
+    # one call alone: the stream idle, L2 flushed by writing a buffer of twice its size just
+    # before, CUDA events around the single call (median of 5) -- launch, prologue and the
+    # input's first bytes are all on this clock, with no previous call to overlap
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    cold = []
+    for i in range(5):
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+            c0.record(stream)
+            call(i)
+            c1.record(stream)
+        stream.synchronize()
+        cold.append(c0.elapsed_time(c1))
+    cold_ms = max_over_ranks(statistics.median(cold), device=dev)
+    del flush
+    cold_call = {"us": round(cold_ms * 1e3, 3), "value": round(ws * step_bytes / (cold_ms * 1e-3) / 1e9, 2),
+                 "unit": "GB/s", "call": "one ds_topk call alone after an L2 flush, CUDA events around it "
+                                         "(median of 5)"}
+
     if rank != 0:
         if dist:
             dist.destroy_process_group()
@@ -653,6 +677,7 @@ def run_gpu(args):
         "hbm_frac_of_peak": round(value / ws / peak, 4),
         "roofline": roofline,
         "input_ready": input_ready,
+        "cold_call": cold_call,
         "cpu_baseline": cpu,
         "cpu_baseline_full_sort": cpu_sort,
         "e2e": e2e,
