@@ -209,6 +209,22 @@ def test_longctx_ascending_compactions_make_progress(seed):
     check_topk(w.x, w.dtype, 2048, v, i, N=w.N, threads=16)
 
 
+@pytest.mark.parametrize("shape,k", [("row65536", 512), ("row65536", 2048), ("indexer", 512), ("indexer", 2048)])
+@pytest.mark.parametrize("seed", [1, 0x5EED])
+def test_sorted_rows_held_whole_share_dense_passes(shape, k, seed):
+    """Rows held whole whose values ascend along the row: every chunk above the edge is a
+    dense pass (all its elements pass), several in one CTA on the single row, so warps
+    share passes out in slices, help from their waits and contend for the one open job."""
+    import top_selection_gb300 as ds
+    w = {"row65536": synth.row65536_f32, "indexer": synth.indexer_bf16}[shape]()
+    assert ds.ds_get_plan(w.dtype, w.rows, w.N, k, w.B, w.B2)["spec_k"] > 0  # held whole
+    x = w.x[:, : w.N]
+    xs = np.sort(synth.bf16_bits_to_f32(x) if w.dtype == synth.BF16 else x, axis=1)
+    xs = synth.f32_to_bf16_bits(xs) if w.dtype == synth.BF16 else np.ascontiguousarray(xs, dtype=np.float32)
+    v, i, _ = run_gpu(xs, w.dtype, k, w.B, w.B2, seed, N=w.N)
+    check_topk(xs, w.dtype, k, v, i, N=w.N, threads=16)
+
+
 # ---------------------------------------------------------------- hot sampled blocks -
 
 def _spikes_in_sampled_blocks(w, k, seed):

@@ -45,7 +45,8 @@ struct Ctrl {
     uint32_t warp_tot[2][32];    // team-scan scratch, two rows used alternately (2 x 16 words)
     uint32_t block_cnt[2][32];   // per-warp appends of the current block, by block parity
     int compact_req;             // split rows: a reservation did not fit the buffer
-    int done_warps;              // split rows: warps that have filtered all their chunks
+    int done_warps;              // split rows: warps that have filtered all their chunks, plus
+                                 //   kJobOpen while a dense pass is shared out (rows held whole)
     int fail_base;               // split rows: first slot of a reservation that did not fit
     uint64_t wbar;               // split rows: warm-up exchange of group maxima
     uint64_t xbar[2];            // split rows: final-select histogram exchange, by pass parity
@@ -68,6 +69,15 @@ struct Ctrl {
     uint32_t lmax;               // split rows: the largest of this CTA's warm-up group maxima
     int hshift;                  // split rows: the first final histogram's bins are 2^hshift keys wide,
     uint32_t hbase;              //   from key hbase up
+    const uint8_t* job_stage;    // split rows held whole, the shared dense pass: its chunk,
+    int job_on;                  //   the owner's lock,
+    int job_next;                //   the next slice to claim (kDenseSlices or more: none open),
+    int job_left;                //   slices not yet finished,
+    int job_cursor;              //   the next free slot of the pass's reservation,
+    int job_p0;                  //   the pass's first vector and the chunk's vectors,
+    int job_nvec;
+    uint32_t job_tb;             //   the compare bits and the chunk's first row column
+    uint32_t job_col0;
 };
 
 // Bounded wait on an mbarrier phase.  On expiry it records a timeout in the status word,

@@ -536,6 +536,151 @@ __device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t e
     }
 }
 
+// A dense pass of a row held whole may be shared out: slice s holds vectors 2s and 2s + 1 of
+// each lane (kDenseSlices slices cover a pass of 512 vectors).  Whoever claims a slice
+// compares it again, reserves its hits' slots from the pass's reservation and appends them
+// position by position; a lane's elements are neighbours in the row, so it counts runs of
+// one histogram bin (sorted or clustered rows) with one atomic per run.
+constexpr int kDenseSlices = 8;
+constexpr int kJobOpen = 1 << 16;  // added to Ctrl::done_warps while a dense pass is shared out
+
+template <typename KeyT>
+__device__ __forceinline__ void dense_slice(const uint8_t* stage, int p0, int nvec, int s, uint32_t tb, uint32_t col0,
+                                            KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int lane, uint32_t& tmax,
+                                            uint32_t* xh, uint32_t hedge, int hs) {
+    constexpr int ES = sizeof(KeyT);
+    constexpr int EPV = 16 / ES;
+    const uint4* vec = reinterpret_cast<const uint4*>(stage);
+    uint4 xv[2];
+    uint32_t mk[2], c = 0u;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int v = p0 + lane + 32 * (2 * s + t);
+        xv[t] = make_uint4(0u, 0u, 0u, 0u);
+        mk[t] = 0u;
+        if (v < nvec) {
+            xv[t] = vec[v];
+            if (ES == 2)  // element 2q at bit q, element 2q + 1 at bit 16 + q
+                mk[t] = (set_gtu_bf16x2(xv[t].x, tb) & 0x10001u) | (set_gtu_bf16x2(xv[t].y, tb) & 0x20002u) |
+                        (set_gtu_bf16x2(xv[t].z, tb) & 0x40004u) | (set_gtu_bf16x2(xv[t].w, tb) & 0x80008u);
+            else  // element q at bit q
+                mk[t] = (set_gtu_f32(xv[t].x, tb) & 1u) | (set_gtu_f32(xv[t].y, tb) & 2u) |
+                        (set_gtu_f32(xv[t].z, tb) & 4u) | (set_gtu_f32(xv[t].w, tb) & 8u);
+        }
+        c += static_cast<uint32_t>(__popc(mk[t]));
+    }
+    const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, c);
+    if (tot == 0u) return;
+    uint32_t run = 0u;
+    if (lane == 0) run = atomicAdd(reinterpret_cast<unsigned int*>(&ctrl->job_cursor), tot);
+    run = __shfl_sync(0xFFFFFFFFu, run, 0);
+    const uint32_t ltm = lanemask_lt();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int v = p0 + lane + 32 * (2 * s + t);
+        const uint32_t xw[4] = {xv[t].x, xv[t].y, xv[t].z, xv[t].w};
+        const uint32_t cb = col0 + static_cast<uint32_t>(v * EPV);  // row column of the vector's first element
+        uint32_t rb = 0u, rc = 0u;  // the current run's histogram bin and length
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+            const int bit = ES == 2 ? (e & 1) * 16 + (e >> 1) : e;
+            const uint32_t raw = ES == 2 ? ((e & 1) ? (xw[e >> 1] >> 16) : (xw[e >> 1] & 0xFFFFu)) : xw[e];
+            const bool hit = (mk[t] >> bit) & 1u;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, hit);
+            if (hit) {
+                const uint32_t slot = run + static_cast<uint32_t>(__popc(bal & ltm));
+                const uint32_t key = ES == 2 ? key_bf16(raw) : key_f32(raw);
+                ckey[slot] = static_cast<KeyT>(key);
+                cidx[slot] = cb + static_cast<uint32_t>(e);
+                tmax = max(tmax, key);
+                if (key >= hedge) {
+                    uint32_t b = (key - hedge) >> hs;
+                    b = b < kXBins - 1 ? b : kXBins - 1;
+                    if (rc != 0u && b != rb) {
+                        atomicAdd(&xh[rb >> 1], rc << ((rb & 1u) * 16u));
+                        rc = 0u;
+                    }
+                    rb = b;
+                    ++rc;
+                }
+            }
+            run += static_cast<uint32_t>(__popc(bal));
+        }
+        if (rc != 0u) atomicAdd(&xh[rb >> 1], rc << ((rb & 1u) * 16u));
+    }
+}
+
+// Claims and appends slices of the open dense pass until none is left; returns the largest
+// key this lane appended (0: none).  Never waits: a slice, once claimed, is finished by its
+// claimant.  Out of line: it runs rarely, and the chunk loop keeps its registers.
+template <typename KeyT>
+__device__ __noinline__ uint32_t dense_claim(KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int lane, uint32_t* xh,
+                                             uint32_t hedge, int hs) {
+    uint32_t mx = 0u;
+    while (true) {
+        int s = 0;
+        if (lane == 0) s = atomicAdd(&ctrl->job_next, 1);
+        s = __shfl_sync(0xFFFFFFFFu, s, 0);
+        if (s >= kDenseSlices) return mx;
+        __threadfence_block();
+        const volatile Ctrl* vc = ctrl;
+        dense_slice<KeyT>(vc->job_stage, vc->job_p0, vc->job_nvec, s, vc->job_tb, vc->job_col0, ckey, cidx, ctrl,
+                          lane, mx, xh, hedge, hs);
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            atomicSub(&ctrl->job_left, 1);
+        }
+    }
+}
+
+// The owner's side of a shared dense pass (slots [base, base + nbits) already reserved):
+// takes the job if no other is open, claims slices with the helpers and waits for theirs.
+// Returns 1 + the largest key this lane appended, or 0 when another job was open (the
+// caller then appends the pass alone).  Out of line, like dense_claim.
+template <typename KeyT>
+__device__ __noinline__ uint64_t dense_share(const uint8_t* stage, int p0, int nvec, uint32_t tb, uint32_t col0,
+                                             uint32_t base, KeyT* ckey, uint32_t* cidx, Ctrl* ctrl, int lane,
+                                             uint32_t* xh, uint32_t hedge, int hs) {
+    int own = 0;
+    if (lane == 0) own = atomicCAS(&ctrl->job_on, 0, 1) == 0;
+    if (!__shfl_sync(0xFFFFFFFFu, own, 0)) return 0u;
+    if (lane == 0) {
+        ctrl->job_stage = stage;
+        ctrl->job_p0 = p0;
+        ctrl->job_nvec = nvec;
+        ctrl->job_tb = tb;
+        ctrl->job_col0 = col0;
+        ctrl->job_cursor = static_cast<int>(base);
+        ctrl->job_left = kDenseSlices;
+        __threadfence_block();
+        atomicExch(&ctrl->job_next, 0);          // open
+        atomicAdd(&ctrl->done_warps, kJobOpen);  // (waiting warps look here)
+    }
+    __syncwarp();
+    const uint32_t mx = dense_claim<KeyT>(ckey, cidx, ctrl, lane, xh, hedge, hs);
+    const long long t0 = clock64();
+    while (true) {  // the slices other warps claimed
+        int left = 0;
+        if (lane == 0) left = *reinterpret_cast<volatile int*>(&ctrl->job_left);
+        if (__shfl_sync(0xFFFFFFFFu, left, 0) <= 0) break;
+        if (clock64() - t0 > kSpinLimit) {  // cannot happen: a claimed slice never waits
+            if (lane == 0) {
+                set_status(kErrTimeout);
+                *reinterpret_cast<volatile int*>(&ctrl->abort) = 1;
+            }
+            break;
+        }
+    }
+    __threadfence_block();
+    if (lane == 0) {
+        atomicSub(&ctrl->done_warps, kJobOpen);
+        *reinterpret_cast<volatile int*>(&ctrl->job_on) = 0;
+    }
+    __syncwarp();
+    return 1ull + mx;
+}
+
 // One warp filters vectors [0, nvec) of a staged chunk (plus, when tail_n > 0, the row's
 // last tail_n elements from global memory) against the compare bits tb and appends the
 // survivors.  Work goes in passes of 512 vectors (16 per lane, lane l taking l, l + 32,
@@ -551,9 +696,10 @@ __device__ __forceinline__ void xhist_add(uint32_t* xh, uint32_t key, uint32_t e
 // its run of the reserved index slots, then the warp walks the reserved slots together
 // (contiguous accesses) to store each hit's key and its row column.  Dense passes (a third
 // or more of the elements pass) skip the per-lane bit loop: the warp walks the pass's
-// element positions, one ballot each, and its lanes' hits take consecutive slots.  The
-// row's tail elements take the last slots.
-template <typename KeyT>
+// element positions, one ballot each, and its lanes' hits take consecutive slots; on rows
+// held whole (SHARE) the pass is shared out in slices with warps that have nothing to
+// filter (dense_share).  The row's tail elements take the last slots.
+template <typename KeyT, bool SHARE>
 __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint32_t col0, const char* xrow,
                                            int64_t tail_first, int tail_n, uint32_t tb, KeyT* ckey, uint32_t* cidx,
                                            Ctrl* ctrl, uint32_t cap, int lane, int& pass, uint32_t& tmax,
@@ -625,7 +771,12 @@ __device__ __forceinline__ bool warp_chunk(const uint8_t* stage, int nvec, uint3
         }
         if (!__shfl_sync(0xFFFFFFFFu, fits, 0)) return false;
         base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        if (nbits * 3u >= 512u * EPV) {
+        uint64_t shared = 0u;  // a dense pass of a row held whole, shared out when no other is
+        if (SHARE && nbits * 3u >= 512u * EPV)
+            shared = dense_share<KeyT>(stage, p0, nvec, tb, col0, base, ckey, cidx, ctrl, lane, xh, hedge, hs);
+        if (shared) {
+            tmax = max(tmax, static_cast<uint32_t>(shared - 1u));
+        } else if (nbits * 3u >= 512u * EPV) {
             // dense pass (a third or more of its elements pass): the warp writes its hits
             // position by position, lanes in order, to consecutive slots -- no per-lane bit
             // loop, no bank conflicts
@@ -985,6 +1136,7 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
         mbar_init(&ctrl->xbar[0], 1);
         mbar_init(&ctrl->xbar[1], 1);
         ctrl->fail_base = 0x7FFFFFFF;
+        ctrl->job_next = kDenseSlices;  // no dense pass open
         fence_mbar_init();
     }
     {  // this CTA's slot of the final select's first exchange round
@@ -1080,11 +1232,14 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
             const long long t0 = clock64();
             while (true) {
                 if (__all_sync(0xFFFFFFFFu, mbar_try_wait_sleep(bar, parity, 2000u))) return true;
-                int f = 0, a = 0;
+                int f = 0, a = 0, d = 0;
                 if (lane == 0) {
                     f = *reinterpret_cast<volatile int*>(&ctrl->compact_req);
                     a = *reinterpret_cast<volatile int*>(&ctrl->abort);
+                    if (HELD) d = *reinterpret_cast<volatile int*>(&ctrl->done_warps);
                 }
+                if (HELD && __shfl_sync(0xFFFFFFFFu, d, 0) >= kJobOpen)  // help with a shared dense pass
+                    tmax = max(tmax, dense_claim<KeyT>(ckey, cidx, ctrl, lane, xh0(), hedge, hs0));
                 if (__shfl_sync(0xFFFFFFFFu, a, 0)) return false;
                 if (__shfl_sync(0xFFFFFFFFu, f, 0)) join_compaction();
                 if (clock64() - t0 > kSpinLimit) {
@@ -1376,10 +1531,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     const int nvec = static_cast<int>(bytes / 16);
                     const int tail = static_cast<int>(ce - bytes / ES);
                     int pass = 0;
-                    while (!warp_chunk<KeyT>(ring + static_cast<size_t>(s) * chunk_bytes, nvec,
-                                             static_cast<uint32_t>(c0), xrow, c0 + bytes / ES, tail,
-                                             compare_bits<KeyT>(have, tk), ckey, cidx, ctrl, cap, lane, pass, tmax,
-                                             xh0(), hedge, hs0)) {
+                    while (!warp_chunk<KeyT, HELD>(ring + static_cast<size_t>(s) * chunk_bytes, nvec,
+                                                   static_cast<uint32_t>(c0), xrow, c0 + bytes / ES, tail,
+                                                   compare_bits<KeyT>(have, tk), ckey, cidx, ctrl, cap, lane, pass,
+                                                   tmax, xh0(), hedge, hs0)) {
                         join_compaction();
                         if (!have || T > tk) {
                             tk = T;
@@ -1444,6 +1599,10 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     }
                     d = __shfl_sync(0xFFFFFFFFu, d, 0);
                     f = __shfl_sync(0xFFFFFFFFu, f, 0);
+                    if (HELD && d >= kJobOpen) {  // help with a shared dense pass
+                        tmax = max(tmax, dense_claim<KeyT>(ckey, cidx, ctrl, lane, xh0(), hedge, hs0));
+                        d -= kJobOpen;
+                    }
                     if (f) {
                         join_compaction();
                         continue;
