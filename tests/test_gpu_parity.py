@@ -193,6 +193,21 @@ def test_workload_sampler_f32(k):
     _auto(synth.sampler_f32(), k)
 
 
+@pytest.mark.parametrize("k,ties", [(64, 3), (512, 8), (512, 40)])
+def test_sampler_rows_ties_at_the_kth_value(k, ties):
+    """Sampler rows (one CTA each) where `ties` more elements, the next ones below the k-th
+    largest value, are set to that value: the final select's pivot bin holds a few keys
+    (ranked in one warp when they number at most 32, counted in further passes
+    otherwise) with several copies of the pivot, of which exactly the quota is taken."""
+    w = synth.sampler_f32()
+    x = w.x[:, : w.N].copy()
+    for r in range(w.rows):
+        order = np.argsort(-x[r], kind="stable")
+        x[r, order[k: k + ties]] = x[r, order[k - 1]]
+    v, i, _ = run_gpu(x, w.dtype, k, w.B, w.B2, 0x5EED, N=w.N)
+    check_topk(x, w.dtype, k, v, i, N=w.N, threads=16)
+
+
 @pytest.mark.parametrize("kind", ["iid", "ascending", "levels"])
 @pytest.mark.parametrize("k", [512, 2048])
 def test_workload_longctx_bf16(kind, k):

@@ -1723,6 +1723,47 @@ __global__ void __launch_bounds__(kSplitThreads, 2) ds_split_kernel(const ScanPa
                     eq_mine = reinterpret_cast<const uint16_t*>(rows)[crank * kXBins + bstar];
                     break;
                 }
+                if (G == 1 && bstar < kXBins - 1 && reinterpret_cast<const uint16_t*>(rows)[bstar] <= 32u) {
+                    // one CTA and few keys in the bin: collect them and rank them in one warp
+                    // instead of counting further passes over the buffer
+                    const uint32_t blo = lbase + (static_cast<uint32_t>(bstar) << s);
+                    const uint64_t top = static_cast<uint64_t>(blo) + ((uint64_t(1) << s) - 1u);
+                    const uint32_t bhi = top < lhi ? static_cast<uint32_t>(top) : lhi;
+                    if (tid == 0) ctrl->fp_tot[8] = 0u;
+                    __syncthreads();
+                    for (int i = tid; i < n; i += NT) {
+                        const uint32_t kk = ckey[i];
+                        if (in_play(kk) && kk >= blo && kk <= bhi) {
+                            const uint32_t q = atomicAdd(&ctrl->fp_tot[8], 1u);
+                            if (q < 32u) hist[q] = kk;
+                        }
+                    }
+                    __syncthreads();
+                    if (warp == 0) {
+                        const uint32_t cnt = min(ctrl->fp_tot[8], 32u);
+                        const uint32_t mk = static_cast<uint32_t>(lane) < cnt ? hist[lane] : 0u;
+                        uint32_t gt = 0u, eq = 0u;  // keys of the bin above and equal to this lane's
+                        for (uint32_t j = 0; j < cnt; ++j) {
+                            const uint32_t o = __shfl_sync(0xFFFFFFFFu, mk, static_cast<int>(j));
+                            gt += o > mk ? 1u : 0u;
+                            eq += o == mk ? 1u : 0u;
+                        }
+                        const bool hold = static_cast<uint32_t>(lane) < cnt && gt < krem && krem <= gt + eq;
+                        const uint32_t hb = __ballot_sync(0xFFFFFFFFu, hold);
+                        if (hb == 0u && lane == 0) set_status(kErrInternal);  // (the bin holds the krem-th key)
+                        if (hb != 0u && lane == __ffs(hb) - 1) {
+                            ctrl->fp_tot[9] = mk;
+                            ctrl->fp_tot[10] = gt;
+                            ctrl->fp_tot[11] = eq;
+                        }
+                    }
+                    __syncthreads();
+                    pivot = ctrl->fp_tot[9];
+                    gt_all += ctrl->fp_tot[10];
+                    eq_lower = 0u;
+                    eq_mine = ctrl->fp_tot[11];
+                    break;
+                }
                 if (bstar < kXBins - 1) {
                     lbase += static_cast<uint32_t>(bstar) << s;
                     const uint64_t top = static_cast<uint64_t>(lbase) + ((uint64_t(1) << s) - 1u);
