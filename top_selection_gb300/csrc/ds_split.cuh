@@ -925,7 +925,7 @@ __device__ __noinline__ uint32_t split_compaction(KeyT* ckey, uint32_t* cidx, ui
     if (cb > 0 && keep <= static_cast<uint32_t>(k + (cap - k) / 2) &&
         keep + static_cast<uint32_t>(room) <= static_cast<uint32_t>(cap)) {
         const uint32_t lo = hedge + (static_cast<uint32_t>(cb) << hs0);
-        constexpr int PER = 4;
+        constexpr int PER = 8;  // (4: 2.2 us more per call on sampler rows at k = 4096; 16: slower on sorted rows)
         uint32_t off = 0u;
         for (int t0 = 0, it = 0; t0 < n; t0 += NC * PER, ++it) {
             KeyT kk[PER];
