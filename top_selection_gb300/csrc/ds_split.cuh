@@ -7,34 +7,38 @@
 // candidates.  This kernel keeps that structure and arranges the work for short critical
 // paths on sm_103a:
 //
-//   * Copies: 8 warps, no producer.  Stage s of an 8- or 16-stage ring of 1-D bulk copies
-//     belongs to warp s mod 8, which filters every chunk landing there (chunk q, in the
-//     part's Philox block order, goes to warp q mod 8) and issues the stage's next copy
-//     itself.  The warm-up's chunks are requested first, the rest once chunk 0 landed.
+//   * Parts and copies: part p of a row takes blocks p, p + P, p + 2P, ... in the order
+//     the row's Philox draws give them.  8 warps, no producer: stage s of an 8- or
+//     16-stage ring of 1-D bulk copies belongs to warp s mod 8, which filters every chunk
+//     landing there and issues the stage's next copy itself.  The warm-up's chunks are
+//     requested first, the rest once chunk 0 landed.  When every CTA can have an SM to
+//     itself, a part of up to 16 chunks of 8 KB is held whole in the SM's shared memory.
 //   * Warm-up (init window): the first ww chunks of every CTA are reduced to group
-//     maxima (the largest key of each group of consecutive vectors).  The CTAs exchange
-//     them with bulk copies into each other's shared memory, and every CTA derives the
-//     same threshold from the union: T sits just below the 2048-bin top-digit bucket
-//     (narrowed by 5 more bits for rows streamed through the ring) that holds the k-th
-//     largest group maximum.  At least k groups have a maximum at or above it, so at
-//     least k elements of the row are kept above T: every element at or below T is
-//     outside the top k (the threshold invariant of the deep dive's proof).
-//   * Filter: each warp filters its 8 KB chunks: lanes read 16-byte vectors and compare
-//     packed values against T with one instruction per word, a shuffle scan places the
-//     lanes' survivors, one shared atomic per warp reserves their slots, and the warp
-//     writes them in two steps (columns per lane, then keys and columns for the warp's
-//     slots in order), counting each key into the final select's first histogram.  On
-//     rows streamed through the ring, a warp raises T from that histogram each time the
-//     buffer passes a mark (just below the bin of the k-th largest appended key).  A
-//     reservation that does not fit makes every warp join a compaction of the CTA's
-//     buffer: a cut at the histogram bin of the k-th largest key where that frees
-//     enough room, else a RadixSelectTopK to exactly k; either raises T, and the warp
-//     then resumes where it stopped.
+//     maxima (the largest key of each group of consecutive vectors) and exchanged with
+//     bulk copies into each other's shared memory; every CTA derives the same edge from
+//     the union.  At least k groups have a maximum at or above the edge, so at least k
+//     elements of the row are kept above T = edge - 1: every element at or below T is
+//     outside the top k (the threshold invariant of the deep dive's proof).  Rows held
+//     whole take the edge from the 2048-bin top-digit bucket of the k-th largest maximum
+//     and may start from a speculative edge instead (the spec_k-th largest maximum,
+//     checked by the final select and redone from the proven edge when it fails); rows
+//     streamed through the ring bin the maxima below the union's largest.
+//   * Filter: each warp compares its chunk's packed values against T with one
+//     instruction per word, reserves its survivors' slots with one shared atomic and
+//     appends them -- sparse passes in two steps (columns per lane, then keys and columns
+//     for the warp's slots in order), dense passes position by position, shared out in
+//     slices with idle warps on rows held whole -- counting each key into the final
+//     select's first histogram.  On streamed rows a warp raises T from that histogram
+//     each time the buffer passes a mark.  A reservation that does not fit makes every
+//     warp join a compaction: a cut at the histogram bin of the k-th largest key where
+//     that frees enough room, else a RadixSelectTopK to exactly k; either raises T.
 //   * Final: the cluster selects the k largest keys of the union of its buffers by
 //     most-significant-digit radix passes over 512 bins.  Each pass, every CTA pushes
-//     its histogram to every other CTA; warp 0 of every CTA then finds the same pivot bin
-//     and every CTA's count above it, so each CTA writes its share of the output at
-//     offsets it computes itself, in one pass with two shared slot cursors.
+//     its histogram to every other CTA and the whole CTA finds the same pivot bin and
+//     every CTA's count above it, so each CTA writes its share of the output at offsets
+//     it computes itself, in one pass with two shared slot cursors.  A bin holding just
+//     the keys still needed is taken whole; on rows of one CTA a bin of at most 32 keys
+//     is ranked in one warp.
 //
 // The packed compare is "greater or unordered" against a float threshold chosen so that
 // every element whose key exceeds T passes (NaNs always pass, and -0 passes a -0
