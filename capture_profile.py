@@ -45,10 +45,11 @@ def _rows(text: str) -> list:
 
 
 def kernel_label(name: str) -> str:
-    """ds_split_kernel<unsigned short>(...) -> ds_split_kernel_u16."""
+    """[void] [dsk::]ds_split_kernel<unsigned short, ...>(...) -> ds_split_kernel_u16."""
     base = name.split("<")[0].split("(")[0].strip()
     if base.startswith("void "):
         base = base[5:]
+    base = base.split("::")[-1]  # (ncu shows some launches with the namespace)
     if "unsigned short" in name or "uint16" in name:
         return base + "_u16"
     if "unsigned int" in name or "uint32" in name:
